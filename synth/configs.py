@@ -1,0 +1,135 @@
+"""The five seeded synthetic workloads (shapes and value distributions).
+
+  tiny         H=256, E=16, top-2, F=64, T=4, Q4 (w = d*(q-8)), fp32 activations,
+               fp32 router ~ N(0, 0.02^2), no bias, no shared expert.
+  q2_layer     H=2560, E=512, top-10, F=640, Q2_0 blocks of 64, d ~ U[0.01, 0.04],
+               bf16 activations, bf16 router ~ N(0, 1/H) plus a Zipf(1.1) bias.
+  gemma_layer  H=2816, E=128, top-8, F=704, shared expert F=2112, Q4, d ~ U[0.005,
+               0.02], bf16 activations, bf16 router ~ N(0, 1/H) plus a Zipf(1.2) bias.
+  q2_stack     48 q2_layer layers (24,576 experts), per-layer Zipf(1.1) bias.
+  prefill      gemma_layer at T = 4096.
+
+The router weights ~ N(0, 1/H) make W_r x ~ N(0, 1) for x ~ N(0, 1), so the bias
+is "a Zipf per-expert bias added to N(0, 1) logits".
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import (bf16_bits_to_f64, expert_blobs, f32_to_bf16_bits, normal, sub_seed,
+               zipf_bias)
+
+Q4, Q2 = 0, 1
+
+
+@dataclass(frozen=True)
+class Config:
+    name: str
+    cid: int
+    kind: int
+    zero_point: int
+    H: int
+    E: int
+    K: int
+    F: int
+    F_shared: int
+    T: tuple
+    x_f32: bool
+    wr_f32: bool
+    wr_std: float
+    zipf_s: float | None
+    d_lo: float
+    d_hi: float
+    layers: int = 1
+    zipf_alpha: float = 1.0  # multiplies the Zipf bias (calibration knob)
+
+    @property
+    def seed(self) -> int:
+        return 0x4D4F45 ^ (self.cid << 8)
+
+    @property
+    def block_weights(self) -> int:
+        return 64 if self.kind == Q2 else 32
+
+    def matrix_blocks(self, F: int | None = None) -> int:
+        F = self.F if F is None else F
+        return self.H * F // self.block_weights
+
+    def expert_bytes(self, F: int | None = None) -> int:
+        return 3 * self.matrix_blocks(F) * 18
+
+    # stream tags (independent SplitMix64 streams per tensor)
+    def tag_router(self, layer: int) -> int:
+        return 1000 * layer + 1
+
+    def tag_bias(self, layer: int) -> int:
+        return 1000 * layer + 2
+
+    def tag_x(self, step: int) -> int:
+        return 500_000_000 + step
+
+    def tag_expert(self, layer: int, e: int) -> int:
+        return 1_000_000 + layer * self.E + e
+
+    def tag_shared(self, layer: int) -> int:
+        return 900_000_000 + layer
+
+
+_H2, _H3 = 2560, 2816
+CONFIGS = {
+    "tiny": Config("tiny", 0, Q4, 8, 256, 16, 2, 64, 0, (4,), True, True, 0.02, None,
+                   0.005, 0.02),
+    "q2_layer": Config("q2_layer", 1, Q2, 1, _H2, 512, 10, 640, 0, (1, 4), False, False,
+                       1 / math.sqrt(_H2), 1.1, 0.01, 0.04),
+    "gemma_layer": Config("gemma_layer", 2, Q4, 8, _H3, 128, 8, 704, 2112, (1, 2, 8), False,
+                          False, 1 / math.sqrt(_H3), 1.2, 0.005, 0.02),
+    "q2_stack": Config("q2_stack", 3, Q2, 1, _H2, 512, 10, 640, 0, (1, 4), False, False,
+                       1 / math.sqrt(_H2), 1.1, 0.01, 0.04, layers=48),
+    "prefill": Config("prefill", 4, Q4, 8, _H3, 128, 8, 704, 2112, (4096,), False, False,
+                      1 / math.sqrt(_H3), 1.2, 0.005, 0.02),
+}
+
+
+def router_weights(cfg: Config, layer: int = 0):
+    """Router weights [E][H]: fp32 array, or uint16 bf16 patterns when cfg.wr_f32 is False."""
+    w = normal(sub_seed(cfg.seed, cfg.tag_router(layer)), cfg.E * cfg.H, cfg.wr_std)
+    w = w.astype(np.float32).reshape(cfg.E, cfg.H)
+    return w if cfg.wr_f32 else f32_to_bf16_bits(w)
+
+
+def router_bias(cfg: Config, layer: int = 0):
+    if cfg.zipf_s is None:
+        return None
+    b = zipf_bias(sub_seed(cfg.seed, cfg.tag_bias(layer)), cfg.E, cfg.zipf_s)
+    return (b * np.float32(cfg.zipf_alpha)).astype(np.float32)
+
+
+def activations(cfg: Config, T: int, step: int = 0):
+    """x [T][H]: fp32 array, or uint16 bf16 patterns when cfg.x_f32 is False."""
+    x = normal(sub_seed(cfg.seed, cfg.tag_x(step)), T * cfg.H).astype(np.float32)
+    x = x.reshape(T, cfg.H)
+    return x if cfg.x_f32 else f32_to_bf16_bits(x)
+
+
+def as_f64(a) -> np.ndarray:
+    """fp64 values of a generated tensor (fp32 array or bf16 patterns)."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return bf16_bits_to_f64(a)
+    return a.astype(np.float64)
+
+
+def experts(cfg: Config, layer: int, ids) -> np.ndarray:
+    """Canonical blobs [len(ids)][expert_bytes] of the given experts of one layer."""
+    return expert_blobs(cfg.seed, [cfg.tag_expert(layer, int(e)) for e in ids],
+                        3 * cfg.matrix_blocks(), cfg.d_lo, cfg.d_hi)
+
+
+def shared_expert(cfg: Config, layer: int = 0):
+    if not cfg.F_shared:
+        return None
+    return expert_blobs(cfg.seed, [cfg.tag_shared(layer)], 3 * cfg.matrix_blocks(cfg.F_shared),
+                        cfg.d_lo, cfg.d_hi)[0]
