@@ -1,0 +1,347 @@
+#!/usr/bin/env python
+"""Benchmark: routed MoE FFN decode on one GB300 (or N replicas).
+
+Workload: the Q2_0 layer geometry (H=2560, 512 experts, top-10, F=640, blocks of
+64 weights, 1,382,400 bytes per expert) as 48 distinct layers (24,576 experts,
+33.97 GB resident in HBM), chained with RMSNorm and a residual add. A step is
+one decode token (T=1, or a T-token verify window) through all 48 layers:
+router GEMV, softmax top-k, bucketing, slot lookup, fused gate/up + SwiGLU,
+down projection and combine, per layer. Each step streams ~0.66 GB of expert
+weights plus 0.13 GB of router weights, far above the 129 MB L2, so nothing
+is served from cache across steps.
+
+metric: MoE-layer tokens/s (layers x tokens per second), with the expert-weight
+HBM GB/s and its fraction of the measured copy bandwidth in "roofline".
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (one layer-token per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth import configs as C  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (decode, Q2_0 layer H=2560 E=512 top-10 F=640)"
+UNIT = "layer-tokens/s"
+EPS = 1e-6
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--T", type=int, default=1, help="tokens per step (1 = decode, 4 = verify window)")
+    ap.add_argument("--layers", type=int, default=48)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+def workload_config(args, n_gpus):
+    return {"workload": f"q2_0 MoE decode: {args.layers} distinct layers of H=2560 E=512 top-10 F=640 "
+                        f"chained (RMSNorm + residual), T={args.T} tokens per step",
+            "T": args.T, "layers": args.layers, "H": 2560, "E": 512, "K": 10, "F": 640,
+            "format": "Q2_0 (64 weights + fp16 scale per 18 bytes)",
+            "global_batch": args.T * n_gpus, "parallelism": f"replicas x{n_gpus}",
+            "l2": "inputs larger than L2: each step streams ~0.79 GB of distinct weights (L2 129 MB)"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.4)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [r for (t, r) in self.rows if t0 - 0.15 <= t <= t1 + 0.15] or [r for _, r in self.rows]
+        sm = [float(r[0]) for r in rows if r and r[0].replace(".", "").isdigit()]
+        smax = [float(r[1]) for r in rows if len(r) > 1 and r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for i, n in enumerate(names):
+                if len(r) > 4 + i and r[4 + i].lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our path
+
+class Stack:
+    """48 (or n) resident Q2_0 layers loaded through the slot table."""
+
+    def __init__(self, L, torch, ctx, n_layers):
+        import synth.device as sdev
+        cfg = C.CONFIGS["q2_stack"]
+        self.cfg, self.L, self.torch = cfg, L, torch
+        self.eb = cfg.expert_bytes()
+        self.arena = L.moe_arena_create(ctx, self.eb * cfg.E * n_layers + (1 << 20))
+        self.slots = L.moe_slots_create(ctx, self.arena, n_layers, cfg.E, cfg.kind, cfg.zero_point,
+                                        cfg.H, cfg.F, cfg.E * n_layers)
+        staging = torch.empty(cfg.E * self.eb, dtype=torch.uint8, device="cuda")
+        nb = 3 * cfg.matrix_blocks()
+        self.Wr, self.bias, self.descs = [], [], []
+        for l in range(n_layers):
+            sdev.expert_blobs_into(staging, cfg.seed, cfg.tag_expert(l, 0), cfg.E, nb, cfg.d_lo, cfg.d_hi)
+            base = staging.data_ptr()
+            for e in range(cfg.E):
+                L.moe_slot_load(self.slots, l, e, base + e * self.eb, self.eb)
+            w = C.router_weights(cfg, l)
+            self.Wr.append(torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).cuda())
+            self.bias.append(torch.from_numpy(C.router_bias(cfg, l)).cuda())
+            self.descs.append(L.layer_desc(self.slots, l, cfg.H, cfg.E, cfg.K, cfg.F, self.Wr[l], self.bias[l]))
+        torch.cuda.synchronize()
+        del staging
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from quantized_expert_ffn_gb300 import _lib as L
+
+    torch.cuda.set_device(local_rank)
+    ctx = L.moe_ctx_create(local_rank)
+    st = Stack(L, torch, ctx, args.layers)
+    cfg = st.cfg
+    T = args.T
+    ws = torch.empty(L.moe_layer_workspace(st.descs[0], T) + T * cfg.H * 4 + 4096, dtype=torch.uint8,
+                     device="cuda")
+    x0 = C.as_f64(C.activations(cfg, T, step=rank)).astype(np.float32)
+    resid = torch.from_numpy(x0.copy()).cuda()
+    stream = torch.cuda.Stream()
+    # one eager pass (also checks status), then capture the whole step in a graph
+    with torch.cuda.stream(stream):
+        L.moe_stack_forward(ctx, st.descs, resid, EPS, ws)
+    stream.synchronize()
+    assert L.moe_status(ctx, stream) == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        L.moe_stack_forward(ctx, st.descs, resid, EPS, ws)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = ev0.elapsed_time(ev1)
+    clocks = sampler.stop(t0, t1) if rank == 0 else None
+    status = L.moe_status(ctx, stream)
+
+    # per-layer roofline: eager layer-by-layer pass with events on the launching stream
+    layer_ms = []
+    with torch.cuda.stream(stream):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.layers + 1)]
+        for rep in range(3):
+            evs[0].record(stream)
+            for l in range(args.layers):
+                L.moe_stack_forward(ctx, [st.descs[l]], resid, EPS, ws)
+                evs[l + 1].record(stream)
+            stream.synchronize()
+            layer_ms.append([evs[l].elapsed_time(evs[l + 1]) for l in range(args.layers)])
+    layer_ms = float(np.mean(layer_ms))
+
+    # end to end through the host-buffer entry point: H2D + 48 layers + D2H every step
+    resid_h = torch.from_numpy(x0.copy()).pin_memory()
+    e2e_steps = max(20, args.steps // 4)
+    for _ in range(3):
+        L.moe_stack_forward_host(ctx, st.descs, resid_h, EPS, ws, stream=stream)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        L.moe_stack_forward_host(ctx, st.descs, resid_h, EPS, ws, stream=stream)
+    e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    times = torch.tensor([ms, e2e_ms], device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
+    ms, e2e_ms_max = float(times[0]), float(times[1])
+    return dict(ms=ms, e2e_ms=e2e_ms_max, layer_ms=layer_ms, clocks=clocks, status=status, cfg=cfg)
+
+
+# ------------------------------------------------------------------ oracle (CPU)
+
+def oracle_sample_rate(seconds: float, T: int = 1, max_steps: int | None = None):
+    """Time the fp64 oracle on layer-tokens of the same workload (one layer and
+    one T-token window per sample), for about `seconds` of CPU work."""
+    import oracle
+    cfg = C.CONFIGS["q2_stack"]
+    oracle.build()
+    done, busy, l = 0, 0.0, 0
+    while busy < seconds and (max_steps is None or done < max_steps):
+        layer = l % cfg.layers
+        Wr = C.as_f64(C.router_weights(cfg, layer))
+        b = C.router_bias(cfg, layer).astype(np.float64)
+        x = oracle.rmsnorm(C.as_f64(C.activations(cfg, T, step=1000 + l)), EPS)
+        t0 = time.perf_counter()
+        lg = oracle.router_logits(x, Wr, b)
+        ids, _, _ = oracle.topk(lg, cfg.K)
+        t1 = time.perf_counter()
+        need = np.unique(ids)  # the inputs the oracle reads: generated outside the timing
+        blobs = C.experts(cfg, layer, need)
+        experts = [None] * cfg.E
+        for i, e in enumerate(need):
+            experts[int(e)] = blobs[i]
+        t2 = time.perf_counter()
+        oracle.layer_forward(cfg.kind, cfg.zero_point, cfg.H, cfg.E, cfg.K, cfg.F, None, None, experts, x,
+                             logits_in=lg)
+        t3 = time.perf_counter()
+        busy += (t1 - t0) + (t3 - t2)
+        done += 1
+        l += 1
+    return done * T / busy, done, busy
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    n_gpus = max(world, 1)
+    cfgj = workload_config(args, n_gpus)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        warm = min(args.warmup, 1)
+        if warm:
+            oracle_sample_rate(0.0, args.T, max_steps=1)
+        rate, done, busy = oracle_sample_rate(1e9, args.T, max_steps=args.steps)
+        line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": n_gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": busy / max(done, 1) * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": cfgj,
+                "cpu_baseline": {"kind": "oracle", "value": rate, "unit": UNIT, "cores": 1,
+                                 "sample": f"{done} layer-steps of one {args.T}-token window each "
+                                           f"(router, top-k, experts, combine; fp64, one thread)"},
+                "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    r = run_ours(args, rank, world, local_rank)
+    cfg = r["cfg"]
+    T = args.T
+    layer_tokens = args.layers * T
+    value = n_gpus * layer_tokens * args.steps / (r["ms"] / 1e3)
+    e2e_value = n_gpus * layer_tokens / (r["e2e_ms"] / 1e3)
+    pk = peaks()
+    hbm_peak = pk["hbm_gbs"] if pk else 6800.0
+    expert_bytes = cfg.expert_bytes()
+    router_bytes = cfg.E * cfg.H * 2
+    # algorithmic bytes of one layer call at T=1: K distinct experts + the router matrix
+    # (for T > 1 the distinct experts per layer vary; K*T is their upper bound)
+    layer_bytes = cfg.K * T * expert_bytes + router_bytes
+    graph_layer_ms = r["ms"] / args.steps / args.layers
+    achieved = layer_bytes / (graph_layer_ms / 1e3) / 1e9
+    step_expert_gbs = args.layers * cfg.K * expert_bytes / (r["ms"] / args.steps / 1e3) / 1e9
+    launches_per_layer = 8  # rmsnorm, router, top-k, bucket, plan, gate/up, down, combine
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": n_gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 mma / fp32 accumulate (Q2_0 weights)",
+        "data": "synthetic", "config": cfgj,
+        "stack_tokens_per_s": n_gpus * T * args.steps / (r["ms"] / 1e3),
+        "expert_weight_gbs": step_expert_gbs if T == 1 else None,
+        "expert_weight_frac_of_hbm": (step_expert_gbs / hbm_peak) if T == 1 else None,
+        "eager_layer_ms": r["layer_ms"],
+        "roofline": {"kernel": "one MoE layer call (8 launches, in the captured step graph)",
+                     "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "peak_source": "measured" if pk else "fallback",
+                     "algorithmic_bytes_per_launch": layer_bytes},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * cfg.H * 4,
+                "d2h_bytes_per_step": T * cfg.H * 4},
+        "gpu_launches": launches_per_layer * args.layers * args.steps,
+        "clocks": r["clocks"],
+        "device_status": r["status"],
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, done, busy = oracle_sample_rate(10.0, T)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{done} layer-steps ({T}-token windows) of the same layers, "
+                                          f"{busy:.1f} s of fp64 single-thread work"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

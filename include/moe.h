@@ -1,0 +1,256 @@
+/*
+ * moe.h -- C ABI of the routed mixture-of-experts FFN layer for one GB300 (sm_103a).
+ *
+ * The layer, per token t of a window of T tokens (Krasis white paper, sec. 5.3
+ * "Per-token routed expert execution"; kairos-engine README, "The MoE forward"):
+ *
+ *   logits[t][e] = sum_h Wr[e][h] * x[t][h] (+ bias[e])           router GEMV
+ *   ids[t][0..K), w[t][0..K) = top-K of logits[t], ties to the lower id;
+ *       w = softmax over all E logits, renormalised over the K chosen
+ *   buckets: the T*K (token, rank) pairs grouped by expert (expert-major)
+ *   per chosen expert e: h = SwiGLU(Wg[e] x, Wu[e] x), y_e = Wd[e] h,
+ *       with Wg, Wu, Wd block-quantised and dequantised on the fly
+ *   y[t] = sum_{k=0}^{K-1} w[t][k] * y_{ids[t][k]}(x[t])   (fixed k order)
+ *          + shared(x[t])                                 (optional shared expert)
+ *
+ * Weights live in a device arena. A flat slot table indexed by (layer, expert)
+ * gives each expert's arena slot, or -1 when it is not resident; the kernels
+ * read the table on the device, so a captured CUDA graph keeps working when
+ * experts move (Krasis white paper, sec. 5.3).
+ *
+ * Conventions for every function:
+ *   - Return MOE_OK (0) or a negative MOE_ERR_* code. Argument and shape errors
+ *     are detected on the host, before anything is enqueued; the message is then
+ *     available from moe_last_error() (thread-local).
+ *   - Pointers to tensors are DEVICE pointers unless the name or comment says
+ *     host. The caller owns every tensor; the library owns the opaque handles.
+ *   - All GPU work is enqueued on the caller's stream (moe_stream_t is the CUDA
+ *     runtime's cudaStream_t; 0 is the legacy default stream) with no host
+ *     synchronisation, so the compute calls can be captured in a CUDA graph.
+ *     Exceptions, stated per function: moe_slot_load with a pageable host blob,
+ *     moe_status (synchronises the stream), and the create/destroy calls.
+ *   - Conditions found on the device (absent expert, non-finite logit, bounds,
+ *     timeout) never trap: the kernel records a MOE_STATUS_* bit in the
+ *     context's status word, the affected contribution is zero, and the caller
+ *     reads the bits with moe_status().
+ *   - There is no CPU fallback. Every call runs on the GPU of its context.
+ *   - Row-major everywhere. x [T][H], logits [T][E], ids/w [T][K], y [T][H].
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* same type as cudaStream_t */
+typedef struct moe_ctx moe_ctx;
+typedef struct moe_arena moe_arena;
+typedef struct moe_slots moe_slots;
+
+/* return codes */
+#define MOE_OK 0
+#define MOE_ERR_ARG (-1)          /* null pointer, bad enum, negative size */
+#define MOE_ERR_SHAPE (-2)        /* dimensions the kernels do not support */
+#define MOE_ERR_UNSUPPORTED (-3)  /* valid request with no implementation */
+#define MOE_ERR_CUDA (-4)         /* a CUDA runtime call failed */
+#define MOE_ERR_NOMEM (-5)        /* device allocation, arena or slot pool full */
+#define MOE_ERR_EXPERT_ABSENT (-6)
+#define MOE_ERR_NONFINITE (-7)
+#define MOE_ERR_TIMEOUT (-8)
+#define MOE_ERR_BOUNDS (-9)
+#define MOE_ERR_WORKSPACE (-10)   /* ws_bytes below moe_layer_workspace() */
+
+/* device status bits (moe_status) */
+#define MOE_STATUS_EXPERT_ABSENT 1u /* a routed expert had no slot: it added 0 */
+#define MOE_STATUS_NONFINITE 2u     /* a router logit was NaN or +-inf */
+#define MOE_STATUS_TIMEOUT 4u       /* a bounded device wait gave up */
+#define MOE_STATUS_BOUNDS 8u        /* an index failed a device range check */
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Block formats. Every block is 18 bytes in the canonical (caller-facing) form:
+ * an fp16 scale d (2 bytes, little-endian) then 16 bytes of codes q.
+ *   MOE_Q2_64: 64 weights of 2 bits; code n in bits 2(n%4)..2(n%4)+1 of code
+ *              byte n/4 ("Strata in the source", sections "The byte budget, in
+ *              code" and "The CPU kernels").
+ *   MOE_Q4_32: 32 weights of 4 bits; code n in bits 4(n%2)..4(n%2)+3 of code
+ *              byte n/2.
+ * Weight value: d * (q - zero_point). The Strata article's Q2_0 reads codes
+ * {0,1,2,3} as {-1,0,1,2} (zero_point 1); zero_point 2 gives {-2,-1,0,1}. Q4
+ * uses zero_point 8. Allowed: 0..3 for Q2, 0..15 for Q4. */
+typedef enum { MOE_Q4_32 = 0, MOE_Q2_64 = 1 } moe_quant;
+
+typedef struct {
+    int kind;       /* moe_quant */
+    int zero_point; /* subtracted from every code */
+} moe_format;
+
+typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_GEGLU_TANH = 1 } moe_act;
+
+/* ------------------------------------------------------------ context */
+
+/* Create a context on CUDA device `device` (made current for the call). The
+ * context owns the device status word. Not thread-safe to share between threads
+ * that enqueue concurrently on different streams (the status word is shared). */
+MOE_API int moe_ctx_create(int device, moe_ctx **out);
+MOE_API int moe_ctx_destroy(moe_ctx *ctx);
+
+/* Synchronise `stream`, then read and clear the device status bits into *bits.
+ * Returns MOE_OK even when bits are set; the caller inspects them. */
+MOE_API int moe_status(moe_ctx *ctx, moe_stream_t stream, uint32_t *bits);
+
+/* Text of the last error raised on this thread ("" if none). */
+MOE_API const char *moe_last_error(void);
+
+/* Bytes of one expert blob (gate [F][H], up [F][H], down [H][F]; canonical and
+ * device forms have the same size): 3*H*F / weights_per_block * 18.
+ * ("Strata in the source", "The byte budget, in code": 1,382,400 bytes for
+ * H=2560, F=640 in Q2_0.) H and F must be positive multiples of 64. */
+MOE_API int moe_expert_bytes(moe_format fmt, int H, int F, size_t *out);
+
+/* ------------------------------------------------------------ arena and slots */
+
+/* One device allocation of `bytes` from which slot pools are carved. */
+MOE_API int moe_arena_create(moe_ctx *ctx, size_t bytes, moe_arena **out);
+MOE_API int moe_arena_destroy(moe_arena *arena);
+
+/* A slot table for n_layers x n_experts experts of one shape (H, F) and format,
+ * with `capacity` resident slots carved from `arena` (each slot holds one
+ * expert in the device layout, rounded up to 256 bytes). Every table entry
+ * starts at -1 (absent). Fails with MOE_ERR_NOMEM if the arena lacks room. */
+MOE_API int moe_slots_create(moe_ctx *ctx, moe_arena *arena, int n_layers, int n_experts,
+                     moe_format fmt, int H, int F, int capacity, moe_slots **out);
+MOE_API int moe_slots_destroy(moe_slots *slots);
+
+/* Make expert (layer, expert) resident. `blob` is the canonical blob of
+ * moe_expert_bytes() bytes, host or device memory (nbytes must equal that
+ * size). The blob is copied (host blobs through a device staging buffer owned
+ * by `slots`), rewritten into the device layout in a free slot (or the slot the
+ * expert already has), and only then is the table entry written, in stream
+ * order, so no kernel can see the entry before the weights are in place. With a pageable host blob the
+ * copy is synchronous with respect to the host; with a pinned or device blob
+ * nothing blocks. The blob may be reused as soon as the call returns for
+ * pageable memory, and after the stream reaches this point otherwise.
+ * MOE_ERR_NOMEM if no slot is free. */
+MOE_API int moe_slot_load(moe_slots *slots, int layer, int expert, const void *blob, size_t nbytes,
+                  moe_stream_t stream);
+
+/* Mark (layer, expert) absent (table entry -1, in stream order) and return its
+ * slot to the free pool. A no-op for an absent expert. Work enqueued earlier on
+ * `stream` still sees the old entry; work on other streams must be ordered by
+ * the caller. */
+MOE_API int moe_slot_evict(moe_slots *slots, int layer, int expert, moe_stream_t stream);
+
+/* Host-side view of the table: the slot index of (layer, expert), or -1. */
+MOE_API int moe_slot_lookup(const moe_slots *slots, int layer, int expert, int32_t *slot_out);
+
+/* ------------------------------------------------------------ the steps */
+
+/* Router GEMV and top-K (steps 1-2 above). x [T][H] (xt F32 or BF16); Wr [E][H]
+ * (wt F32 or BF16); bias [E] f32 or NULL. Outputs ids [T][K] in rank order
+ * (larger logit first, equal logits to the lower id; NaN ranks last and sets
+ * MOE_STATUS_NONFINITE, as does +-inf) and w [T][K] f32 (softmax renormalised
+ * over the K chosen; NaN for a token with a non-finite logit). logits_out
+ * [T][E] f32 receives the logits and is required. Logits accumulate in fp32. 1 <= K <= min(E, 32),
+ * E <= 4096, H % 8 == 0. */
+MOE_API int moe_router_topk(moe_ctx *ctx, const void *x, moe_dtype xt, int T, int H, const void *Wr,
+                    moe_dtype wt, const float *bias, int E, int K, float *logits_out,
+                    int32_t *ids, float *w, moe_stream_t stream);
+
+/* Stable counting sort of the T*K pairs p = t*K + k by expert ids[p] (kairos
+ * README, "The MoE forward": the batch is bucketed by expert). counts [E];
+ * offsets [E+1] (exclusive prefix sum, offsets[E] = T*K); perm [T*K] lists the
+ * pairs of expert 0, then expert 1, ..., each in increasing p; active [E] lists
+ * the experts with count > 0 in increasing order, *n_active (device int) their
+ * number. Integer results are exact. ids outside [0, E) set MOE_STATUS_BOUNDS
+ * and are left out of every bucket. */
+MOE_API int moe_bucket(moe_ctx *ctx, const int32_t *ids, int T, int K, int E, int32_t *counts,
+               int32_t *offsets, int32_t *perm, int32_t *active, int32_t *n_active,
+               moe_stream_t stream);
+
+/* Bytes of workspace moe_expert_ffn / moe_layer_forward / moe_stack_forward need
+ * for up to T_max tokens with this layer description (below). */
+typedef struct {
+    const moe_slots *slots;  /* routed experts, table of n_layers x E */
+    int layer;               /* which layer of `slots` */
+    int H, E, K, F;          /* hidden, experts, top-K, expert FFN width */
+    const void *Wr;          /* router weights [E][H] (device) */
+    moe_dtype wr_dtype;
+    const float *bias;       /* router bias [E] or NULL */
+    const moe_slots *shared; /* shared expert (layer `layer`, expert 0) or NULL */
+    int F_shared;            /* its FFN width */
+    int act;                 /* moe_act */
+} moe_layer_desc;
+
+MOE_API int moe_layer_workspace(const moe_layer_desc *desc, int T_max, size_t *bytes);
+
+/* Expert part of the layer (steps 4-6): with the routing (ids, w) and buckets
+ * (offsets, perm from moe_bucket over the same ids) given, computes
+ *   y[t] = sum_k w[t][k] * expert_{ids[t][k]}(x[t]) (+ shared(x[t]))
+ * with the layer description's slots (desc->Wr and bias are not read). Pairs
+ * with w == 0 do no expert work and add nothing. ws: device workspace of at
+ * least moe_layer_workspace(desc, T) bytes, 256-byte aligned. */
+MOE_API int moe_expert_ffn(moe_ctx *ctx, const moe_layer_desc *desc, const void *x, moe_dtype xt, int T,
+                   const int32_t *ids, const float *w, const int32_t *offsets,
+                   const int32_t *perm, float *y, void *ws, size_t ws_bytes,
+                   moe_stream_t stream);
+
+/* The whole layer: router, top-K, buckets, experts, combine. y [T][H] f32.
+ * logits_out [T][E] and ids_out [T][K] may be NULL. Deterministic: the same
+ * inputs give the same bits, and token t's result does not depend on the other
+ * tokens of the window or on T (Strata article, "Drafting and verifying": a
+ * multi-token pass does per token what the single-token pass does). */
+MOE_API int moe_layer_forward(moe_ctx *ctx, const moe_layer_desc *desc, const void *x, moe_dtype xt,
+                      int T, float *y, float *logits_out, int32_t *ids_out, void *ws,
+                      size_t ws_bytes, moe_stream_t stream);
+
+/* Same, with x [T][H] and y [T][H] in HOST memory (pinned for asynchronous
+ * copies): x is copied into the workspace, the layer runs, y is copied back, all
+ * on `stream`. The host buffers must stay valid until the stream reaches the
+ * end of the call. Needs moe_layer_workspace() + T*H*(4 + element size of xt)
+ * bytes (rounded up to 256 each). */
+MOE_API int moe_layer_forward_host(moe_ctx *ctx, const moe_layer_desc *desc, const void *x_host,
+                           moe_dtype xt, int T, float *y_host, void *ws, size_t ws_bytes,
+                           moe_stream_t stream);
+
+/* A chain of n_layers MoE layers over a residual stream (one decode step of an
+ * expert stack): for l in 0..n_layers-1:
+ *   u = bf16(RMSNorm(resid))   (weightless, eps; kairos README "normalise")
+ *   resid += layer_l(u)
+ * resid [T][H] f32 is updated in place. trace_in [n_layers][T][H] bf16 and
+ * trace_logits [n_layers][T][E] f32 may be NULL; when given they receive each
+ * layer's input and router logits (for per-layer checks). All layers must share
+ * H, E, K, F and the router dtype. */
+MOE_API int moe_stack_forward(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers, float *resid,
+                      int T, float eps, void *trace_in, float *trace_logits, void *ws,
+                      size_t ws_bytes, moe_stream_t stream);
+
+/* Same chain with resid [T][H] f32 in HOST memory (pinned for asynchronous
+ * copies): copied into the workspace, run through the n_layers layers, copied
+ * back, all on `stream`. Needs moe_layer_workspace() + T*H*4 (rounded up to
+ * 256) bytes. The host buffer must stay valid until the stream reaches the end
+ * of the call. */
+MOE_API int moe_stack_forward_host(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers,
+                                   float *resid_host, int T, float eps, void *ws, size_t ws_bytes,
+                                   moe_stream_t stream);
+
+/* Weightless RMSNorm with bf16 output: out[t][h] = bf16(x[t][h] / sqrt(mean_h
+ * x[t][h]^2 + eps)), x f32. H % 8 == 0. */
+MOE_API int moe_rmsnorm_bf16(moe_ctx *ctx, const float *x, int T, int H, float eps, void *out,
+                     moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,212 @@
+// bucket.cu -- expert-major bucketing of the (token, rank) pairs and the plan of
+// expert work groups built from the buckets.
+//
+// kairos-engine README, "The MoE forward": the expert loop buckets the whole
+// batch by expert, then runs each expert once over every token that chose it.
+// Strata article, "The plan: three destinations per expert": a verify window's
+// routed ids are deduplicated, so an expert chosen by two tokens is computed once
+// for both. Both follow from one stable counting sort.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kBucketThreads = 1024;
+
+// Block-wide exclusive scan of one int per thread; returns the prefix and writes
+// the block total to *total. All threads of the block must call it.
+__device__ int block_exclusive_scan(int v, int *total, int *scratch /* >= 33 ints */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += n;
+    }
+    if (lane == 31) scratch[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int s = lane < nw ? scratch[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += n;
+        }
+        if (lane < nw) scratch[lane] = s;  // inclusive per-warp totals
+        if (lane == 31) scratch[32] = s;
+    }
+    __syncthreads();
+    const int warp_base = warp > 0 ? scratch[warp - 1] : 0;
+    *total = scratch[32];
+    __syncthreads();
+    return warp_base + inc - v;
+}
+
+// One CTA of 1024 threads. Counting pass (order-free), exclusive scan, then the
+// stable placement: pairs are placed in chunks of 1024 in pair order; inside a
+// chunk a pair's rank among equal experts = (count in earlier warps) + (count in
+// earlier lanes of its warp), so perm lists each expert's pairs in increasing p.
+__global__ void __launch_bounds__(kBucketThreads) k_bucket(const int32_t *__restrict__ ids, int P, int E,
+                                                           int32_t *counts, int32_t *offsets, int32_t *perm,
+                                                           int32_t *active, int32_t *n_active,
+                                                           uint32_t *status) {
+    extern __shared__ int sm[];
+    int *cnt = sm;              // [E]
+    int *base = cnt + E;        // [E] running placement base
+    int *wt = base + E;         // [32][E] per-warp counts of the current chunk
+    int *scr = wt + 32 * E;     // [64] scan scratch
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    bool oob = false;
+    for (int p = tid; p < P; p += blockDim.x) {
+        const int e = ids[p];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        else oob = true;
+    }
+    if (__syncthreads_or(oob) && tid == 0) set_status(status, MOE_STATUS_BOUNDS);
+    // exclusive scan of counts over E (E <= 1024 = one element per thread)
+    {
+        const int c = tid < E ? cnt[tid] : 0;
+        int total;
+        const int pre = block_exclusive_scan(c, &total, scr);
+        if (tid < E) {
+            counts[tid] = c;
+            offsets[tid] = pre;
+            base[tid] = pre;
+        }
+        if (tid == 0) offsets[E] = total;
+        const int act = (tid < E && c > 0) ? 1 : 0;
+        int nact;
+        const int apos = block_exclusive_scan(act, &nact, scr);
+        if (act) active[apos] = tid;
+        if (tid == 0) *n_active = nact;
+    }
+    __syncthreads();
+    for (int c0 = 0; c0 < P; c0 += blockDim.x) {
+        for (int i = tid; i < 32 * E; i += blockDim.x) wt[i] = 0;
+        __syncthreads();
+        const int p = c0 + tid;
+        int e = p < P ? ids[p] : -1;
+        if (e >= E) e = -1;
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & ((1u << lane) - 1));
+        if (e >= 0 && rank == 0) wt[warp * E + e] = __popc(same);
+        __syncthreads();
+        for (int ee = tid; ee < E; ee += blockDim.x) {
+            int run = base[ee];
+            for (int w = 0; w < 32; ++w) {
+                const int c = wt[w * E + ee];
+                wt[w * E + ee] = run;
+                run += c;
+            }
+            base[ee] = run;
+        }
+        __syncthreads();
+        if (e >= 0) perm[wt[warp * E + e] + rank] = p;
+        __syncthreads();
+    }
+}
+
+// Plan: live pairs (weight != 0 and the expert resident) in bucket order form
+// the column list; each expert's live pairs are cut into groups of at most
+// nc_gu (gate/up) and nc_d (down) columns. Shared-expert groups cover all T
+// tokens and sit after the routed groups' maximum count.
+__global__ void __launch_bounds__(kBucketThreads) k_plan(PlanArgs a) {
+    extern __shared__ int sm[];
+    const int tid = threadIdx.x;
+    const int P = a.T * a.K, E = a.E;
+    int *lc = sm;          // [E] live count per expert
+    int *cstart = lc + E;  // [E]
+    int *scr = cstart + E; // [64]
+    bool absent = false, oob = false;
+    int running = 0;
+    for (int p = tid; p < P; p += blockDim.x) a.live[p] = 0;
+    __syncthreads();
+    const int nb = a.offsets[E];  // pairs with an id in range (the rest were left out)
+    for (int c0 = 0; c0 < nb; c0 += blockDim.x) {
+        const int i = c0 + tid;
+        int live = 0, p = -1;
+        if (i < nb) {
+            p = a.perm[i];
+            const int e = a.ids[p];
+            if (e >= 0 && e < E) {
+                const int slot = a.table[(size_t)a.layer * E + e];
+                if (slot < 0) absent = true;
+                else if (slot >= a.capacity) oob = true;
+                else live = a.w[p] != 0.f;
+            } else {
+                oob = true;
+            }
+            a.live[p] = live;
+        }
+        int tot;
+        const int pos = block_exclusive_scan(live, &tot, scr);
+        if (live) a.cols[running + pos] = p;
+        running += tot;
+    }
+    const int nlive = running;
+    if (__syncthreads_or(absent) && tid == 0) set_status(a.status, MOE_STATUS_EXPERT_ABSENT);
+    if (__syncthreads_or(oob) && tid == 0) set_status(a.status, MOE_STATUS_BOUNDS);
+    // live count per expert (its pairs are offsets[e]..offsets[e+1] of perm)
+    int my_lc = 0;
+    if (tid < E) {
+        for (int i = a.offsets[tid]; i < a.offsets[tid + 1]; ++i) my_lc += a.live[a.perm[i]];
+        lc[tid] = my_lc;
+    }
+    int dummy;
+    const int my_cs = block_exclusive_scan(tid < E ? my_lc : 0, &dummy, scr);
+    if (tid < E) cstart[tid] = my_cs;
+    __syncthreads();
+    // groups
+    const int ng_gu = tid < E ? (my_lc + a.nc_gu - 1) / a.nc_gu : 0;
+    const int ng_d = tid < E ? (my_lc + a.nc_d - 1) / a.nc_d : 0;
+    int tot_gu, tot_d;
+    const int gb_gu = block_exclusive_scan(ng_gu, &tot_gu, scr);
+    const int gb_d = block_exclusive_scan(ng_d, &tot_d, scr);
+    if (tid < E && my_lc > 0) {
+        const int slot = a.table[(size_t)a.layer * E + tid];
+        for (int j = 0; j < ng_gu; ++j)
+            a.groups_gu[gb_gu + j] = Group{slot, my_cs + j * a.nc_gu, min(a.nc_gu, my_lc - j * a.nc_gu), 0};
+        for (int j = 0; j < ng_d; ++j)
+            a.groups_d[gb_d + j] = Group{slot, my_cs + j * a.nc_d, min(a.nc_d, my_lc - j * a.nc_d), 0};
+    }
+    if (tid == 0) {
+        a.n_groups[0] = tot_gu;
+        a.n_groups[1] = tot_d;
+    }
+    if (a.has_shared) {
+        for (int t = tid; t < a.T; t += blockDim.x) a.cols[nlive + t] = -(t + 1);
+        const int sg_gu = (a.T + a.nc_gu - 1) / a.nc_gu, sg_d = (a.T + a.nc_d - 1) / a.nc_d;
+        for (int j = tid; j < sg_gu; j += blockDim.x)
+            a.groups_gu[a.max_routed_gu + j] = Group{-2, nlive + j * a.nc_gu, min(a.nc_gu, a.T - j * a.nc_gu), 0};
+        for (int j = tid; j < sg_d; j += blockDim.x)
+            a.groups_d[a.max_routed_d + j] = Group{-2, nlive + j * a.nc_d, min(a.nc_d, a.T - j * a.nc_d), 0};
+    }
+}
+
+}  // namespace
+
+int launch_bucket(const int32_t *ids, int T, int K, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
+                  int32_t *active, int32_t *n_active, uint32_t *status, cudaStream_t s) {
+    const size_t smem = ((size_t)2 * E + 32 * (size_t)E + 64) * sizeof(int);
+    k_bucket<<<1, kBucketThreads, smem, s>>>(ids, T * K, E, counts, offsets, perm, active, n_active, status);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int init_bucket_attributes(int max_smem) {
+    MOE_CUDA_TRY(cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem));
+    return MOE_OK;
+}
+
+int launch_plan(const PlanArgs &a, cudaStream_t s) {
+    const size_t smem = ((size_t)2 * a.E + 64) * sizeof(int);
+    k_plan<<<1, kBucketThreads, smem, s>>>(a);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+}  // namespace moe

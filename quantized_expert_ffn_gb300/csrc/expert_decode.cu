@@ -1,0 +1,441 @@
+// expert_decode.cu -- the routed experts for decode and verify windows.
+//
+// Krasis white paper sec. 5.3: batched expert projections, activation/gating,
+// weighted reduce; fusing the activation into the projection work cut a MoE
+// layer from 30 launches to four. kairos-engine README, "Prefill and decode are
+// different machines": the decode GEMV reads the quantised codes straight from
+// memory with no dequantised scratch copy.
+//
+// Each expert's weights stream from HBM once per layer call. A warp unpacks
+// 32-bit code words into bf16 A fragments holding (q - zero_point) exactly and
+// multiplies them on the tensor cores (mma.sync m16n8k16, fp32 accumulate)
+// against the bucket's tokens (B, one column per token). Each quantisation
+// block accumulates from zero and is added to the running sum times its fp16
+// scale, so the scale never touches a weight.
+//
+//   k_gateup:  CTA = (group, 16-row tile of gate and up), 4 warps splitting the
+//              H chunks; fixed-order cross-warp sum; h = act(gate) * up.
+//   k_down:    CTA = (group, 4 tiles of 16 output rows), one warp per tile;
+//              y_pair = W_down h, unweighted, per (token, rank) pair.
+//   k_combine: y[t] = sum_k w[t][k] y_pair[t*K+k] in k order (+ shared expert).
+// fp32 inputs (x of fp32 layers, and h) enter as two bf16 limbs hi + lo in
+// separate B columns, so a group holds at most 4 such columns.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarps = 4;
+
+template <int KIND>
+struct ChunkRegs;
+template <>
+struct ChunkRegs<MOE_Q2_64> {
+    uint32_t w[4];
+    uint32_t s[2];
+};
+template <>
+struct ChunkRegs<MOE_Q4_32> {
+    uint32_t w[8];
+    uint32_t s[4];
+};
+
+// codes at `cp`, scales at `sp`, for lane `lane`
+template <int KIND>
+__device__ __forceinline__ void load_chunk(const uint8_t *cp, const uint8_t *sp, bool half, int lane,
+                                           ChunkRegs<KIND> &r) {
+    const int g = lane >> 2;
+    if constexpr (KIND == MOE_Q2_64) {
+        if (!half) {
+            const uint4 v = ldg_stream16(cp + 16 * lane);
+            r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
+            r.s[0] = ldg_stream4(sp + 4 * g);
+            r.s[1] = ldg_stream4(sp + 4 * (8 + g));
+        } else {
+            const uint2 v = ldg_stream8(cp + 8 * lane);
+            r.w[0] = v.x; r.w[1] = v.y; r.w[2] = 0; r.w[3] = 0;
+            r.s[0] = ldg_stream4(sp + 4 * g);
+            r.s[1] = 0;
+        }
+    } else {
+        const uint4 v = ldg_stream16(cp + 16 * lane);
+        r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
+        r.s[0] = ldg_stream4(sp + 4 * g);
+        r.s[1] = ldg_stream4(sp + 4 * (8 + g));
+        if (!half) {
+            const uint4 u = ldg_stream16(cp + 512 + 16 * lane);
+            r.w[4] = u.x; r.w[5] = u.y; r.w[6] = u.z; r.w[7] = u.w;
+            r.s[2] = ldg_stream4(sp + 4 * (16 + g));
+            r.s[3] = ldg_stream4(sp + 4 * (24 + g));
+        } else {
+            r.w[4] = r.w[5] = r.w[6] = r.w[7] = 0;
+            r.s[2] = r.s[3] = 0;
+        }
+    }
+}
+
+__device__ __forceinline__ void apply_scale(uint32_t s, float blk[4], float acc[4]) {
+    const float lo = __half2float(__ushort_as_half((unsigned short)(s & 0xFFFFu)));
+    const float hi = __half2float(__ushort_as_half((unsigned short)(s >> 16)));
+    acc[0] = fmaf(lo, blk[0], acc[0]);
+    acc[1] = fmaf(lo, blk[1], acc[1]);
+    acc[2] = fmaf(hi, blk[2], acc[2]);
+    acc[3] = fmaf(hi, blk[3], acc[3]);
+    blk[0] = blk[1] = blk[2] = blk[3] = 0.f;
+}
+
+// NMAT matrices of one chunk against the B columns in shared memory
+// (xrow = xs + g*ldx + 2c, indexed by the chunk's absolute k).
+template <int KIND, int NMAT>
+__device__ __forceinline__ void mma_chunk(const ChunkRegs<KIND> (&r)[NMAT], bool half, const __nv_bfloat16 *xrow,
+                                          int k0, const Unpack &un, float (&acc)[NMAT][4]) {
+    float blk[NMAT][4];
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) blk[m][0] = blk[m][1] = blk[m][2] = blk[m][3] = 0.f;
+    if constexpr (KIND == MOE_Q2_64) {
+        const int nwords = half ? 2 : 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (i >= nwords) break;
+            uint32_t R[NMAT][8];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) unpack_q2(r[m].w[i], un, R[m]);
+#pragma unroll
+            for (int hs = 0; hs < 2; ++hs) {
+                const int k = k0 + 16 * (2 * i + hs);
+                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(xrow + k);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(xrow + k + 8);
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) mma_bf16(blk[m], &R[m][4 * hs], b0, b1, blk[m]);
+            }
+            if (i & 1) {
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) apply_scale(r[m].s[i >> 1], blk[m], acc[m]);
+            }
+        }
+    } else {
+        const int nwords = half ? 4 : 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i >= nwords) break;
+            uint32_t R[NMAT][4];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) unpack_q4(r[m].w[i], un, R[m]);
+            const int k = k0 + 16 * i;
+            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(xrow + k);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(xrow + k + 8);
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) mma_bf16(blk[m], R[m], b0, b1, blk[m]);
+            if (i & 1) {
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) apply_scale(r[m].s[i >> 1], blk[m], acc[m]);
+            }
+        }
+    }
+}
+
+// token of a column value (pair p >= 0 or shared token -(t+1)) and its h / y_pair row
+__device__ __forceinline__ int col_token(int cv, int K) { return cv >= 0 ? cv / K : -cv - 1; }
+__device__ __forceinline__ int col_row(int cv, int T, int K) { return cv >= 0 ? cv : T * K + (-cv - 1); }
+
+struct Task {
+    Group grp;
+    QLayout L;
+    const uint8_t *wbase;
+    int tile;  // gate/up: row tile; down: first of 4 row tiles
+    bool shared;
+};
+
+// Resolve blockIdx.x into a task. Routed tasks first (max_routed groups x
+// tiles_r), then shared (n_shared groups x tiles_s). Returns false if idle.
+__device__ __forceinline__ bool resolve_task(const ExpertArgs &a, int tiles_r, int tiles_s, Task &t) {
+    const int bid = blockIdx.x;
+    const int routed_tasks = a.max_routed * tiles_r;
+    if (bid < routed_tasks) {
+        const int gi = bid / tiles_r;
+        if (gi >= *a.n_groups) return false;
+        t.grp = a.groups[gi];
+        t.tile = bid % tiles_r;
+        t.L = a.src.L;
+        if (t.grp.slot < 0 || t.grp.slot >= a.src.capacity) {
+            set_status(a.status, MOE_STATUS_BOUNDS);
+            return false;
+        }
+        t.wbase = a.src.arena_base + (long long)t.grp.slot * a.src.slot_stride;
+        t.shared = false;
+    } else {
+        const int b2 = bid - routed_tasks;
+        const int gi = b2 / tiles_s;
+        if (gi >= a.n_shared) return false;
+        t.grp = a.groups[a.max_routed + gi];
+        t.tile = b2 % tiles_s;
+        t.L = a.src.LS;
+        t.wbase = a.src.shared;
+        t.shared = true;
+    }
+    return true;
+}
+
+template <int KIND, bool XF32>
+__global__ void __launch_bounds__(32 * kWarps) k_gateup(ExpertArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    Task tk;
+    if (!resolve_task(a, a.src.L.gu_tiles, a.src.shared ? a.src.LS.gu_tiles : 1, tk)) return;
+    const QLayout &L = tk.L;
+    const int H = L.H, ldx = H + 8;
+    __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem);
+    float *red = reinterpret_cast<float *>(smem + (size_t)8 * ldx * sizeof(__nv_bfloat16));
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ncols = tk.grp.ncols;
+    // stage the group's tokens as bf16 B columns (fp32 x: hi in rows 0..3, lo in 4..7)
+    for (int idx = tid; idx < 8 * (H / 8); idx += blockDim.x) {
+        const int r = idx / (H / 8), h8 = (idx % (H / 8)) * 8;
+        const int j = XF32 ? (r & 3) : r;
+        uint4 out = make_uint4(0, 0, 0, 0);
+        if (j < ncols) {
+            const int t = col_token(a.cols[tk.grp.col0 + j], a.K);
+            if constexpr (XF32) {
+                const float *xp = reinterpret_cast<const float *>(a.x) + (size_t)t * H + h8;
+                const float4 v0 = *reinterpret_cast<const float4 *>(xp);
+                const float4 v1 = *reinterpret_cast<const float4 *>(xp + 4);
+                const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                __nv_bfloat16 o[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    __nv_bfloat16 hi, lo;
+                    split_bf16(v[q], hi, lo);
+                    o[q] = r < 4 ? hi : lo;
+                }
+                out = *reinterpret_cast<const uint4 *>(o);
+            } else {
+                out = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.x) +
+                                                       (size_t)t * H + h8);
+            }
+        }
+        *reinterpret_cast<uint4 *>(xs + (size_t)r * ldx + h8) = out;
+    }
+    __syncthreads();
+
+    const Unpack un = tk.shared ? a.un_s : a.un;
+    const int g = lane >> 2, c = lane & 3;
+    const __nv_bfloat16 *xrow = xs + (size_t)g * ldx + 2 * c;
+    const int n_chunks = L.gu_chunks;
+    const int c_begin = warp * n_chunks / kWarps, c_end = (warp + 1) * n_chunks / kWarps;
+    const uint8_t *tile_ptr = tk.wbase + (long long)tk.tile * L.gu_tile_bytes;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    ChunkRegs<KIND> cur[2], nxt[2];
+    auto load = [&](int ch, ChunkRegs<KIND>(&r)[2]) {
+        const bool half = L.gu_half && ch == n_chunks - 1;
+        const int cb = half ? L.cb / 2 : L.cb, sb = half ? L.sb / 2 : L.sb;
+        const uint8_t *cp = tile_ptr + (long long)ch * L.gu_chunk_bytes;
+        load_chunk<KIND>(cp, cp + 2 * cb, half, lane, r[0]);
+        load_chunk<KIND>(cp + cb, cp + 2 * cb + sb, half, lane, r[1]);
+    };
+    if (c_begin < c_end) load(c_begin, cur);
+    for (int ch = c_begin; ch < c_end; ++ch) {
+        if (ch + 1 < c_end) load(ch + 1, nxt);
+        const bool half = L.gu_half && ch == n_chunks - 1;
+        mma_chunk<KIND, 2>(cur, half, xrow, ch * 128, un, acc);
+        if (ch + 1 < c_end) {
+            cur[0] = nxt[0];
+            cur[1] = nxt[1];
+        }
+    }
+    // fixed-order sum over the 4 warps
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) red[(warp * 32 + lane) * 8 + m * 4 + q] = acc[m][q];
+    __syncthreads();
+    if (warp != 0) return;
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float s = red[lane * 8 + q];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) s += red[(w * 32 + lane) * 8 + q];
+        v[q] = s;
+    }
+    if constexpr (XF32) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], 2);
+        if (c >= 2) return;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int rr = g + 8 * (q >> 1), j = 2 * c + (q & 1);
+        if (j >= ncols) continue;
+        const float gv = v[q], uv = v[4 + q];
+        const float act = a.act == MOE_ACT_GEGLU_TANH ? gelu_tanh_f(gv) : silu_f(gv);
+        const int row = col_row(a.cols[tk.grp.col0 + j], a.T, a.K);
+        a.h[(size_t)row * a.h_ld + tk.tile * 16 + rr] = act * uv;
+    }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(32 * kWarps) k_down(ExpertArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    Task tk;
+    const int tiles_r = (a.src.L.d_tiles + kWarps - 1) / kWarps;
+    const int tiles_s = a.src.shared ? (a.src.LS.d_tiles + kWarps - 1) / kWarps : 1;
+    if (!resolve_task(a, tiles_r, tiles_s, tk)) return;
+    const QLayout &L = tk.L;
+    const int F = L.F, ldx = F + 8;
+    __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ncols = tk.grp.ncols;
+    // h of the group's columns as hi (rows 0..3) and lo (rows 4..7) limbs
+    for (int idx = tid; idx < 8 * (F / 8); idx += blockDim.x) {
+        const int r = idx / (F / 8), f8 = (idx % (F / 8)) * 8;
+        const int j = r & 3;
+        uint4 out = make_uint4(0, 0, 0, 0);
+        if (j < ncols) {
+            const int row = col_row(a.cols[tk.grp.col0 + j], a.T, a.K);
+            const float *hp = a.h + (size_t)row * a.h_ld + f8;
+            const float4 v0 = *reinterpret_cast<const float4 *>(hp);
+            const float4 v1 = *reinterpret_cast<const float4 *>(hp + 4);
+            const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            __nv_bfloat16 o[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                __nv_bfloat16 hi, lo;
+                split_bf16(v[q], hi, lo);
+                o[q] = r < 4 ? hi : lo;
+            }
+            out = *reinterpret_cast<const uint4 *>(o);
+        }
+        *reinterpret_cast<uint4 *>(xs + (size_t)r * ldx + f8) = out;
+    }
+    __syncthreads();
+    const int tile = tk.tile * kWarps + warp;
+    if (tile >= L.d_tiles) return;
+    const Unpack un = tk.shared ? a.un_s : a.un;
+    const int g = lane >> 2, c = lane & 3;
+    const __nv_bfloat16 *xrow = xs + (size_t)g * ldx + 2 * c;
+    const int n_chunks = L.d_chunks;
+    const uint8_t *tile_ptr = tk.wbase + L.d_offset + (long long)tile * L.d_tile_bytes;
+    float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+    ChunkRegs<KIND> cur[1], nxt[1];
+    auto load = [&](int ch, ChunkRegs<KIND>(&r)[1]) {
+        const bool half = L.d_half && ch == n_chunks - 1;
+        const int cb = half ? L.cb / 2 : L.cb;
+        const uint8_t *cp = tile_ptr + (long long)ch * L.d_chunk_bytes;
+        load_chunk<KIND>(cp, cp + cb, half, lane, r[0]);
+    };
+    load(0, cur);
+    for (int ch = 0; ch < n_chunks; ++ch) {
+        if (ch + 1 < n_chunks) load(ch + 1, nxt);
+        const bool half = L.d_half && ch == n_chunks - 1;
+        mma_chunk<KIND, 1>(cur, half, xrow, ch * 128, un, acc);
+        if (ch + 1 < n_chunks) cur[0] = nxt[0];
+    }
+    float v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = acc[0][q] + __shfl_xor_sync(0xffffffffu, acc[0][q], 2);
+    if (c >= 2) return;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int rr = g + 8 * (q >> 1), j = 2 * c + (q & 1);
+        if (j >= ncols) continue;
+        const int row = col_row(a.cols[tk.grp.col0 + j], a.T, a.K);
+        a.yp[(size_t)row * L.H + tile * 16 + rr] = v[q];
+    }
+}
+
+__global__ void __launch_bounds__(256) k_combine(const float *__restrict__ yp, const float *__restrict__ w,
+                                                 const int32_t *__restrict__ live, int T, int K, int H,
+                                                 int has_shared, int accumulate, float *y) {
+    const int j = blockIdx.x * 256 + threadIdx.x, t = blockIdx.y;
+    if (j >= H) return;
+    float acc = 0.f;
+    for (int k = 0; k < K; ++k) {
+        const int p = t * K + k;
+        if (live[p]) acc = fmaf(w[p], yp[(size_t)p * H + j], acc);
+    }
+    if (has_shared) acc += yp[(size_t)(T * K + t) * H + j];
+    float *yt = y + (size_t)t * H + j;
+    *yt = accumulate ? *yt + acc : acc;
+}
+
+__global__ void __launch_bounds__(256) k_rmsnorm_bf16(const float *__restrict__ x, int H, float eps,
+                                                      __nv_bfloat16 *__restrict__ out) {
+    __shared__ float ws[8];
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const float *xt = x + (size_t)t * H;
+    float s = 0.f;
+    for (int h = tid; h < H; h += 256) s = fmaf(xt[h], xt[h], s);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((tid & 31) == 0) ws[tid >> 5] = s;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += ws[w];
+    const float r = 1.0f / sqrtf(tot / (float)H + eps);
+    for (int h = tid; h < H; h += 256) out[(size_t)t * H + h] = __float2bfloat16_rn(xt[h] * r);
+}
+
+}  // namespace
+
+int launch_gateup(const ExpertArgs &a, moe_dtype xt, cudaStream_t s) {
+    const int tasks = a.max_routed * a.src.L.gu_tiles + (a.src.shared ? a.n_shared * a.src.LS.gu_tiles : 0);
+    if (tasks == 0) return MOE_OK;
+    const int H = a.src.L.H;
+    const size_t smem = (size_t)8 * (H + 8) * 2 + (size_t)kWarps * 32 * 8 * 4;
+#define MOE_GU_CASE(KIND, XF)                                                                          \
+    {                                                                                                  \
+        k_gateup<KIND, XF><<<tasks, 32 * kWarps, smem, s>>>(a);                                        \
+    }
+    const bool f32 = xt == MOE_F32;
+    if (a.src.L.kind == MOE_Q2_64) {
+        if (f32) MOE_GU_CASE(MOE_Q2_64, true) else MOE_GU_CASE(MOE_Q2_64, false)
+    } else {
+        if (f32) MOE_GU_CASE(MOE_Q4_32, true) else MOE_GU_CASE(MOE_Q4_32, false)
+    }
+#undef MOE_GU_CASE
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int launch_down(const ExpertArgs &a, cudaStream_t s) {
+    const int tiles_r = (a.src.L.d_tiles + kWarps - 1) / kWarps;
+    const int tiles_s = a.src.shared ? (a.src.LS.d_tiles + kWarps - 1) / kWarps : 0;
+    const int tasks = a.max_routed * tiles_r + (a.src.shared ? a.n_shared * tiles_s : 0);
+    if (tasks == 0) return MOE_OK;
+    int Fmax = a.src.L.F;
+    if (a.src.shared && a.src.LS.F > Fmax) Fmax = a.src.LS.F;
+    const size_t smem = (size_t)8 * (Fmax + 8) * 2;
+    if (a.src.L.kind == MOE_Q2_64) {
+        k_down<MOE_Q2_64><<<tasks, 32 * kWarps, smem, s>>>(a);
+    } else {
+        k_down<MOE_Q4_32><<<tasks, 32 * kWarps, smem, s>>>(a);
+    }
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int init_expert_attributes(int max_smem) {
+    const void *ks[] = {(const void *)k_gateup<MOE_Q2_64, true>, (const void *)k_gateup<MOE_Q2_64, false>,
+                        (const void *)k_gateup<MOE_Q4_32, true>, (const void *)k_gateup<MOE_Q4_32, false>,
+                        (const void *)k_down<MOE_Q2_64>, (const void *)k_down<MOE_Q4_32>};
+    for (const void *k : ks) MOE_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem));
+    return MOE_OK;
+}
+
+int launch_combine(const float *yp, const float *w, const int32_t *live, int T, int K, int H, int has_shared,
+                   int accumulate, float *y, cudaStream_t s) {
+    if (T == 0) return MOE_OK;
+    k_combine<<<dim3((H + 255) / 256, T), 256, 0, s>>>(yp, w, live, T, K, H, has_shared, accumulate, y);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int launch_rmsnorm_bf16(const float *x, int T, int H, float eps, __nv_bfloat16 *out, cudaStream_t s) {
+    if (T == 0) return MOE_OK;
+    k_rmsnorm_bf16<<<T, 256, 0, s>>>(x, H, eps, out);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+}  // namespace moe

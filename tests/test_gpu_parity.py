@@ -1,0 +1,335 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Routing: expert ids, bucket offsets and permutations bit-exact given the same
+fp32 logits. Layer outputs: per token, ||y - y_oracle||_inf / ||y_oracle||_inf
+<= 2e-3 (fp32 accumulation against fp64)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from quantized_expert_ffn_gb300 import _lib as L
+from synth import configs as C
+from tests.gpu_util import TOL, GpuLayers, oracle_layer, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+    torch.cuda.init()
+    return torch
+
+
+@pytest.fixture(scope="module")
+def ctx(torch):
+    c = L.moe_ctx_create(0)
+    yield c
+    L.moe_ctx_destroy(c)
+
+
+def _x(cfg, T, step=0):
+    return C.activations(cfg, T, step)
+
+
+# ------------------------------------------------------------------ router + top-k
+
+@pytest.mark.parametrize("name,T", [("tiny", 4), ("q2_layer", 1), ("q2_layer", 4), ("gemma_layer", 8),
+                                    ("gemma_layer", 37)])
+def test_router_topk_matches_oracle(torch, ctx, name, T):
+    cfg = C.CONFIGS[name]
+    x = _x(cfg, T, step=3)
+    Wr = C.router_weights(cfg, 0)
+    b = C.router_bias(cfg, 0)
+    logits = torch.empty(T, cfg.E, device="cuda")
+    ids = torch.empty(T, cfg.K, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, cfg.K, device="cuda")
+    L.moe_router_topk(ctx, to_dev(x), to_dev(Wr), None if b is None else to_dev(b), cfg.K, logits, ids, w)
+    assert L.moe_status(ctx) == 0
+    lg = logits.cpu().numpy()
+    ref = oracle.router_logits(C.as_f64(x), C.as_f64(Wr), None if b is None else b.astype(np.float64))
+    assert np.abs(lg - ref).max() <= 1e-4
+    oids, ow, bad = oracle.topk(lg.astype(np.float64), cfg.K)
+    assert not bad
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-5, atol=1e-7)
+
+
+def test_topk_ties_and_nonfinite(torch, ctx):
+    E, K, H, T = 24, 6, 64, 5
+    Wr = torch.zeros(E, H, device="cuda")
+    rng = np.random.default_rng(0)
+    bias = rng.integers(-2, 3, size=E).astype(np.float32)  # many exact ties
+    x = torch.zeros(T, H, device="cuda")
+    logits = torch.empty(T, E, device="cuda")
+    ids = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, K, device="cuda")
+    L.moe_router_topk(ctx, x, Wr, to_dev(bias), K, logits, ids, w)
+    assert L.moe_status(ctx) == 0
+    oids, ow, _ = oracle.topk(np.tile(bias.astype(np.float64), (T, 1)), K)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=1e-6)
+    # NaN and inf logits: NaN ranks last, the status bit is set, weights are NaN
+    bias2 = bias.copy()
+    bias2[3] = np.nan
+    bias2[7] = np.inf
+    ids_all = torch.empty(T, E, dtype=torch.int32, device="cuda")
+    w_all = torch.empty(T, E, device="cuda")
+    L.moe_router_topk(ctx, x, Wr, to_dev(bias2), E, logits, ids_all, w_all)
+    assert L.moe_status(ctx) & L.STATUS_NONFINITE
+    oids2, _, bad = oracle.topk(np.tile(bias2.astype(np.float64), (T, 1)), E)
+    assert bad
+    assert np.array_equal(ids_all.cpu().numpy(), oids2)
+    assert oids2[0, -1] == 3 and oids2[0, 0] == 7
+    assert np.isnan(w_all.cpu().numpy()).all()
+
+
+# ------------------------------------------------------------------ bucket
+
+@pytest.mark.parametrize("T,K,E", [(1, 1, 1), (1, 10, 512), (4, 10, 512), (4, 2, 16), (8, 8, 128),
+                                   (4096, 8, 128), (333, 7, 1000), (2, 32, 1024)])
+def test_bucket_bit_exact(torch, ctx, T, K, E):
+    rng = np.random.default_rng(T + K + E)
+    ids = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    if E > 4:  # skew: most pairs on a few experts
+        ids[: T // 2, 0] = 1
+    ref = oracle.bucket(ids, E)
+    d = lambda n: torch.empty(max(n, 1), dtype=torch.int32, device="cuda")
+    counts, offsets, perm, active, na = d(E), d(E + 1), d(T * K), d(E), d(1)
+    L.moe_bucket(ctx, to_dev(ids), E, counts, offsets, perm, active, na)
+    assert L.moe_status(ctx) == 0
+    n = int(na.cpu()[0])
+    assert np.array_equal(counts.cpu().numpy(), ref["counts"])
+    assert np.array_equal(offsets.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(perm.cpu().numpy()[:T * K], ref["perm"])
+    assert n == ref["active"].size
+    assert np.array_equal(active.cpu().numpy()[:n], ref["active"])
+
+
+def test_bucket_out_of_range_ids_flag_bounds(torch, ctx):
+    ids = np.array([[0, 5], [2, 9]], dtype=np.int32)  # 5 and 9 outside E = 4
+    d = lambda n: torch.zeros(n, dtype=torch.int32, device="cuda")
+    counts, offsets, perm, active, na = d(4), d(5), d(4), d(4), d(1)
+    L.moe_bucket(ctx, to_dev(ids), 4, counts, offsets, perm, active, na)
+    assert L.moe_status(ctx) & L.STATUS_BOUNDS
+    assert counts.cpu().tolist() == [1, 0, 1, 0]
+    assert offsets.cpu().tolist() == [0, 1, 1, 2, 2]
+    assert perm.cpu().tolist()[:2] == [0, 2]
+
+
+# ------------------------------------------------------------------ whole layer
+
+@pytest.fixture(scope="module")
+def tiny(ctx):
+    g = GpuLayers(ctx, C.CONFIGS["tiny"])
+    yield g
+    g.close()
+
+
+@pytest.fixture(scope="module")
+def q2(ctx):
+    g = GpuLayers(ctx, C.CONFIGS["q2_layer"])
+    yield g
+    g.close()
+
+
+@pytest.fixture(scope="module")
+def gemma(ctx):
+    g = GpuLayers(ctx, C.CONFIGS["gemma_layer"])
+    yield g
+    g.close()
+
+
+def _check_layer(g, T, step=0, tokens=None):
+    cfg = g.cfg
+    x = _x(cfg, T, step)
+    y, logits, ids = g.forward(to_dev(x))
+    assert L.moe_status(g.ctx) == 0
+    y, lg, ids = y.cpu().numpy(), logits.cpu().numpy(), ids.cpu().numpy()
+    rows = np.arange(T) if tokens is None else np.asarray(tokens)
+    r = oracle_layer(cfg, 0, C.as_f64(x), lg, zero_point=g.zp, tokens=rows)
+    assert r["status"] == 0
+    assert np.array_equal(ids[rows], r["ids"])
+    err = rel_err(y[rows], r["y"])
+    assert err <= TOL, err
+    return err
+
+
+def test_layer_tiny(tiny):
+    err = _check_layer(tiny, 4)
+    assert err < 1e-4
+
+
+@pytest.mark.parametrize("T", [1, 4, 3])
+def test_layer_q2(q2, T):
+    _check_layer(q2, T, step=T)
+
+
+@pytest.mark.parametrize("T", [1, 2, 8, 5])
+def test_layer_gemma_with_shared(gemma, T):
+    _check_layer(gemma, T, step=10 + T)
+
+
+def test_layer_q2_zero_point_two(ctx):
+    cfg = C.CONFIGS["q2_layer"]
+    g = GpuLayers(ctx, cfg, zero_point=2)
+    try:
+        _check_layer(g, 4, step=77)
+    finally:
+        g.close()
+
+
+def test_prefill_sampled_tokens(gemma):
+    # 4096 tokens through the same path; the oracle checks a sample of rows.
+    rng = np.random.default_rng(5)
+    rows = np.sort(rng.choice(4096, size=10, replace=False))
+    _check_layer(gemma, 4096, step=4096, tokens=rows)
+
+
+# ------------------------------------------------------------------ invariants
+
+def test_t_invariance_bitwise(q2, gemma):
+    for g in (q2, gemma):
+        x = to_dev(_x(g.cfg, 4, step=21))
+        y4, l4, i4 = g.forward(x)
+        for t in range(4):
+            y1, l1, i1 = g.forward(x[t:t + 1].contiguous())
+            assert torch_equal(y1[0], y4[t])
+            assert torch_equal(l1[0], l4[t])
+            assert torch_equal(i1[0], i4[t])
+
+
+def torch_equal(a, b):
+    import torch
+    return bool(torch.equal(a, b))
+
+
+def test_token_permutation_equivariance(q2):
+    import torch
+    x = to_dev(_x(q2.cfg, 4, step=22))
+    p = torch.tensor([2, 0, 3, 1], device="cuda")
+    y, _, _ = q2.forward(x)
+    yp, _, _ = q2.forward(x[p].contiguous())
+    assert torch.equal(yp, y[p])
+
+
+def test_deterministic_repeat(gemma):
+    import torch
+    x = to_dev(_x(gemma.cfg, 8, step=23))
+    a, _, _ = gemma.forward(x)
+    b, _, _ = gemma.forward(x)
+    assert torch.equal(a, b)
+
+
+def test_expert_ffn_matches_layer_and_zero_weight_skip(torch, ctx, q2):
+    cfg = q2.cfg
+    T = 3
+    x = to_dev(_x(cfg, T, step=31))
+    y, logits, ids = q2.forward(x)
+    # the same routing through the step-by-step calls, then moe_expert_ffn
+    w = torch.empty(T, cfg.K, device="cuda")
+    ids2 = torch.empty(T, cfg.K, dtype=torch.int32, device="cuda")
+    L.moe_router_topk(ctx, x, q2.Wr[0], q2.bias[0], cfg.K, logits.clone(), ids2, w)
+    d = lambda n: torch.empty(n, dtype=torch.int32, device="cuda")
+    counts, offsets, perm, active, na = d(cfg.E), d(cfg.E + 1), d(T * cfg.K), d(cfg.E), d(1)
+    L.moe_bucket(ctx, ids2, cfg.E, counts, offsets, perm, active, na)
+    ws = q2.workspace(T)
+    y2 = torch.empty_like(y)
+    L.moe_expert_ffn(ctx, q2.desc(), x, ids2, w, offsets, perm, y2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    # zero the weight of rank 0 of token 1: its contribution disappears
+    w0 = w.clone()
+    w0[1, 0] = 0.0
+    y3 = torch.empty_like(y)
+    L.moe_expert_ffn(ctx, q2.desc(), x, ids2, w0, offsets, perm, y3, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y3[0], y[0]) and torch.equal(y3[2], y[2])
+    r = oracle_layer(cfg, 0, C.as_f64(_x(cfg, T, step=31)), logits.cpu().numpy(), tokens=[1])
+    e0 = int(r["ids"][0, 0])
+    ye = oracle.expert_ffn(cfg.kind, cfg.zero_point, C.experts(cfg, 0, [e0])[0], cfg.H, cfg.F,
+                           C.as_f64(_x(cfg, T, step=31))[1:2])
+    want = r["y"][0] - r["w"][0, 0] * ye[0]
+    assert rel_err(y3[1:2].cpu().numpy(), want[None]) <= TOL
+
+
+def test_absent_expert_status_and_zero_contribution(torch, ctx):
+    cfg = C.CONFIGS["tiny"]
+    g = GpuLayers(ctx, cfg)
+    try:
+        x = _x(cfg, 4, step=41)
+        y, logits, ids = g.forward(to_dev(x))
+        assert L.moe_status(ctx) == 0
+        e = int(ids.cpu()[0, 0])
+        L.moe_slot_evict(g.slots, 0, e)
+        assert L.moe_slot_lookup(g.slots, 0, e) == -1
+        y2, logits2, _ = g.forward(to_dev(x))
+        assert L.moe_status(ctx) & L.STATUS_EXPERT_ABSENT
+        lg = logits2.cpu().numpy().astype(np.float64)
+        oids, _, _ = oracle.topk(lg, cfg.K)
+        blobs = C.experts(cfg, 0, range(cfg.E))
+        experts = [None if i == e else blobs[i] for i in range(cfg.E)]
+        r = oracle.layer_forward(cfg.kind, cfg.zero_point, cfg.H, cfg.E, cfg.K, cfg.F, None, None, experts,
+                                 C.as_f64(x), logits_in=lg)
+        assert r["status"] == oracle.STATUS_ABSENT
+        assert rel_err(y2.cpu().numpy(), r["y"]) <= TOL
+        # reload: output returns to the original bits
+        L.moe_slot_load(g.slots, 0, e, torch.from_numpy(blobs[e]).cuda())
+        y3, _, _ = g.forward(to_dev(x))
+        assert torch.equal(y3, y)
+    finally:
+        g.close()
+
+
+def test_host_buffers_path_equals_device_path(torch, ctx, q2):
+    cfg = q2.cfg
+    T = 4
+    xb = _x(cfg, T, step=51)
+    y, _, _ = q2.forward(to_dev(xb))
+    x_host = torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    y_host = torch.empty(T, cfg.H, dtype=torch.float32).pin_memory()
+    extra = 2 * (T * cfg.H * 4 + 256)
+    ws = q2.workspace(T, extra)
+    L.moe_layer_forward_host(ctx, q2.desc(), x_host, y_host, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host, y.cpu())
+
+
+# ------------------------------------------------------------------ stack chain
+
+def test_stack_teacher_forced(torch, ctx):
+    cfg = C.CONFIGS["q2_stack"]
+    n = 3
+    g = GpuLayers(ctx, cfg, n_layers=n)
+    try:
+        T = 4
+        resid0 = C.as_f64(C.activations(cfg, T, step=61)).astype(np.float32)
+        eps = 1e-6
+        descs = [g.desc(l) for l in range(n)]
+        ws = g.workspace(T)
+        # whole chain with traces
+        resid = torch.from_numpy(resid0.copy()).cuda()
+        tr_in = torch.empty(n, T, cfg.H, dtype=torch.bfloat16, device="cuda")
+        tr_lg = torch.empty(n, T, cfg.E, device="cuda")
+        L.moe_stack_forward(ctx, descs, resid, eps, ws, tr_in, tr_lg)
+        assert L.moe_status(ctx) == 0
+        # layer by layer: same bits, and each layer teacher-forced against the oracle
+        r = torch.from_numpy(resid0.copy()).cuda()
+        for l in range(n):
+            before = r.cpu().numpy().astype(np.float64)
+            u = torch.empty(T, cfg.H, dtype=torch.bfloat16, device="cuda")
+            lg = torch.empty(1, T, cfg.E, device="cuda")
+            L.moe_stack_forward(ctx, [descs[l]], r, eps, ws, u, lg)
+            torch.cuda.synchronize()
+            assert torch.equal(u, tr_in[l]) and torch.equal(lg[0], tr_lg[l])
+            u64 = u.float().cpu().numpy().astype(np.float64)
+            # RMSNorm then bf16: within one bf16 rounding of the oracle
+            norm = oracle.rmsnorm(before, eps)
+            assert np.abs(u64 - norm).max() <= 2.0 ** -8 * np.abs(norm).max()
+            ro = oracle_layer(cfg, l, u64, lg[0].cpu().numpy())
+            ylayer = r.cpu().numpy().astype(np.float64) - before
+            assert rel_err(ylayer, ro["y"]) <= TOL
+        assert torch.equal(r, resid)
+    finally:
+        g.close()
