@@ -244,6 +244,33 @@ MOE_API int moe_stack_forward_host(moe_ctx *ctx, const moe_layer_desc *layers, i
                                    float *resid_host, int T, float eps, void *ws, size_t ws_bytes,
                                    moe_stream_t stream);
 
+/* Size of the library's fixed scratch area used by moe_layer_forward_static. */
+#define MOE_STATIC_SCRATCH_BYTES (4 * 1024 * 1024)
+
+/* moe_layer_forward without a workspace argument, for callers that cannot
+ * allocate device memory: a host framework that owns the whole GPU through its
+ * own memory pool and gives libraries no allocator, a latency-critical decode
+ * loop that must not call cudaMalloc (it can synchronise the device), or a thin
+ * binding with no way to size and keep a buffer. The paper has no counterpart:
+ * it is a packaging choice of this library.
+ *
+ * The scratch is one file-scope device array of MOE_STATIC_SCRATCH_BYTES (4 MiB)
+ * that every GPU loading the library holds until the process exits. This call
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture. A window whose moe_layer_workspace() exceeds the array fails with
+ * MOE_ERR_WORKSPACE (4 MiB covers decode and verify windows: about 150 KB at
+ * T=1 and 600 KB at T=4 for the H=2560, E=512, top-10, F=640 layer; 1.5 MB at T=8
+ * for the H=2816 layer with a 2112-wide shared expert). Every call on every
+ * stream shares the array and leaves its contents behind; nothing in it needs
+ * to start at zero (each call writes what it reads). Calls that overlap on the
+ * GPU race on the array: serialise them (one stream, or events). Arguments and
+ * results are those of moe_layer_forward. */
+MOE_API int moe_layer_forward_static(moe_ctx *ctx, const moe_layer_desc *desc, const void *x,
+                                     moe_dtype xt, int T, float *y, float *logits_out,
+                                     int32_t *ids_out, moe_stream_t stream);
+
 /* Weightless RMSNorm with bf16 output: out[t][h] = bf16(x[t][h] / sqrt(mean_h
  * x[t][h]^2 + eps)), x f32. H % 8 == 0. */
 MOE_API int moe_rmsnorm_bf16(moe_ctx *ctx, const float *x, int T, int H, float eps, void *out,

@@ -61,6 +61,7 @@ _SIGS = {
     "moe_layer_workspace": [ctypes.POINTER(LayerDesc), _I, ctypes.POINTER(_SZ)],
     "moe_expert_ffn": [_P, ctypes.POINTER(LayerDesc), _P, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "moe_layer_forward": [_P, ctypes.POINTER(LayerDesc), _P, _I, _I, _P, _P, _P, _P, _SZ, _P],
+    "moe_layer_forward_static": [_P, ctypes.POINTER(LayerDesc), _P, _I, _I, _P, _P, _P, _P],
     "moe_layer_forward_host": [_P, ctypes.POINTER(LayerDesc), _P, _I, _I, _P, _P, _SZ, _P],
     "moe_stack_forward": [_P, ctypes.POINTER(LayerDesc), _I, _P, _I, ctypes.c_float, _P, _P, _P, _SZ,
                           _P],
@@ -224,6 +225,13 @@ def moe_layer_forward(ctx: int, desc: LayerDesc, x, y, ws, logits=None, ids=None
     T = x.shape[0]
     _check(load().moe_layer_forward(ctx, ctypes.byref(desc), _ptr(x), dtype_code(x), T, _ptr(y),
                                     _ptr(logits), _ptr(ids), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def moe_layer_forward_static(ctx: int, desc: LayerDesc, x, y, logits=None, ids=None, stream=None):
+    """moe_layer_forward with the library's fixed scratch (no workspace, no allocation)."""
+    T = x.shape[0]
+    _check(load().moe_layer_forward_static(ctx, ctypes.byref(desc), _ptr(x), dtype_code(x), T, _ptr(y),
+                                           _ptr(logits), _ptr(ids), _stream(stream)))
 
 
 def moe_layer_forward_host(ctx: int, desc: LayerDesc, x_host, y_host, ws, stream=None):

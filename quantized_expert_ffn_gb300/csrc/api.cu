@@ -251,6 +251,8 @@ int cuda_error(cudaError_t e, const char *what) {
     return set_error(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+int ctx_device(const moe_ctx *ctx) { return ctx->device; }
+
 }  // namespace moe
 
 using namespace moe;

@@ -1,0 +1,66 @@
+"""moe_layer_forward_static: the layer entry point for callers that cannot
+allocate device memory (it runs on the library's fixed 4 MiB scratch array).
+
+Checked against moe_layer_forward with a caller workspace on the same inputs,
+on two calls in a row (the second call finds the first call's leftovers in the
+shared scratch). This file is collected last on purpose."""
+import numpy as np
+import pytest
+
+from quantized_expert_ffn_gb300 import _lib as L
+from synth import configs as C
+from tests.gpu_util import TOL, GpuLayers, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    import torch
+    torch.cuda.init()
+    c = L.moe_ctx_create(0)
+    yield c
+    L.moe_ctx_destroy(c)
+
+
+@pytest.mark.parametrize("name,T", [("q2_layer", 4), ("gemma_layer", 8)])
+def test_static_scratch_matches_workspace_entry_point(ctx, name, T):
+    import torch
+    cfg = C.CONFIGS[name]
+    g = GpuLayers(ctx, cfg)
+    try:
+        desc = g.desc()
+        for step in (0, 1):
+            x = to_dev(C.activations(cfg, T, step=900 + step))
+            y_ref, logits_ref, ids_ref = g.forward(x)
+            outs = []
+            for _ in range(2):  # two calls in a row on the shared scratch
+                y = torch.full((T, cfg.H), float("nan"), device="cuda")
+                logits = torch.empty(T, cfg.E, device="cuda")
+                ids = torch.empty(T, cfg.K, dtype=torch.int32, device="cuda")
+                L.moe_layer_forward_static(ctx, desc, x, y, logits=logits, ids=ids)
+                torch.cuda.synchronize()
+                assert L.moe_status(ctx) == 0
+                assert torch.equal(ids, ids_ref)
+                assert rel_err(y.cpu().numpy(), y_ref.cpu().numpy()) <= TOL
+                outs.append(y)
+            assert rel_err(outs[1].cpu().numpy(), outs[0].cpu().numpy()) <= TOL
+    finally:
+        g.close()
+
+
+def test_static_scratch_rejects_windows_that_do_not_fit(ctx):
+    import torch
+    cfg = C.CONFIGS["tiny"]
+    g = GpuLayers(ctx, cfg)
+    try:
+        desc = g.desc()
+        assert L.moe_layer_workspace(desc, 4096) > 4 * 1024 * 1024
+        x = to_dev(C.activations(cfg, 4096))
+        y = torch.empty(4096, cfg.H, device="cuda")
+        with pytest.raises(L.MoeError) as e:
+            L.moe_layer_forward_static(ctx, desc, x, y)
+        assert e.value.code == -10
+        assert "static scratch" in str(e.value)
+    finally:
+        g.close()
