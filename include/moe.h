@@ -105,6 +105,13 @@ typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_GEGLU_TANH = 1 } moe_act;
 MOE_API int moe_ctx_create(int device, moe_ctx **out);
 MOE_API int moe_ctx_destroy(moe_ctx *ctx);
 
+/* Context options. MOE_OPT_PERSISTENT_DECODE (default 1): windows of up to 8
+ * tokens (4 with fp32 x) run as one cooperative persistent kernel per call (a
+ * whole moe_stack_forward chain per launch); 0 forces the multi-kernel path.
+ * Both paths give the same bits. MOE_ERR_ARG for an unknown option. */
+#define MOE_OPT_PERSISTENT_DECODE 1
+MOE_API int moe_ctx_set_option(moe_ctx *ctx, int option, int value);
+
 /* Synchronise `stream`, then read and clear the device status bits into *bits.
  * Returns MOE_OK even when bits are set; the caller inspects them. */
 MOE_API int moe_status(moe_ctx *ctx, moe_stream_t stream, uint32_t *bits);

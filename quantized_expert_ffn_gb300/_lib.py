@@ -48,6 +48,7 @@ _SIGS = {
     "moe_ctx_create": [_I, ctypes.POINTER(_P)],
     "moe_ctx_destroy": [_P],
     "moe_status": [_P, _P, ctypes.POINTER(ctypes.c_uint32)],
+    "moe_ctx_set_option": [_P, _I, _I],
     "moe_expert_bytes": [Format, _I, _I, ctypes.POINTER(_SZ)],
     "moe_arena_create": [_P, _SZ, ctypes.POINTER(_P)],
     "moe_arena_destroy": [_P],
@@ -134,6 +135,13 @@ def moe_ctx_create(device: int = 0) -> int:
 
 def moe_ctx_destroy(ctx: int):
     _check(load().moe_ctx_destroy(ctx))
+
+
+OPT_PERSISTENT_DECODE = 1
+
+
+def moe_ctx_set_option(ctx: int, option: int, value: int):
+    _check(load().moe_ctx_set_option(ctx, option, value))
 
 
 def moe_status(ctx: int, stream=None) -> int:

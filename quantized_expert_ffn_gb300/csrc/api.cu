@@ -2,14 +2,18 @@
 // table over the device arena, workspace carving and the order of launches.
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <string>
 #include <vector>
 
+#include "decode_persistent.cuh"
 #include "moe_internal.cuh"
 
 struct moe_ctx {
     int device;
     uint32_t *d_status;
+    int persistent;  // MOE_OPT_PERSISTENT_DECODE
+    int max_smem;    // opt-in shared memory per block
 };
 
 struct moe_arena {
@@ -81,7 +85,7 @@ int check_dims(int H, int F) {
 // Workspace carving for one layer call of up to T tokens.
 struct WsLayout {
     size_t logits, ids, w, counts, offsets, perm, active, n_active, live, cols, groups_gu, groups_d, n_groups, h, yp,
-        u, total;
+        u, bar, total;
     int max_routed_gu, max_routed_d, max_shared, h_ld;
 };
 
@@ -113,6 +117,7 @@ WsLayout ws_layout(const moe_layer_desc *d, int T, int nc_gu) {
     W.h = take((P + T) * (size_t)W.h_ld * 4);
     W.yp = take((P + T) * (size_t)d->H * 4);
     W.u = take((size_t)T * d->H * 2);
+    W.bar = take(16);
     W.total = o;
     return W;
 }
@@ -217,6 +222,95 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
     return launch_combine(ea.yp, w, pa.live, T, d->K, d->H, d->shared != nullptr, accumulate, y, s);
 }
 
+// The persistent decode kernel runs a whole step (one layer, or a chain of
+// layers) in one cooperative launch when the window is small and every layer
+// has the same shapes and formats. Returns MOE_OK with *used = false when it
+// does not apply (the multi-kernel path then runs).
+int try_persistent(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers, bool stack, const void *x,
+                   moe_dtype xt, int T, float *out, float *logits_out, int32_t *ids_out, void *trace_in,
+                   float *trace_logits, float eps, uint8_t *ws, const WsLayout &W, cudaStream_t s, bool *used) {
+    *used = false;
+    if (!ctx->persistent || T < 1 || T > kMaxTok || (xt == MOE_F32 && T > 4)) return MOE_OK;
+    const moe_layer_desc &d0 = layers[0];
+    if (d0.K * T > 256) return MOE_OK;
+    const moe_slots *s0 = d0.slots;
+    for (int l = 0; l < n_layers; ++l) {
+        const moe_layer_desc &d = layers[l];
+        const moe_slots *sl = d.slots;
+        if (d.H != d0.H || d.E != d0.E || d.K != d0.K || d.F != d0.F || d.act != d0.act || d.wr_dtype != d0.wr_dtype ||
+            sl->fmt.kind != s0->fmt.kind || sl->fmt.zero_point != s0->fmt.zero_point ||
+            (d.shared != nullptr) != (d0.shared != nullptr))
+            return MOE_OK;
+        if (d.shared && (d.F_shared != d0.F_shared || d.shared->fmt.zero_point != d0.shared->fmt.zero_point))
+            return MOE_OK;
+        if ((uintptr_t)d.Wr % 16) return MOE_OK;
+    }
+    if (xt == MOE_BF16 && (uintptr_t)x % 16) return MOE_OK;
+    if (stack && (uintptr_t)out % 16) return MOE_OK;
+    int G = 0;
+    const int wr_bytes = d0.wr_dtype == MOE_BF16 ? 2 : 4;
+    // the grid is one CTA per SM; the geometry depends on it through the router rows
+    int sms = 0;
+    MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device));
+    PersistGeom geom = persist_geom(T, d0.H, d0.E, d0.K, d0.F, d0.shared ? d0.F_shared : 0, wr_bytes, sms,
+                                    (size_t)ctx->max_smem);
+    if (geom.bytes > (size_t)ctx->max_smem) return MOE_OK;
+    int rc = persist_max_ctas((int)geom.bytes, &G);
+    if (rc) return rc;
+    if (G != sms) return MOE_OK;
+    if ((d0.E + G - 1) / G > 16) return MOE_OK;  // router rows per CTA
+
+    PersistArgs a;
+    memset(&a, 0, sizeof a);
+    a.T = T;
+    a.H = d0.H;
+    a.E = d0.E;
+    a.K = d0.K;
+    a.act = d0.act;
+    a.stack = stack ? 1 : 0;
+    a.wr_bf16 = d0.wr_dtype == MOE_BF16;
+    a.x_f32 = xt == MOE_F32;
+    a.eps = eps;
+    a.L = s0->layout;
+    a.LS = d0.shared ? d0.shared->layout : s0->layout;
+    a.un = make_unpack(s0->fmt.zero_point);
+    a.un_s = d0.shared ? make_unpack(d0.shared->fmt.zero_point) : a.un;
+    a.geom = geom;
+    a.x = x;
+    a.y = stack ? nullptr : out;
+    a.resid = stack ? out : nullptr;
+    a.logits = logits_out ? logits_out : (float *)(ws + W.logits);
+    a.ids_out = ids_out;
+    a.h_ld = W.h_ld;
+    const size_t hrows = (size_t)T * d0.K + T;
+    a.h_hi = (__nv_bfloat16 *)(ws + W.h);
+    a.h_lo = a.h_hi + hrows * W.h_ld;
+    a.bar = (unsigned *)(ws + W.bar);
+    a.status = ctx->d_status;
+    for (int l0 = 0; l0 < n_layers; l0 += kMaxPersistLayers) {
+        const int n = n_layers - l0 < kMaxPersistLayers ? n_layers - l0 : kMaxPersistLayers;
+        a.n_layers = n;
+        a.trace_in = trace_in ? (__nv_bfloat16 *)trace_in + (size_t)l0 * T * d0.H : nullptr;
+        a.trace_logits = trace_logits ? trace_logits + (size_t)l0 * T * d0.E : nullptr;
+        for (int l = 0; l < n; ++l) {
+            const moe_layer_desc &d = layers[l0 + l];
+            PersistLayer &P = a.layers[l];
+            P.Wr = d.Wr;
+            P.bias = d.bias;
+            P.table = d.slots->d_table;
+            P.layer = d.layer;
+            P.capacity = d.slots->capacity;
+            P.arena = d.slots->base;
+            P.stride = (long long)d.slots->stride;
+            P.shared = d.shared ? d.shared->base + (size_t)d.shared->h_table[0] * d.shared->stride : nullptr;
+        }
+        rc = launch_decode_persistent(a, G, s);
+        if (rc) return rc;
+    }
+    *used = true;
+    return MOE_OK;
+}
+
 // Router + top-K + bucket + experts for one layer; y written or accumulated.
 int layer_core(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype xt, int T, float *y, int accumulate,
                float *logits_out, int32_t *ids_out, uint8_t *ws, const WsLayout &W, cudaStream_t s) {
@@ -253,6 +347,14 @@ int cuda_error(cudaError_t e, const char *what) {
 
 int ctx_device(const moe_ctx *ctx) { return ctx->device; }
 
+int set_max_dynamic_smem(const void *kernel, int max_smem) {
+    cudaFuncAttributes fa;
+    MOE_CUDA_TRY(cudaFuncGetAttributes(&fa, kernel));
+    MOE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      max_smem - (int)fa.sharedSizeBytes));
+    return MOE_OK;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -284,7 +386,7 @@ int moe_ctx_create(int device, moe_ctx **out) {
         return set_error(MOE_ERR_CUDA, "no CUDA device %d (%d visible)", device, n);
     DeviceGuard g(device);
     if (!g.ok) return set_error(MOE_ERR_CUDA, "cudaSetDevice(%d) failed", device);
-    moe_ctx *c = new moe_ctx{device, nullptr};
+    moe_ctx *c = new moe_ctx{device, nullptr, 1, 0};
     cudaError_t e = cudaMalloc(&c->d_status, sizeof(uint32_t));
     if (e != cudaSuccess) {
         delete c;
@@ -306,6 +408,8 @@ int moe_ctx_create(int device, moe_ctx **out) {
     if (!rc) rc = init_bucket_attributes(max_smem);
     if (!rc) rc = init_expert_attributes(max_smem);
     if (!rc) rc = init_repack_attributes(max_smem);
+    if (!rc) rc = init_persist_attributes(max_smem);
+    c->max_smem = max_smem;
     if (rc) {
         cudaFree(c->d_status);
         delete c;
@@ -323,6 +427,15 @@ int moe_ctx_destroy(moe_ctx *ctx) {
     }
     delete ctx;
     return MOE_OK;
+}
+
+int moe_ctx_set_option(moe_ctx *ctx, int option, int value) {
+    if (!ctx) return set_error(MOE_ERR_ARG, "null context");
+    if (option == MOE_OPT_PERSISTENT_DECODE) {
+        ctx->persistent = value != 0;
+        return MOE_OK;
+    }
+    return set_error(MOE_ERR_ARG, "unknown option %d", option);
 }
 
 int moe_status(moe_ctx *ctx, moe_stream_t stream, uint32_t *bits) {
@@ -550,6 +663,10 @@ int moe_layer_forward(moe_ctx *ctx, const moe_layer_desc *desc, const void *x, m
     rc = check_ws(ws, ws_bytes, ws_layout(desc, T, 4).total);
     if (rc) return rc;
     MOE_GUARD(ctx);
+    bool used = false;
+    rc = try_persistent(ctx, desc, 1, false, x, xt, T, y, logits_out, ids_out, nullptr, nullptr, 0.f, (uint8_t *)ws, W,
+                        (cudaStream_t)stream, &used);
+    if (rc || used) return rc;
     return layer_core(ctx, desc, x, xt, T, y, 0, logits_out, ids_out, (uint8_t *)ws, W, (cudaStream_t)stream);
 }
 
@@ -573,7 +690,9 @@ int moe_layer_forward_host(moe_ctx *ctx, const moe_layer_desc *desc, const void 
     float *yd = (float *)(w8 + base + align256(xbytes));
     const cudaStream_t s = (cudaStream_t)stream;
     MOE_CUDA_TRY(cudaMemcpyAsync(xd, x_host, xbytes, cudaMemcpyHostToDevice, s));
-    rc = layer_core(ctx, desc, xd, xt, T, yd, 0, nullptr, nullptr, w8, W, s);
+    bool used = false;
+    rc = try_persistent(ctx, desc, 1, false, xd, xt, T, yd, nullptr, nullptr, nullptr, nullptr, 0.f, w8, W, s, &used);
+    if (!rc && !used) rc = layer_core(ctx, desc, xd, xt, T, yd, 0, nullptr, nullptr, w8, W, s);
     if (rc) return rc;
     MOE_CUDA_TRY(cudaMemcpyAsync(y_host, yd, ybytes, cudaMemcpyDeviceToHost, s));
     return MOE_OK;
@@ -609,6 +728,10 @@ int moe_stack_forward(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers, 
     const cudaStream_t s = (cudaStream_t)stream;
     uint8_t *w8 = (uint8_t *)ws;
     const int H = layers[0].H, E = layers[0].E;
+    bool used = false;
+    rc = try_persistent(ctx, layers, n_layers, true, nullptr, MOE_BF16, T, resid, nullptr, nullptr, trace_in,
+                        trace_logits, eps, w8, W, s, &used);
+    if (rc || used) return rc;
     for (int l = 0; l < n_layers; ++l) {
         __nv_bfloat16 *u = trace_in ? (__nv_bfloat16 *)trace_in + (size_t)l * T * H : (__nv_bfloat16 *)(w8 + W.u);
         float *lg = trace_logits ? trace_logits + (size_t)l * T * E : nullptr;

@@ -197,9 +197,9 @@ int launch_bucket(const int32_t *ids, int T, int K, int E, int32_t *counts, int3
 }
 
 int init_bucket_attributes(int max_smem) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem));
-    MOE_CUDA_TRY(cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem));
-    return MOE_OK;
+    int rc = set_max_dynamic_smem((const void *)k_bucket, max_smem);
+    if (!rc) rc = set_max_dynamic_smem((const void *)k_plan, max_smem);
+    return rc;
 }
 
 int launch_plan(const PlanArgs &a, cudaStream_t s) {

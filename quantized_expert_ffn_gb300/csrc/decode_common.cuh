@@ -1,0 +1,343 @@
+// decode_common.cuh -- device code shared by the multi-kernel path
+// (expert_decode.cu, router.cu) and the persistent decode kernel
+// (decode_persistent.cu). Both paths call these functions so that every output
+// element is computed with the same operations in the same order: a token's
+// result is the same bits whichever path runs it and however many tokens share
+// the window.
+#pragma once
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------- expert chunks
+
+template <int KIND>
+struct ChunkRegs;
+template <>
+struct ChunkRegs<MOE_Q2_64> {
+    uint32_t w[4];
+    uint32_t s[2];
+};
+template <>
+struct ChunkRegs<MOE_Q4_32> {
+    uint32_t w[8];
+    uint32_t s[4];
+};
+
+// codes at `cp`, scales at `sp` (one matrix of one chunk), for lane `lane`
+template <int KIND>
+__device__ __forceinline__ void load_chunk(const uint8_t *cp, const uint8_t *sp, bool half, int lane,
+                                           ChunkRegs<KIND> &r) {
+    const int g = lane >> 2;
+    if constexpr (KIND == MOE_Q2_64) {
+        if (!half) {
+            const uint4 v = ldg_stream16(cp + 16 * lane);
+            r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
+            r.s[0] = ldg_stream4(sp + 4 * g);
+            r.s[1] = ldg_stream4(sp + 4 * (8 + g));
+        } else {
+            const uint2 v = ldg_stream8(cp + 8 * lane);
+            r.w[0] = v.x; r.w[1] = v.y; r.w[2] = 0; r.w[3] = 0;
+            r.s[0] = ldg_stream4(sp + 4 * g);
+            r.s[1] = 0;
+        }
+    } else {
+        const uint4 v = ldg_stream16(cp + 16 * lane);
+        r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
+        r.s[0] = ldg_stream4(sp + 4 * g);
+        r.s[1] = ldg_stream4(sp + 4 * (8 + g));
+        if (!half) {
+            const uint4 u = ldg_stream16(cp + 512 + 16 * lane);
+            r.w[4] = u.x; r.w[5] = u.y; r.w[6] = u.z; r.w[7] = u.w;
+            r.s[2] = ldg_stream4(sp + 4 * (16 + g));
+            r.s[3] = ldg_stream4(sp + 4 * (24 + g));
+        } else {
+            r.w[4] = r.w[5] = r.w[6] = r.w[7] = 0;
+            r.s[2] = r.s[3] = 0;
+        }
+    }
+}
+
+__device__ __forceinline__ void apply_scale(uint32_t s, float blk[4], float acc[4]) {
+    const float lo = __half2float(__ushort_as_half((unsigned short)(s & 0xFFFFu)));
+    const float hi = __half2float(__ushort_as_half((unsigned short)(s >> 16)));
+    acc[0] = fmaf(lo, blk[0], acc[0]);
+    acc[1] = fmaf(lo, blk[1], acc[1]);
+    acc[2] = fmaf(hi, blk[2], acc[2]);
+    acc[3] = fmaf(hi, blk[3], acc[3]);
+    blk[0] = blk[1] = blk[2] = blk[3] = 0.f;
+}
+
+// B operand of one n8 tile: lane (g, c) reads column g at brow + k (+8); a lane
+// whose column is empty passes valid = false and multiplies zeros.
+struct BTile {
+    const __nv_bfloat16 *row;
+    bool valid;
+};
+
+__device__ __forceinline__ uint32_t ld_b(const BTile &b, int k) {
+    return b.valid ? *reinterpret_cast<const uint32_t *>(b.row + k) : 0u;
+}
+
+// NMAT matrices of one chunk (k0 = absolute reduction index of the chunk) times
+// NB n8 tiles of B, accumulated into acc[m][nb].
+template <int KIND, int NMAT, int NB>
+__device__ __forceinline__ void mma_chunk(const ChunkRegs<KIND> (&r)[NMAT], bool half, const BTile (&bt)[NB],
+                                          int k0, const Unpack &un, float (&acc)[NMAT][NB][4]) {
+    float blk[NMAT][NB][4];
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) blk[m][nb][0] = blk[m][nb][1] = blk[m][nb][2] = blk[m][nb][3] = 0.f;
+    if constexpr (KIND == MOE_Q2_64) {
+        const int nwords = half ? 2 : 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (i >= nwords) break;
+            uint32_t R[NMAT][8];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) unpack_q2(r[m].w[i], un, R[m]);
+#pragma unroll
+            for (int hs = 0; hs < 2; ++hs) {
+                const int k = k0 + 16 * (2 * i + hs);
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    const uint32_t b0 = ld_b(bt[nb], k), b1 = ld_b(bt[nb], k + 8);
+#pragma unroll
+                    for (int m = 0; m < NMAT; ++m) mma_bf16(blk[m][nb], &R[m][4 * hs], b0, b1, blk[m][nb]);
+                }
+            }
+            if (i & 1) {
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) apply_scale(r[m].s[i >> 1], blk[m][nb], acc[m][nb]);
+            }
+        }
+    } else {
+        const int nwords = half ? 4 : 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i >= nwords) break;
+            uint32_t R[NMAT][4];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) unpack_q4(r[m].w[i], un, R[m]);
+            const int k = k0 + 16 * i;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                const uint32_t b0 = ld_b(bt[nb], k), b1 = ld_b(bt[nb], k + 8);
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) mma_bf16(blk[m][nb], R[m], b0, b1, blk[m][nb]);
+            }
+            if (i & 1) {
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) apply_scale(r[m].s[i >> 1], blk[m][nb], acc[m][nb]);
+            }
+        }
+    }
+}
+
+// The canonical split of a gate/up row tile's chunks over 4 warps: warp w sums
+// chunks [w*n/4, (w+1)*n/4), and the four partial sums are added in warp order.
+constexpr int kGuSplit = 4;
+__device__ __forceinline__ int gu_chunk_begin(int w, int n) { return w * n / kGuSplit; }
+
+// bf16 hi/lo limbs of an fp32 value
+__device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
+    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+}
+
+__device__ __forceinline__ float act_f(int act, float g) {
+    return act == MOE_ACT_GEGLU_TANH ? gelu_tanh_f(g) : silu_f(g);
+}
+
+// ---------------------------------------------------------------- router
+
+// Router dot products with the canonical order: one expert row is shared by 4
+// warps (128 lanes); lane L = 32q + lane accumulates h = 8L + 1024j .. +7 (j
+// ascending, fmaf in h order), an xor butterfly sums each warp, and the four warp
+// sums are added in warp order ((s0 + s1) + s2) + s3 by combine_router4. A
+// token's logit does not depend on the other tokens. xf(t, h, v[8]) gives 8 fp32
+// inputs of token t; tokens t >= nt are skipped.
+constexpr int kRouterLanes = 128;
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 a, float v[8]) {
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+template <typename WT>
+__device__ __forceinline__ void load_w8(const WT *p, float v[8]);
+template <>
+__device__ __forceinline__ void load_w8<float>(const float *p, float v[8]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void load_w8<__nv_bfloat16>(const __nv_bfloat16 *p, float v[8]) {
+    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(p), v);
+}
+
+// Partial logits of 128-lane slot L (0..127) for up to NT tokens; returns the
+// warp-reduced partial (identical in every lane of the warp).
+template <typename WT, int NT, typename XF>
+__device__ __forceinline__ void router_partial(const WT *wrow, int H, int L, int nt, XF xf, float (&acc)[NT]) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+    for (int h = L * 8; h < H; h += kRouterLanes * 8) {
+        float wv[8];
+        load_w8<WT>(wrow + h, wv);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t >= nt) break;
+            float xv[8];
+            xf(t, h, xv);
+            float a = acc[t];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a = fmaf(wv[j], xv[j], a);
+            acc[t] = a;
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        if (t >= nt) break;
+        float a = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        acc[t] = a;
+    }
+}
+
+// The four warp partials of one expert row, added in warp order.
+__device__ __forceinline__ float combine_router4(const float *part /* [4] */) {
+    return ((part[0] + part[1]) + part[2]) + part[3];
+}
+
+// ---------------------------------------------------------------- top-k
+
+// a ranks before b: larger value first, equal values to the lower index, NaN
+// below every number (NaNs among themselves by index). idx < 0 = no candidate.
+__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
+    if (ib < 0) return ia >= 0;
+    if (ia < 0) return false;
+    const bool na = isnan(va), nb = isnan(vb);
+    if (na != nb) return nb;
+    if (!na && va != vb) return va > vb;
+    return ia < ib;
+}
+
+// Top-K on 64-bit keys that order exactly like ranks_before: the high word maps
+// the fp32 value monotonically to an unsigned integer (NaN lowest, -0 == +0), the
+// low word is ~index (the lower index wins a tie). Key 0 means "no candidate".
+__device__ __forceinline__ unsigned long long topk_key(float v, int idx) {
+    uint32_t b = __float_as_uint(v);
+    uint32_t ord;
+    if (isnan(v)) {
+        ord = 0;
+    } else {
+        if (v == 0.f) b = 0;
+        ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    }
+    return ((unsigned long long)ord << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)idx);
+}
+
+__device__ __forceinline__ int topk_key_index(unsigned long long k) {
+    return k ? (int)(0xFFFFFFFFu - (uint32_t)k) : -1;
+}
+
+__device__ __forceinline__ float topk_key_value(unsigned long long k) {
+    const uint32_t ord = (uint32_t)(k >> 32);
+    const uint32_t b = (ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord;
+    return __uint_as_float(b);
+}
+
+__device__ __forceinline__ unsigned long long shfl_xor64(unsigned long long v, int m) {
+    const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+    return ((unsigned long long)hi << 32) | lo;
+}
+
+__device__ __forceinline__ unsigned long long shfl64(unsigned long long v, int src) {
+    const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)v, src);
+    const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(v >> 32), src);
+    return ((unsigned long long)hi << 32) | lo;
+}
+
+// Warp bitonic sort of 32 keys (one per lane), largest first.
+__device__ __forceinline__ unsigned long long warp_sort32(unsigned long long key, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const unsigned long long o = shfl_xor64(key, j);
+            const bool lower = (lane & j) == 0, desc = (lane & k) == 0;
+            const bool take = (lower == desc) ? (o > key) : (o < key);
+            if (take) key = o;
+        }
+    }
+    return key;
+}
+
+// Top 32 of two lists sorted largest first (one element per lane each): the
+// element-wise max of A and reversed B is bitonic and holds the 32 largest; a
+// bitonic merge sorts it.
+__device__ __forceinline__ unsigned long long warp_merge32(unsigned long long a, unsigned long long b, int lane) {
+    const unsigned long long br = shfl64(b, 31 - lane);
+    unsigned long long c = a > br ? a : br;
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1) {
+        const unsigned long long o = shfl_xor64(c, j);
+        const bool lower = (lane & j) == 0;
+        c = lower ? (o > c ? o : c) : (o < c ? o : c);
+    }
+    return c;
+}
+
+// Sorted keys of logits chunk `ch` (32 entries) of one token.
+__device__ __forceinline__ unsigned long long topk_chunk_keys(const float *l, int E, int ch, int lane, bool &bad) {
+    const int e = ch * 32 + lane;
+    unsigned long long key = 0;
+    if (e < E) {
+        const float v = l[e];
+        bad = !isfinite(v);
+        key = topk_key(v, e);
+    } else {
+        bad = false;
+    }
+    return warp_sort32(key, lane);
+}
+
+// Rank of candidate key `k` among n candidate keys (number of larger keys).
+__device__ __forceinline__ int topk_rank(unsigned long long k, const unsigned long long *cand, int n) {
+    int r = 0;
+    for (int i = 0; i < n; ++i) r += cand[i] > k;
+    return r;
+}
+
+// Softmax of the K chosen logits (lane k holds the k-th; the first is the
+// largest): w_k = exp(l_k - l_0) / sum_j exp(l_j - l_0), the sum in k order.
+__device__ __forceinline__ float topk_weight(float sel_v, int K, int lane) {
+    const float m = __shfl_sync(0xffffffffu, sel_v, 0);
+    const float ex = lane < K ? expf(sel_v - m) : 0.f;
+    float s = 0.f;
+    for (int k = 0; k < K; ++k) s += __shfl_sync(0xffffffffu, ex, k);
+    return ex / s;
+}
+
+// ---------------------------------------------------------------- rmsnorm
+
+// Sum of squares of a token's H values with the canonical 256-lane order:
+// thread i (0..255) accumulates h = i, i+256, ... with fmaf, then a butterfly per
+// warp, then the 8 warp sums in warp order.
+constexpr int kNormThreads = 256;
+
+}  // namespace moe

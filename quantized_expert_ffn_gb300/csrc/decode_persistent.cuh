@@ -1,0 +1,59 @@
+// decode_persistent.cuh -- arguments of the persistent decode kernel.
+#pragma once
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+constexpr int kPersistThreads = 512;
+constexpr int kMaxTok = 8;             // tokens per window on this path
+constexpr int kMaxPersistLayers = 48;  // layers per launch (longer stacks: several launches)
+constexpr size_t kRedBytes = 4 * 4 * 32 * 8 * sizeof(float);
+
+// Dynamic shared memory: [wr: router rows][xs][u] during the input, router, top-K
+// and gate/up phases; during the down phase [wr][hst: h limbs][yp: partial sums]
+// (hst and yp reuse the space of xs and u).
+struct PersistGeom {
+    size_t off_wr, off_xs, off_u, off_hst, off_yp;
+    size_t hst_bytes;  // 0: the down phase reads h from global memory
+    size_t bytes;      // dynamic + static shared memory of the kernel
+    size_t dyn_bytes;  // dynamic part
+};
+
+struct PersistLayer {
+    const void *Wr;         // router rows [E][H] (16-byte aligned)
+    const float *bias;      // [E] or null
+    const int32_t *table;   // slot table of the layer's slots object
+    int layer, capacity;    // row of the table; slots in the pool
+    const uint8_t *arena;   // slot 0 of the pool
+    long long stride;       // bytes per slot
+    const uint8_t *shared;  // shared expert (device layout) or null
+};
+
+struct PersistArgs {
+    int n_layers, T, H, E, K, act, stack, wr_bf16, x_f32;
+    float eps;
+    QLayout L, LS;
+    Unpack un, un_s;
+    PersistGeom geom;
+    const void *x;        // single layer: input [T][H]
+    float *y;             // single layer: output [T][H]
+    float *resid;         // stack: residual [T][H], updated in place
+    float *logits;        // [T][E] (scratch, or the caller's logits_out)
+    float *trace_logits;  // stack: [n_layers][T][E] or null
+    __nv_bfloat16 *trace_in;  // stack: [n_layers][T][H] or null
+    int32_t *ids_out;     // single layer: [T][K] or null
+    __nv_bfloat16 *h_hi, *h_lo;  // [T*K + T][h_ld]
+    int h_ld;
+    unsigned *bar;        // [2]: arrivals, abort (zeroed before each launch)
+    uint32_t *status;
+    PersistLayer layers[kMaxPersistLayers];
+};
+static_assert(sizeof(PersistArgs) <= 4096, "kernel parameters must fit in 4 KB");
+
+PersistGeom persist_geom(int T, int H, int E, int K, int F, int F_shared, int wr_bytes, int G, size_t max_smem);
+int launch_decode_persistent(const PersistArgs &a, int G, cudaStream_t s);
+int persist_max_ctas(int smem_bytes, int *G);
+int init_persist_attributes(int max_smem);
+
+}  // namespace moe

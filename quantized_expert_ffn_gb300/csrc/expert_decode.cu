@@ -20,116 +20,39 @@
 //   k_combine: y[t] = sum_k w[t][k] y_pair[t*K+k] in k order (+ shared expert).
 // fp32 inputs (x of fp32 layers, and h) enter as two bf16 limbs hi + lo in
 // separate B columns, so a group holds at most 4 such columns.
-#include "moe_internal.cuh"
+#include "decode_common.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = kGuSplit;
 
-template <int KIND>
-struct ChunkRegs;
-template <>
-struct ChunkRegs<MOE_Q2_64> {
-    uint32_t w[4];
-    uint32_t s[2];
-};
-template <>
-struct ChunkRegs<MOE_Q4_32> {
-    uint32_t w[8];
-    uint32_t s[4];
-};
-
-// codes at `cp`, scales at `sp`, for lane `lane`
-template <int KIND>
-__device__ __forceinline__ void load_chunk(const uint8_t *cp, const uint8_t *sp, bool half, int lane,
-                                           ChunkRegs<KIND> &r) {
-    const int g = lane >> 2;
-    if constexpr (KIND == MOE_Q2_64) {
-        if (!half) {
-            const uint4 v = ldg_stream16(cp + 16 * lane);
-            r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
-            r.s[0] = ldg_stream4(sp + 4 * g);
-            r.s[1] = ldg_stream4(sp + 4 * (8 + g));
-        } else {
-            const uint2 v = ldg_stream8(cp + 8 * lane);
-            r.w[0] = v.x; r.w[1] = v.y; r.w[2] = 0; r.w[3] = 0;
-            r.s[0] = ldg_stream4(sp + 4 * g);
-            r.s[1] = 0;
-        }
-    } else {
-        const uint4 v = ldg_stream16(cp + 16 * lane);
-        r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
-        r.s[0] = ldg_stream4(sp + 4 * g);
-        r.s[1] = ldg_stream4(sp + 4 * (8 + g));
-        if (!half) {
-            const uint4 u = ldg_stream16(cp + 512 + 16 * lane);
-            r.w[4] = u.x; r.w[5] = u.y; r.w[6] = u.z; r.w[7] = u.w;
-            r.s[2] = ldg_stream4(sp + 4 * (16 + g));
-            r.s[3] = ldg_stream4(sp + 4 * (24 + g));
-        } else {
-            r.w[4] = r.w[5] = r.w[6] = r.w[7] = 0;
-            r.s[2] = r.s[3] = 0;
-        }
-    }
-}
-
-__device__ __forceinline__ void apply_scale(uint32_t s, float blk[4], float acc[4]) {
-    const float lo = __half2float(__ushort_as_half((unsigned short)(s & 0xFFFFu)));
-    const float hi = __half2float(__ushort_as_half((unsigned short)(s >> 16)));
-    acc[0] = fmaf(lo, blk[0], acc[0]);
-    acc[1] = fmaf(lo, blk[1], acc[1]);
-    acc[2] = fmaf(hi, blk[2], acc[2]);
-    acc[3] = fmaf(hi, blk[3], acc[3]);
-    blk[0] = blk[1] = blk[2] = blk[3] = 0.f;
-}
-
-// NMAT matrices of one chunk against the B columns in shared memory
-// (xrow = xs + g*ldx + 2c, indexed by the chunk's absolute k).
-template <int KIND, int NMAT>
-__device__ __forceinline__ void mma_chunk(const ChunkRegs<KIND> (&r)[NMAT], bool half, const __nv_bfloat16 *xrow,
-                                          int k0, const Unpack &un, float (&acc)[NMAT][4]) {
-    float blk[NMAT][4];
+// Stream chunks [c_begin, c_end) of one tile through a window of W chunks held
+// in registers (loads for the next W chunks are in flight while one computes).
+template <int KIND, int NMAT, int NB, int W>
+__device__ __forceinline__ void stream_chunks(const uint8_t *tile_ptr, int chunk_bytes, int cb, int sb,
+                                              int c_begin, int c_end, int n_chunks, bool has_half,
+                                              const BTile (&bt)[NB], const Unpack &un, int lane,
+                                              float (&acc)[NMAT][NB][4]) {
+    ChunkRegs<KIND> buf[W][NMAT];
+    auto load = [&](int ch, ChunkRegs<KIND>(&r)[NMAT]) {
+        const bool half = has_half && ch == n_chunks - 1;
+        const int cbh = half ? cb / 2 : cb, sbh = half ? sb / 2 : sb;
+        const uint8_t *cp = tile_ptr + (long long)ch * chunk_bytes;
 #pragma unroll
-    for (int m = 0; m < NMAT; ++m) blk[m][0] = blk[m][1] = blk[m][2] = blk[m][3] = 0.f;
-    if constexpr (KIND == MOE_Q2_64) {
-        const int nwords = half ? 2 : 4;
+        for (int m = 0; m < NMAT; ++m) load_chunk<KIND>(cp + m * cbh, cp + NMAT * cbh + m * sbh, half, lane, r[m]);
+    };
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (i >= nwords) break;
-            uint32_t R[NMAT][8];
+    for (int j = 0; j < W; ++j)
+        if (c_begin + j < c_end) load(c_begin + j, buf[j]);
+    for (int base = c_begin; base < c_end; base += W) {
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m) unpack_q2(r[m].w[i], un, R[m]);
-#pragma unroll
-            for (int hs = 0; hs < 2; ++hs) {
-                const int k = k0 + 16 * (2 * i + hs);
-                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(xrow + k);
-                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(xrow + k + 8);
-#pragma unroll
-                for (int m = 0; m < NMAT; ++m) mma_bf16(blk[m], &R[m][4 * hs], b0, b1, blk[m]);
-            }
-            if (i & 1) {
-#pragma unroll
-                for (int m = 0; m < NMAT; ++m) apply_scale(r[m].s[i >> 1], blk[m], acc[m]);
-            }
-        }
-    } else {
-        const int nwords = half ? 4 : 8;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (i >= nwords) break;
-            uint32_t R[NMAT][4];
-#pragma unroll
-            for (int m = 0; m < NMAT; ++m) unpack_q4(r[m].w[i], un, R[m]);
-            const int k = k0 + 16 * i;
-            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(xrow + k);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(xrow + k + 8);
-#pragma unroll
-            for (int m = 0; m < NMAT; ++m) mma_bf16(blk[m], R[m], b0, b1, blk[m]);
-            if (i & 1) {
-#pragma unroll
-                for (int m = 0; m < NMAT; ++m) apply_scale(r[m].s[i >> 1], blk[m], acc[m]);
+        for (int j = 0; j < W; ++j) {
+            const int ch = base + j;
+            if (ch < c_end) {
+                mma_chunk<KIND, NMAT, NB>(buf[j], has_half && ch == n_chunks - 1, bt, ch * 128, un, acc);
+                if (ch + W < c_end) load(ch + W, buf[j]);
             }
         }
     }
@@ -219,29 +142,18 @@ __global__ void __launch_bounds__(32 * kWarps) k_gateup(ExpertArgs a) {
 
     const Unpack un = tk.shared ? a.un_s : a.un;
     const int g = lane >> 2, c = lane & 3;
-    const __nv_bfloat16 *xrow = xs + (size_t)g * ldx + 2 * c;
+    const BTile bt[1] = {{xs + (size_t)g * ldx + 2 * c, true}};
     const int n_chunks = L.gu_chunks;
-    const int c_begin = warp * n_chunks / kWarps, c_end = (warp + 1) * n_chunks / kWarps;
+    const int c_begin = gu_chunk_begin(warp, n_chunks), c_end = gu_chunk_begin(warp + 1, n_chunks);
     const uint8_t *tile_ptr = tk.wbase + (long long)tk.tile * L.gu_tile_bytes;
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    ChunkRegs<KIND> cur[2], nxt[2];
-    auto load = [&](int ch, ChunkRegs<KIND>(&r)[2]) {
-        const bool half = L.gu_half && ch == n_chunks - 1;
-        const int cb = half ? L.cb / 2 : L.cb, sb = half ? L.sb / 2 : L.sb;
-        const uint8_t *cp = tile_ptr + (long long)ch * L.gu_chunk_bytes;
-        load_chunk<KIND>(cp, cp + 2 * cb, half, lane, r[0]);
-        load_chunk<KIND>(cp + cb, cp + 2 * cb + sb, half, lane, r[1]);
-    };
-    if (c_begin < c_end) load(c_begin, cur);
-    for (int ch = c_begin; ch < c_end; ++ch) {
-        if (ch + 1 < c_end) load(ch + 1, nxt);
-        const bool half = L.gu_half && ch == n_chunks - 1;
-        mma_chunk<KIND, 2>(cur, half, xrow, ch * 128, un, acc);
-        if (ch + 1 < c_end) {
-            cur[0] = nxt[0];
-            cur[1] = nxt[1];
-        }
-    }
+    float acc3[2][1][4] = {};
+    stream_chunks<KIND, 2, 1, 2>(tile_ptr, L.gu_chunk_bytes, L.cb, L.sb, c_begin, c_end, n_chunks, L.gu_half, bt,
+                                 un, lane, acc3);
+    float acc[2][4];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[m][q] = acc3[m][0][q];
     // fixed-order sum over the 4 warps
 #pragma unroll
     for (int m = 0; m < 2; ++m)
@@ -267,7 +179,7 @@ __global__ void __launch_bounds__(32 * kWarps) k_gateup(ExpertArgs a) {
         const int rr = g + 8 * (q >> 1), j = 2 * c + (q & 1);
         if (j >= ncols) continue;
         const float gv = v[q], uv = v[4 + q];
-        const float act = a.act == MOE_ACT_GEGLU_TANH ? gelu_tanh_f(gv) : silu_f(gv);
+        const float act = act_f(a.act, gv);
         const int row = col_row(a.cols[tk.grp.col0 + j], a.T, a.K);
         a.h[(size_t)row * a.h_ld + tk.tile * 16 + rr] = act * uv;
     }
@@ -312,24 +224,14 @@ __global__ void __launch_bounds__(32 * kWarps) k_down(ExpertArgs a) {
     if (tile >= L.d_tiles) return;
     const Unpack un = tk.shared ? a.un_s : a.un;
     const int g = lane >> 2, c = lane & 3;
-    const __nv_bfloat16 *xrow = xs + (size_t)g * ldx + 2 * c;
-    const int n_chunks = L.d_chunks;
+    const BTile bt[1] = {{xs + (size_t)g * ldx + 2 * c, true}};
     const uint8_t *tile_ptr = tk.wbase + L.d_offset + (long long)tile * L.d_tile_bytes;
-    float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
-    ChunkRegs<KIND> cur[1], nxt[1];
-    auto load = [&](int ch, ChunkRegs<KIND>(&r)[1]) {
-        const bool half = L.d_half && ch == n_chunks - 1;
-        const int cb = half ? L.cb / 2 : L.cb;
-        const uint8_t *cp = tile_ptr + (long long)ch * L.d_chunk_bytes;
-        load_chunk<KIND>(cp, cp + cb, half, lane, r[0]);
-    };
-    load(0, cur);
-    for (int ch = 0; ch < n_chunks; ++ch) {
-        if (ch + 1 < n_chunks) load(ch + 1, nxt);
-        const bool half = L.d_half && ch == n_chunks - 1;
-        mma_chunk<KIND, 1>(cur, half, xrow, ch * 128, un, acc);
-        if (ch + 1 < n_chunks) cur[0] = nxt[0];
-    }
+    float acc3[1][1][4] = {};
+    stream_chunks<KIND, 1, 1, 2>(tile_ptr, L.d_chunk_bytes, L.cb, L.sb, 0, L.d_chunks, L.d_chunks, L.d_half, bt, un,
+                                 lane, acc3);
+    float acc[1][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[0][q] = acc3[0][0][q];
     float v[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) v[q] = acc[0][q] + __shfl_xor_sync(0xffffffffu, acc[0][q], 2);
@@ -419,7 +321,10 @@ int init_expert_attributes(int max_smem) {
     const void *ks[] = {(const void *)k_gateup<MOE_Q2_64, true>, (const void *)k_gateup<MOE_Q2_64, false>,
                         (const void *)k_gateup<MOE_Q4_32, true>, (const void *)k_gateup<MOE_Q4_32, false>,
                         (const void *)k_down<MOE_Q2_64>, (const void *)k_down<MOE_Q4_32>};
-    for (const void *k : ks) MOE_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem));
+    for (const void *k : ks) {
+        int rc = set_max_dynamic_smem(k, max_smem);
+        if (rc) return rc;
+    }
     return MOE_OK;
 }
 

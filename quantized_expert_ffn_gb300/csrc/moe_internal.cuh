@@ -268,6 +268,9 @@ struct ExpertArgs {
     uint32_t *status;
 };
 
+// Allow `kernel` the opt-in maximum of dynamic shared memory left beside its
+// static shared memory.
+int set_max_dynamic_smem(const void *kernel, int max_smem);
 int init_router_attributes(int max_smem);
 int init_bucket_attributes(int max_smem);
 int init_expert_attributes(int max_smem);

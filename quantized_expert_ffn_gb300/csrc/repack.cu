@@ -126,8 +126,7 @@ __global__ void k_repack_tile(QLayout L, const uint8_t *blob, uint8_t *dst, int 
 }  // namespace
 
 int init_repack_attributes(int max_smem) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(k_repack_tile, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem));
-    return MOE_OK;
+    return set_max_dynamic_smem((const void *)k_repack_tile, max_smem);
 }
 
 int repack_expert(const QLayout &L, const uint8_t *blob, uint8_t *dst, cudaStream_t stream) {
