@@ -168,6 +168,7 @@ def run_ours(args, rank, world, local_rank):
         L.moe_stack_forward(ctx, st.descs, resid, EPS, ws)
     stream.synchronize()
     assert L.moe_status(ctx, stream) == 0
+    path = "persistent" if L.moe_ctx_get_option(ctx, L.OPT_LAST_PATH) == 1 else "multi-kernel"
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         L.moe_stack_forward(ctx, st.descs, resid, EPS, ws)
@@ -227,7 +228,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
     ms, e2e_ms_max = float(times[0]), float(times[1])
-    return dict(ms=ms, e2e_ms=e2e_ms_max, layer_ms=layer_ms, clocks=clocks, status=status, cfg=cfg)
+    return dict(ms=ms, e2e_ms=e2e_ms_max, layer_ms=layer_ms, clocks=clocks, status=status, cfg=cfg, path=path)
 
 
 # ------------------------------------------------------------------ oracle (CPU)
@@ -310,7 +311,10 @@ def main():
     graph_layer_ms = r["ms"] / args.steps / args.layers
     achieved = layer_bytes / (graph_layer_ms / 1e3) / 1e9
     step_expert_gbs = args.layers * cfg.K * expert_bytes / (r["ms"] / args.steps / 1e3) / 1e9
-    launches_per_layer = 8  # rmsnorm, router, top-k, bucket, plan, gate/up, down, combine
+    # kernels of ours per step: the persistent path runs the whole 48-layer chain as
+    # one cooperative kernel (plus a memset of its barrier words); the multi-kernel
+    # path runs rmsnorm, router, top-k, bucket, plan, gate/up, down, combine per layer
+    launches_per_step = 1 if r["path"] == "persistent" else 8 * args.layers
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": n_gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True,
@@ -320,14 +324,16 @@ def main():
         "expert_weight_gbs": step_expert_gbs if T == 1 else None,
         "expert_weight_frac_of_hbm": (step_expert_gbs / hbm_peak) if T == 1 else None,
         "eager_layer_ms": r["layer_ms"],
-        "roofline": {"kernel": "one MoE layer call (8 launches, in the captured step graph)",
+        "roofline": {"kernel": ("k_decode (persistent, one launch per step), per layer" if r["path"] == "persistent"
+                                else "one MoE layer call (8 launches, in the captured step graph)"),
                      "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": None,
                      "peak_source": "measured" if pk else "fallback",
                      "algorithmic_bytes_per_launch": layer_bytes},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * cfg.H * 4,
                 "d2h_bytes_per_step": T * cfg.H * 4},
-        "gpu_launches": launches_per_layer * args.layers * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
+        "path": r["path"],
         "clocks": r["clocks"],
         "device_status": r["status"],
     }

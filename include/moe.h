@@ -112,6 +112,15 @@ MOE_API int moe_ctx_destroy(moe_ctx *ctx);
 #define MOE_OPT_PERSISTENT_DECODE 1
 MOE_API int moe_ctx_set_option(moe_ctx *ctx, int option, int value);
 
+/* Read a context option into *value. Besides MOE_OPT_PERSISTENT_DECODE:
+ * MOE_OPT_LAST_PATH (read only): 1 if the last moe_layer_forward*,
+ * moe_layer_forward_static or moe_stack_forward* call on this context ran the
+ * persistent kernel, 0 if it ran the multi-kernel path (or no such call yet).
+ * MOE_ERR_ARG for an unknown option or a null pointer; setting
+ * MOE_OPT_LAST_PATH is MOE_ERR_ARG too. */
+#define MOE_OPT_LAST_PATH 2
+MOE_API int moe_ctx_get_option(moe_ctx *ctx, int option, int *value);
+
 /* Synchronise `stream`, then read and clear the device status bits into *bits.
  * Returns MOE_OK even when bits are set; the caller inspects them. */
 MOE_API int moe_status(moe_ctx *ctx, moe_stream_t stream, uint32_t *bits);

@@ -49,6 +49,7 @@ _SIGS = {
     "moe_ctx_destroy": [_P],
     "moe_status": [_P, _P, ctypes.POINTER(ctypes.c_uint32)],
     "moe_ctx_set_option": [_P, _I, _I],
+    "moe_ctx_get_option": [_P, _I, ctypes.POINTER(_I)],
     "moe_expert_bytes": [Format, _I, _I, ctypes.POINTER(_SZ)],
     "moe_arena_create": [_P, _SZ, ctypes.POINTER(_P)],
     "moe_arena_destroy": [_P],
@@ -138,10 +139,17 @@ def moe_ctx_destroy(ctx: int):
 
 
 OPT_PERSISTENT_DECODE = 1
+OPT_LAST_PATH = 2
 
 
 def moe_ctx_set_option(ctx: int, option: int, value: int):
     _check(load().moe_ctx_set_option(ctx, option, value))
+
+
+def moe_ctx_get_option(ctx: int, option: int) -> int:
+    out = _I()
+    _check(load().moe_ctx_get_option(ctx, option, ctypes.byref(out)))
+    return out.value
 
 
 def moe_status(ctx: int, stream=None) -> int:

@@ -13,6 +13,7 @@ struct moe_ctx {
     int device;
     uint32_t *d_status;
     int persistent;  // MOE_OPT_PERSISTENT_DECODE
+    int last_path;   // MOE_OPT_LAST_PATH
     int max_smem;    // opt-in shared memory per block
 };
 
@@ -86,6 +87,7 @@ int check_dims(int H, int F) {
 struct WsLayout {
     size_t logits, ids, w, counts, offsets, perm, active, n_active, live, cols, groups_gu, groups_d, n_groups, h, yp,
         u, bar, total;
+    int sync_words;  // persistent path: barrier words + down tile counters
     int max_routed_gu, max_routed_d, max_shared, h_ld;
 };
 
@@ -117,7 +119,8 @@ WsLayout ws_layout(const moe_layer_desc *d, int T, int nc_gu) {
     W.h = take((P + T) * (size_t)W.h_ld * 4);
     W.yp = take((P + T) * (size_t)d->H * 4);
     W.u = take((size_t)T * d->H * 2);
-    W.bar = take(16);
+    W.sync_words = 4 + d->H / 16;
+    W.bar = take((size_t)W.sync_words * 4);
     W.total = o;
     return W;
 }
@@ -230,6 +233,7 @@ int try_persistent(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers, boo
                    moe_dtype xt, int T, float *out, float *logits_out, int32_t *ids_out, void *trace_in,
                    float *trace_logits, float eps, uint8_t *ws, const WsLayout &W, cudaStream_t s, bool *used) {
     *used = false;
+    ctx->last_path = 0;
     if (!ctx->persistent || T < 1 || T > kMaxTok || (xt == MOE_F32 && T > 4)) return MOE_OK;
     const moe_layer_desc &d0 = layers[0];
     if (d0.K * T > 256) return MOE_OK;
@@ -252,9 +256,10 @@ int try_persistent(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers, boo
     // the grid is one CTA per SM; the geometry depends on it through the router rows
     int sms = 0;
     MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device));
-    PersistGeom geom = persist_geom(T, d0.H, d0.E, d0.K, d0.F, d0.shared ? d0.F_shared : 0, wr_bytes, sms,
-                                    (size_t)ctx->max_smem);
-    if (geom.bytes > (size_t)ctx->max_smem) return MOE_OK;
+    if (d0.H > 3072 || d0.F > 3072 || (d0.shared && d0.F_shared > 4096)) return MOE_OK;
+    PersistGeom geom = persist_geom(s0->fmt.kind, T, d0.H, d0.E, d0.K, d0.F, d0.shared ? d0.F_shared : 0, wr_bytes,
+                                    xt == MOE_F32 ? 1 : 0, sms, (size_t)ctx->max_smem);
+    if (geom.ring_bytes == 0 || geom.bytes > (size_t)ctx->max_smem) return MOE_OK;
     int rc = persist_max_ctas((int)geom.bytes, &G);
     if (rc) return rc;
     if (G != sms) return MOE_OK;
@@ -286,6 +291,9 @@ int try_persistent(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers, boo
     a.h_hi = (__nv_bfloat16 *)(ws + W.h);
     a.h_lo = a.h_hi + hrows * W.h_ld;
     a.bar = (unsigned *)(ws + W.bar);
+    a.d_cnt = (int *)(ws + W.bar) + 4;
+    a.yp = (float *)(ws + W.yp);
+    a.sync_words = W.sync_words;
     a.status = ctx->d_status;
     for (int l0 = 0; l0 < n_layers; l0 += kMaxPersistLayers) {
         const int n = n_layers - l0 < kMaxPersistLayers ? n_layers - l0 : kMaxPersistLayers;
@@ -308,6 +316,7 @@ int try_persistent(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers, boo
         if (rc) return rc;
     }
     *used = true;
+    ctx->last_path = 1;
     return MOE_OK;
 }
 
@@ -386,7 +395,7 @@ int moe_ctx_create(int device, moe_ctx **out) {
         return set_error(MOE_ERR_CUDA, "no CUDA device %d (%d visible)", device, n);
     DeviceGuard g(device);
     if (!g.ok) return set_error(MOE_ERR_CUDA, "cudaSetDevice(%d) failed", device);
-    moe_ctx *c = new moe_ctx{device, nullptr, 1, 0};
+    moe_ctx *c = new moe_ctx{device, nullptr, 1, 0, 0};
     cudaError_t e = cudaMalloc(&c->d_status, sizeof(uint32_t));
     if (e != cudaSuccess) {
         delete c;
@@ -433,6 +442,20 @@ int moe_ctx_set_option(moe_ctx *ctx, int option, int value) {
     if (!ctx) return set_error(MOE_ERR_ARG, "null context");
     if (option == MOE_OPT_PERSISTENT_DECODE) {
         ctx->persistent = value != 0;
+        return MOE_OK;
+    }
+    if (option == MOE_OPT_LAST_PATH) return set_error(MOE_ERR_ARG, "option %d is read only", option);
+    return set_error(MOE_ERR_ARG, "unknown option %d", option);
+}
+
+int moe_ctx_get_option(moe_ctx *ctx, int option, int *value) {
+    if (!ctx || !value) return set_error(MOE_ERR_ARG, "null argument");
+    if (option == MOE_OPT_PERSISTENT_DECODE) {
+        *value = ctx->persistent;
+        return MOE_OK;
+    }
+    if (option == MOE_OPT_LAST_PATH) {
+        *value = ctx->last_path;
         return MOE_OK;
     }
     return set_error(MOE_ERR_ARG, "unknown option %d", option);

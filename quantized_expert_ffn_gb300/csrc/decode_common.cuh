@@ -140,10 +140,16 @@ __device__ __forceinline__ void mma_chunk(const ChunkRegs<KIND> (&r)[NMAT], bool
     }
 }
 
-// The canonical split of a gate/up row tile's chunks over 4 warps: warp w sums
-// chunks [w*n/4, (w+1)*n/4), and the four partial sums are added in warp order.
-constexpr int kGuSplit = 4;
-__device__ __forceinline__ int gu_chunk_begin(int w, int n) { return w * n / kGuSplit; }
+// The canonical split of a gate/up row tile's chunks into parts: part w sums
+// chunks [w*n/S, (w+1)*n/S) and the S partial sums are added in part order
+// (((p0 + p1) + p2) + ...). S = 4 for Q2 (1,152-byte chunks) and 8 for Q4
+// (2,304-byte chunks), so a part is at most ~7 KB for H <= 3072.
+template <int KIND>
+struct GuSplit {
+    static constexpr int S = KIND == MOE_Q2_64 ? 4 : 8;
+};
+__host__ __device__ __forceinline__ int gu_split(int kind) { return kind == MOE_Q2_64 ? 4 : 8; }
+__device__ __forceinline__ int gu_chunk_begin(int w, int n, int S) { return w * n / S; }
 
 // bf16 hi/lo limbs of an fp32 value
 __device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
@@ -238,17 +244,18 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
 // Top-K on 64-bit keys that order exactly like ranks_before: the high word maps
 // the fp32 value monotonically to an unsigned integer (NaN lowest, -0 == +0), the
 // low word is ~index (the lower index wins a tie). Key 0 means "no candidate".
-__device__ __forceinline__ unsigned long long topk_key(float v, int idx) {
+__device__ __forceinline__ uint32_t topk_ord(float v) {
+    if (isnan(v)) return 0u;
     uint32_t b = __float_as_uint(v);
-    uint32_t ord;
-    if (isnan(v)) {
-        ord = 0;
-    } else {
-        if (v == 0.f) b = 0;
-        ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    }
+    if (v == 0.f) b = 0;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned long long topk_key_of(uint32_t ord, int idx) {
     return ((unsigned long long)ord << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)idx);
 }
+
+__device__ __forceinline__ unsigned long long topk_key(float v, int idx) { return topk_key_of(topk_ord(v), idx); }
 
 __device__ __forceinline__ int topk_key_index(unsigned long long k) {
     return k ? (int)(0xFFFFFFFFu - (uint32_t)k) : -1;
@@ -335,9 +342,28 @@ __device__ __forceinline__ float topk_weight(float sel_v, int K, int lane) {
 
 // ---------------------------------------------------------------- rmsnorm
 
-// Sum of squares of a token's H values with the canonical 256-lane order:
-// thread i (0..255) accumulates h = i, i+256, ... with fmaf, then a butterfly per
-// warp, then the 8 warp sums in warp order.
-constexpr int kNormThreads = 256;
+// RMSNorm with the canonical 512-lane order: thread i (0..511) accumulates x_h^2
+// for h = i, i+512, ... with fmaf, an xor butterfly sums each warp, and the 16
+// warp sums are added in warp order; r = 1 / sqrt(sum / H + eps) and the output
+// is bf16(x_h * r).
+constexpr int kNormThreads = 512;
+constexpr int kNormWarps = kNormThreads / 32;
+
+// Warp-reduced partial of thread `tid` (identical in every lane of its warp).
+__device__ __forceinline__ float rms_partial(const float *xt, int H, int tid) {
+    float acc = 0.f;
+    for (int h = tid; h < H; h += kNormThreads) acc = fmaf(xt[h], xt[h], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc;
+}
+
+// Scale from the 16 warp partials.
+__device__ __forceinline__ float rms_scale(const float *wsum, int H, float eps) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kNormWarps; ++w) tot += wsum[w];
+    return 1.0f / sqrtf(tot / (float)H + eps);
+}
 
 }  // namespace moe

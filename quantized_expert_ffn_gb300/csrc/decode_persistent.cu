@@ -1,28 +1,44 @@
 // decode_persistent.cu -- one cooperative launch per decode step: every SM runs
-// one CTA that walks through all the layers of the step, phase by phase, with a
-// grid barrier between phases that depend on each other.
+// one CTA that walks through all the layers of the step, phase by phase.
 //
 // Per layer (Krasis white paper sec. 5.3; kairos-engine README "The MoE forward"):
 //   N  layer input: x (single layer) or u = bf16(RMSNorm(resid)) (stack), every
-//      CTA for itself (no barrier needed: all read the same resid);
-//   R  router logits: CTA c owns experts c, c+G, ...; their router rows were
-//      prefetched into shared memory while the previous layer ran;
-//   -- barrier --
-//   T  top-K, weights and the plan (distinct experts, their live columns): every
-//      CTA computes the same result from the logits, so no further barrier;
-//   GU gate/up items (16 rows of one expert, all H) are dealt round-robin over
-//      CTAs and over the 4 quads of 4 warps in a CTA; each warp streams a quarter
-//      of the item's chunks through registers; h = act(gate) * up;
-//   -- barrier --
-//   D  output row tiles (16 rows x all chosen experts) are dealt over CTAs; the
-//      warps of a CTA share the experts; the combine adds the experts in k order
+//      CTA for itself from the same resid;
+//   R  router logits: CTA c owns experts c, c+G, ...; four warps share a row; the
+//      rows, bias and slot-table row were prefetched into shared memory during the
+//      previous layer, and the next layer's are requested as soon as R is done;
+//   -- grid barrier --
+//   T  top-K, weights and the plan, every CTA the same result from the logits: the
+//      K-th largest of a few segment maxima is a threshold, the experts at or above
+//      it are ranked exactly; the distinct live experts and their columns; the
+//      split of the down work over the CTAs;
+//   GU gate/up items (16 rows of one expert, all of H) are dealt round-robin over
+//      CTAs and over the groups of S warps of a CTA (S = 4 for Q2, 8 for Q4); warp
+//      q of a group sums part q of H; the group adds the parts in order and applies
+//      the activation;
+//   -- grid barrier --
+//   D  down units (one expert x 16 output rows) in expert order, split over the
+//      CTAs so that gate/up plus down bytes are even, then over the CTA's warps;
+//      h of the CTA's experts is staged in shared memory; the last unit of a row
+//      tile to arrive (atomic ticket, no waiting) combines the experts in k order
 //      (+ the shared expert) and writes y, or adds into resid;
-//   -- barrier (stack only) --
+//   -- grid barrier (stack only) --
 //
-// Arithmetic per output element is exactly that of the multi-kernel path
-// (same device functions, same split of the reduction, same orders), so results
-// match it bit for bit. Waits are bounded: a barrier that does not complete
-// within about a second sets MOE_STATUS_TIMEOUT and every CTA leaves.
+// Weights move through one ring per warp in shared memory, filled by bulk copies
+// (TMA, cp.async.bulk, completion counted on an mbarrier) of a few chunks each, in
+// the order the warp consumes them: its gate/up chunks, then its down chunks. One
+// lane issues a copy and nobody waits for the issue; a down chunk does not depend
+// on h, so a warp requests its down weights as soon as ring space frees up during
+// gate/up, and the whole layer's expert bytes are in flight from the moment the
+// plan is known.
+//
+// Arithmetic per output element is that of the multi-kernel path (same device
+// functions, same splits of the reductions, same orders), so results match it bit
+// for bit. Every wait is bounded: a barrier or a copy that does not complete in
+// about a second sets MOE_STATUS_TIMEOUT and the CTAs stop at the next barrier;
+// before a warp leaves it waits (bounded) for every copy it issued.
+#include <type_traits>
+
 #include "decode_common.cuh"
 #include "decode_persistent.cuh"
 
@@ -33,11 +49,22 @@ namespace {
 constexpr int kPWarps = kPersistThreads / 32;
 constexpr long long kSpinCycles = 2000000000LL;  // about 1 s at GB300 clocks
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
+// Static shared memory: the plan of the current layer and small per-CTA state.
+struct alignas(16) Plan {
+    int ids[256], live[256], sorted[256], cols[256], cexp[256], cslot[256];
+    float w[256];
+    int ustart[264], uexp[264], uslot[264];
+    // 0: distinct live experts, 1: live pairs, 2: stop flag, 4..11: token t has a
+    // non-finite logit, 12 / 13: first / end down unit of this CTA
+    int misc[16];
+    int ncand[kMaxTok];
+    uint32_t theta[kMaxTok];
+    float bias[2][16];                    // router bias of this CTA's experts, by layer parity
+    float rpart[16][kMaxTok][4];          // router partial sums [row][token][warp]
+    float wsum[kMaxTok][kNormWarps];      // RMSNorm warp sums
+    unsigned long long sel[kMaxTok][32];  // chosen keys per token, rank order
+    uint64_t ring_bar[kPersistThreads / 32][8];  // weight-ring mbarriers per warp
+};
 
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p) {
     unsigned v;
@@ -56,17 +83,8 @@ __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Ask L2 to fetch [p, p + bytes) from HBM (bytes a multiple of 16, p 16-aligned).
-__device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void quad_sync(int quad) {
-    asm volatile("bar.sync %0, 128;" ::"r"(quad + 1) : "memory");
-}
-
 // Barrier over all CTAs of the (co-resident) grid. bar[0] counts arrivals
-// monotonically within the launch; bar[1] is the abort word. Returns false when
+// monotonically within the launch; bar[1] is the stop word. Returns false when
 // the kernel must stop (this or another CTA gave up waiting).
 __device__ bool grid_sync(unsigned *bar, unsigned &target, uint32_t *status, int *s_flag) {
     target += gridDim.x;
@@ -77,46 +95,182 @@ __device__ bool grid_sync(unsigned *bar, unsigned &target, uint32_t *status, int
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
         const long long t0 = clock64();
         int stop = 0;
-        while ((int)(ld_acquire_u32(bar) - target) < 0) {
-            if (ld_relaxed_u32(bar + 1)) {
-                stop = 1;
-                break;
-            }
-            if (clock64() - t0 > kSpinCycles) {
-                atomicExch(bar + 1, 1u);
-                set_status(status, MOE_STATUS_TIMEOUT);
-                stop = 1;
-                break;
+        // the stop word is set only by a CTA that gave up, and then the count never
+        // completes: it needs checking only while waiting
+        for (unsigned it = 0; (int)(ld_relaxed_u32(bar) - target) < 0; ++it) {
+            if ((it & 63) == 63) {
+                if (ld_relaxed_u32(bar + 1)) {
+                    stop = 1;
+                    break;
+                }
+                if (clock64() - t0 > kSpinCycles) {
+                    atomicExch(bar + 1, 1u);
+                    set_status(status, MOE_STATUS_TIMEOUT);
+                    stop = 1;
+                    break;
+                }
             }
         }
+        // acquire: the other CTAs' writes before their arrivals are visible to this CTA
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
         *s_flag = stop;
     }
     __syncthreads();
     return *s_flag == 0;
 }
 
-// Dynamic shared memory: [xs: 8 rows x (H+8) bf16][wr: router rows of this
-// CTA][u: top-k candidates | (gate/up reduction + down partial sums)]; offsets in
-// PersistGeom (identical on host and device). The plan lives in static arrays.
-struct Plan {
-    int ids[256], live[256], sorted[256], cols[256], cexp[256], cslot[256];
-    float w[256];
-    int ustart[264], uexp[264], uslot[264];
-    int misc[16];
-    alignas(16) int32_t table[1024];  // slot-table row of the current layer
-    float bias[16];                   // router bias of this CTA's experts
-    float rpart[16][kMaxTok][4];      // router partial sums [row][token][warp]
-    unsigned long long sel[kMaxTok][32];  // chosen keys per token, rank order  // 0: distinct live experts, 1: live pairs, 2: stop flag, 4..11: bad token
+// ------------------------------------------------------------------ weight ring
+// One ring of R bytes per warp. A piece (a few consecutive chunks of one tile, a
+// contiguous chunk image in global memory) is copied by one bulk copy that
+// completes on one of the warp's kRingBars mbarriers; pieces are consumed in
+// issue order. A piece that would cross the end of the ring starts at the next
+// lap; producer and consumer apply the same rule to the same piece sizes, so they
+// agree on every placement.
+constexpr int kRingBars = 8;  // pieces in flight per warp
+
+__device__ __forceinline__ unsigned smem_u32(const void *p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *m, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(m)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *m, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(m)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *m, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(m)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of parity `parity` to complete; false after about a second.
+__device__ __forceinline__ bool mbar_wait(uint64_t *m, unsigned parity) {
+    if (mbar_try_wait(m, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(m, parity))
+        if (clock64() - t0 > kSpinCycles) return false;
+    return true;
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *m) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(m))
+                 : "memory");
+}
+
+struct Ring {
+    uint8_t *base;
+    uint64_t *bar;         // kRingBars mbarriers
+    int R;                 // bytes
+    int head, tail;        // bytes taken / released (monotonic, lap padding included)
+    int issued, consumed;  // pieces
+    int front;             // counter value of the piece being consumed
 };
 
-// Prefetch the router rows this CTA owns for layer l into shared memory.
+__device__ __forceinline__ int ring_place(int at, int bytes, int R) {
+    const int pos = at % R;
+    return pos + bytes > R ? at + (R - pos) : at;
+}
+
+// Request `bytes` from src as the next piece; false (nothing issued) if the ring
+// has no room. Every lane of the warp calls it with the same arguments.
+__device__ __forceinline__ bool ring_push(Ring &r, const uint8_t *src, int bytes, int lane) {
+    if (r.issued - r.consumed >= kRingBars) return false;
+    if (r.issued == r.consumed) r.head = r.tail = 0;  // empty: start at offset 0 (a piece <= R always fits)
+    const int at = ring_place(r.head, bytes, r.R);
+    if (at + bytes - r.tail > r.R) return false;
+    if (lane == 0) {
+        uint64_t *m = r.bar + r.issued % kRingBars;
+        // the warp's earlier reads of these bytes (ordered by the __syncwarp of
+        // ring_pop) come before the copy's writes
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(m, (unsigned)bytes);
+        bulk_g2s(r.base + at % r.R, src, (unsigned)bytes, m);
+    }
+    r.head = at + bytes;
+    ++r.issued;
+    return true;
+}
+
+// Wait until the oldest piece (`bytes` long) has landed; its address. A copy that
+// does not land in about a second sets MOE_STATUS_TIMEOUT and the stop word.
+__device__ __forceinline__ const uint8_t *ring_front(Ring &r, int bytes, uint32_t *status, unsigned *bar) {
+    r.front = ring_place(r.tail, bytes, r.R);
+    if (!mbar_wait(r.bar + r.consumed % kRingBars, (unsigned)(r.consumed / kRingBars) & 1u)) {
+        if ((threadIdx.x & 31) == 0) {
+            set_status(status, MOE_STATUS_TIMEOUT);
+            atomicExch(bar + 1, 1u);
+        }
+    }
+    return r.base + r.front % r.R;
+}
+
+// Release the oldest piece (every lane has read what it needs from it).
+__device__ __forceinline__ void ring_pop(Ring &r, int bytes) {
+    __syncwarp();
+    r.tail = r.front + bytes;
+    ++r.consumed;
+}
+
+// Wait (bounded) for every piece still in flight.
+__device__ __forceinline__ void ring_drain(Ring &r) {
+    for (; r.consumed < r.issued; ++r.consumed)
+        mbar_wait(r.bar + r.consumed % kRingBars, (unsigned)(r.consumed / kRingBars) & 1u);
+}
+
+// Bytes of the piece of chunks [c0, c0 + nc) of a tile of n chunks (the last
+// chunk is half when has_half).
+__device__ __forceinline__ int piece_bytes(int cbytes, int has_half, int n, int c0, int nc) {
+    return nc * cbytes - ((has_half && c0 + nc == n) ? cbytes / 2 : 0);
+}
+
+// Chunk registers from shared memory (same offsets as the global layout).
+template <int KIND>
+__device__ __forceinline__ void load_chunk_s(const uint8_t *cp, const uint8_t *sp, bool half, int lane,
+                                             ChunkRegs<KIND> &r) {
+    const int g = lane >> 2;
+    if constexpr (KIND == MOE_Q2_64) {
+        if (!half) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(cp + 16 * lane);
+            r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
+            r.s[0] = *reinterpret_cast<const uint32_t *>(sp + 4 * g);
+            r.s[1] = *reinterpret_cast<const uint32_t *>(sp + 4 * (8 + g));
+        } else {
+            const uint2 v = *reinterpret_cast<const uint2 *>(cp + 8 * lane);
+            r.w[0] = v.x; r.w[1] = v.y; r.w[2] = 0; r.w[3] = 0;
+            r.s[0] = *reinterpret_cast<const uint32_t *>(sp + 4 * g);
+            r.s[1] = 0;
+        }
+    } else {
+        const uint4 v = *reinterpret_cast<const uint4 *>(cp + 16 * lane);
+        r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
+        r.s[0] = *reinterpret_cast<const uint32_t *>(sp + 4 * g);
+        r.s[1] = *reinterpret_cast<const uint32_t *>(sp + 4 * (8 + g));
+        if (!half) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(cp + 512 + 16 * lane);
+            r.w[4] = u.x; r.w[5] = u.y; r.w[6] = u.z; r.w[7] = u.w;
+            r.s[2] = *reinterpret_cast<const uint32_t *>(sp + 4 * (16 + g));
+            r.s[3] = *reinterpret_cast<const uint32_t *>(sp + 4 * (24 + g));
+        } else {
+            r.w[4] = r.w[5] = r.w[6] = r.w[7] = 0;
+            r.s[2] = r.s[3] = 0;
+        }
+    }
+}
+
+// Request the router rows this CTA owns for layer l, their bias and the layer's
+// slot-table row into shared memory (one commit group).
 __device__ void prefetch_router(const PersistArgs &a, int l, uint8_t *wr_s, int32_t *tab_s, float *bias_s) {
     const int G = gridDim.x, c = blockIdx.x;
     const int wsz = a.wr_bf16 ? 2 : 4;
     const int row_bytes = a.H * wsz;
     const uint8_t *Wr = reinterpret_cast<const uint8_t *>(a.layers[l].Wr);
-    int nr = 0;
-    for (int e = c; e < a.E; e += G) ++nr;
+    const int nr = (a.E - c + G - 1) / G;
     const int per_row = row_bytes / 16;
     for (int i = threadIdx.x; i < nr * per_row; i += blockDim.x) {
         const int r = i / per_row, o = (i % per_row) * 16;
@@ -125,129 +279,119 @@ __device__ void prefetch_router(const PersistArgs &a, int l, uint8_t *wr_s, int3
     }
     if (a.layers[l].bias)
         for (int r = threadIdx.x; r < nr; r += blockDim.x) cp_async4(bias_s + r, a.layers[l].bias + c + r * G);
-    // the slot-table row of this layer (E int32, E a multiple of 4 or copied by 4s)
     const int32_t *tab = a.layers[l].table + (size_t)a.layers[l].layer * a.E;
     if (((uintptr_t)tab & 15) == 0 && (a.E & 3) == 0) {
         for (int i = threadIdx.x; i < a.E / 4; i += blockDim.x) cp_async16(tab_s + 4 * i, tab + 4 * i);
     } else {
-        for (int i = threadIdx.x; i < a.E; i += blockDim.x) tab_s[i] = tab[i];
+        for (int i = threadIdx.x; i < a.E; i += blockDim.x) cp_async4(tab_s + i, tab + i);
     }
     cp_async_commit();
 }
 
-template <int KIND, int NMAT, int NB, int W>
-__device__ __forceinline__ void stream_chunks(const uint8_t *tile_ptr, int chunk_bytes, int cb, int sb,
-                                              int c_begin, int c_end, int n_chunks, bool has_half,
-                                              const BTile (&bt)[NB], const Unpack &un, int lane,
-                                              float (&acc)[NMAT][NB][4]) {
-    ChunkRegs<KIND> buf[W][NMAT];
-    auto load = [&](int ch, ChunkRegs<KIND>(&r)[NMAT]) {
-        const bool half = has_half && ch == n_chunks - 1;
-        const int cbh = half ? cb / 2 : cb, sbh = half ? sb / 2 : sb;
-        const uint8_t *cp = tile_ptr + (long long)ch * chunk_bytes;
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m) load_chunk<KIND>(cp + m * cbh, cp + NMAT * cbh + m * sbh, half, lane, r[m]);
-    };
-#pragma unroll
-    for (int j = 0; j < W; ++j)
-        if (c_begin + j < c_end) load(c_begin + j, buf[j]);
-    for (int base = c_begin; base < c_end; base += W) {
-#pragma unroll
-        for (int j = 0; j < W; ++j) {
-            const int ch = base + j;
-            if (ch < c_end) {
-                mma_chunk<KIND, NMAT, NB>(buf[j], has_half && ch == n_chunks - 1, bt, ch * 128, un, acc);
-                if (ch + W < c_end) load(ch + W, buf[j]);
+// Top-K keys of every token by sorting 32-logit chunks and merging them pairwise
+// (used when the threshold pass keeps too many candidates, e.g. many equal
+// logits). lists: T * ceil(E/32) * 32 keys of scratch.
+__device__ void topk_sort_merge(const float *logits, int T, int E, unsigned long long *lists,
+                                unsigned long long (*sel)[32]) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nch = (E + 31) / 32;
+    for (int task = warp; task < T * nch; task += kPWarps) {
+        const int t = task / nch, ch = task % nch;
+        const int e = ch * 32 + lane;
+        const unsigned long long key = e < E ? topk_key(__ldcg(logits + (size_t)t * E + e), e) : 0ull;
+        lists[((size_t)t * nch + ch) * 32 + lane] = warp_sort32(key, lane);
+    }
+    __syncthreads();
+    // merge tree: list i absorbs list i + stride (the top 32 of the union, sorted)
+    for (int stride = 1; stride < nch; stride *= 2) {
+        const int groups = (nch + 2 * stride - 1) / (2 * stride);
+        for (int task = warp; task < T * groups; task += kPWarps) {
+            const int t = task / groups, i0 = (task % groups) * 2 * stride;
+            if (i0 + stride < nch) {
+                unsigned long long *la = lists + ((size_t)t * nch + i0) * 32;
+                const unsigned long long m = warp_merge32(la[lane], la[stride * 32 + lane], lane);
+                __syncwarp();
+                la[lane] = m;
             }
         }
+        __syncthreads();
     }
+    if (tid < T * 32) sel[tid >> 5][tid & 31] = lists[(size_t)(tid >> 5) * nch * 32 + (tid & 31)];
 }
-
-// Register window per format: Q2 chunks are half the bytes of Q4 chunks.
-template <int KIND>
-struct Win {
-    static constexpr int GU = KIND == MOE_Q2_64 ? 2 : 1;
-    static constexpr int D = KIND == MOE_Q2_64 ? 2 : 1;
-};
 
 template <int KIND, bool XF32>
 __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_constant__ PersistArgs a) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ Plan s;
     __nv_bfloat16 *const xs = reinterpret_cast<__nv_bfloat16 *>(smem_raw + a.geom.off_xs);
     uint8_t *const wr_s = smem_raw + a.geom.off_wr;
-    float *const u_region = reinterpret_cast<float *>(smem_raw + a.geom.off_u);
-    float *const ypart = reinterpret_cast<float *>(smem_raw + a.geom.off_yp);
+    int32_t *const tab_s = reinterpret_cast<int32_t *>(smem_raw + a.geom.off_tab);
+    uint8_t *const u_region = smem_raw + a.geom.off_u;
     __nv_bfloat16 *const hst = reinterpret_cast<__nv_bfloat16 *>(smem_raw + a.geom.off_hst);
+    float *const red = reinterpret_cast<float *>(smem_raw + a.geom.off_red);
     const int G = gridDim.x, cta = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.T, H = a.H, E = a.E, K = a.K, P = T * K;
     const int ldx = H + 8;
     const int g = lane >> 2, c = lane & 3;
+    const int tab_ld = a.geom.tab_ld;
     unsigned target = 0;
     int *s_flag = &s.misc[2];
+    constexpr int S_GU = GuSplit<KIND>::S;
+    constexpr int NG = kPWarps / S_GU;  // gate/up warp groups per CTA
+    const QLayout &L = a.L;
+    const int dt = L.d_tiles;  // output row tiles (the shared expert has the same)
 
-    prefetch_router(a, 0, wr_s, s.table, s.bias);
+    static_assert(kRingBars == 8, "Plan::ring_bar holds 8 mbarriers per warp");
+    Ring ring;
+    ring.base = smem_raw + a.geom.off_ring + (size_t)warp * a.geom.ring_bytes;
+    ring.bar = s.ring_bar[warp];
+    ring.R = a.geom.ring_bytes;
+    ring.head = ring.tail = ring.issued = ring.consumed = ring.front = 0;
+    if (lane < kRingBars) mbar_init(&s.ring_bar[warp][lane], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
+    // chunks per piece: two pieces of each kind fit in the ring at once
+    const int pcg = a.geom.ring_bytes / (2 * L.gu_chunk_bytes) < 2 ? 1 : 2;
+    const int pcd_fit = a.geom.ring_bytes / (2 * L.d_chunk_bytes);
+    const int pcd = pcd_fit < 1 ? 1 : (pcd_fit > 4 ? 4 : pcd_fit);
+
+    prefetch_router(a, 0, wr_s, tab_s, s.bias[0]);
     for (int l = 0; l < a.n_layers; ++l) {
         const PersistLayer &Ly = a.layers[l];
+        const int32_t *const tab = tab_s + (l & 1) * tab_ld;
+        if (tid < kMaxTok) {
+            s.misc[4 + tid] = 0;
+            s.ncand[tid] = 0;
+            s.theta[tid] = 0;
+        }
         // ------------------------------------------------ N: layer input
         if (a.stack) {
-            // rmsnorm of resid with the canonical 256-thread order, two tokens at a time;
-            // resid is staged once in shared memory (one global round trip)
-            float *rs = u_region;  // [T][H]
+            // RMSNorm of resid in the canonical order of rms_partial / rms_scale;
+            // resid is staged once in shared memory
+            float *rs = reinterpret_cast<float *>(u_region);  // [T][H]
             const float4 *r4 = reinterpret_cast<const float4 *>(a.resid);
-            for (int idx = tid; idx < T * H / 4; idx += blockDim.x) reinterpret_cast<float4 *>(rs)[idx] = r4[idx];
+            for (int idx = tid; idx < T * H / 4; idx += kPersistThreads)
+                reinterpret_cast<float4 *>(rs)[idx] = __ldcg(r4 + idx);
             __syncthreads();
-            const int half = tid >> 8, i = tid & 255;
-            float r_t[kMaxTok / 2];
-            float ss[kMaxTok / 2];
-#pragma unroll
-            for (int j = 0; j < kMaxTok / 2; ++j) {
-                const int t = half + 2 * j;
-                float acc = 0.f;
-                if (t < T) {
-                    const float *xt = rs + (size_t)t * H;
-                    for (int h = i; h < H; h += kNormThreads) acc = fmaf(xt[h], xt[h], acc);
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                ss[j] = acc;
-            }
-            __shared__ float wsum[kMaxTok * 8];
-            if (lane == 0) {
-#pragma unroll
-                for (int j = 0; j < kMaxTok / 2; ++j) {
-                    const int t = half + 2 * j;
-                    if (t < T) wsum[t * 8 + (i >> 5)] = ss[j];
-                }
+            for (int t = 0; t < T; ++t) {
+                const float p = rms_partial(rs + (size_t)t * H, H, tid);
+                if (lane == 0) s.wsum[t][warp] = p;
             }
             __syncthreads();
-#pragma unroll
-            for (int j = 0; j < kMaxTok / 2; ++j) {
-                const int t = half + 2 * j;
-                float tot = 0.f;
-                if (t < T) {
-#pragma unroll
-                    for (int w = 0; w < 8; ++w) tot += wsum[t * 8 + w];
-                }
-                r_t[j] = 1.0f / sqrtf(tot / (float)H + a.eps);
-            }
-#pragma unroll
-            for (int j = 0; j < kMaxTok / 2; ++j) {
-                const int t = half + 2 * j;
-                if (t < T) {
-                    const float *xt = rs + (size_t)t * H;
-                    for (int h = i; h < H; h += kNormThreads) {
-                        const __nv_bfloat16 u = __float2bfloat16_rn(xt[h] * r_t[j]);
-                        xs[(size_t)t * ldx + h] = u;
-                        if (a.trace_in && cta == 0) a.trace_in[((size_t)l * T + t) * H + h] = u;
-                    }
+            for (int t = 0; t < T; ++t) {
+                const float r = rms_scale(s.wsum[t], H, a.eps);
+                const float *xt = rs + (size_t)t * H;
+                for (int h = tid; h < H; h += kPersistThreads) {
+                    const __nv_bfloat16 u = __float2bfloat16_rn(xt[h] * r);
+                    xs[(size_t)t * ldx + h] = u;
+                    if (a.trace_in && cta == 0) a.trace_in[((size_t)l * T + t) * H + h] = u;
                 }
             }
         } else if (XF32) {
             // hi limbs in rows 0..3, lo limbs in rows 4..7
             const float *x = reinterpret_cast<const float *>(a.x);
-            for (int idx = tid; idx < T * H; idx += blockDim.x) {
+            for (int idx = tid; idx < T * H; idx += kPersistThreads) {
                 const int t = idx / H, h = idx % H;
                 __nv_bfloat16 hi, lo;
                 split_bf16(x[idx], hi, lo);
@@ -256,12 +400,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
             }
         } else {
             const uint4 *x = reinterpret_cast<const uint4 *>(a.x);
-            for (int idx = tid; idx < T * H / 8; idx += blockDim.x) {
+            for (int idx = tid; idx < T * H / 8; idx += kPersistThreads) {
                 const int t = idx / (H / 8), h8 = (idx % (H / 8)) * 8;
                 *reinterpret_cast<uint4 *>(xs + (size_t)t * ldx + h8) = x[idx];
             }
         }
-        cp_async_wait_all();
+        cp_async_wait_all();  // this layer's router rows, bias and table row
         __syncthreads();
         // ------------------------------------------------ R: router logits of my experts
         {
@@ -290,60 +434,120 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
             if (tid < nr * T) {
                 const int r = tid / T, t = tid % T;
                 const int e = cta + r * G;
-                const float v = combine_router4(&s.rpart[r][t][0]) + (Ly.bias ? s.bias[r] : 0.f);
+                const float v = combine_router4(&s.rpart[r][t][0]) + (Ly.bias ? s.bias[l & 1][r] : 0.f);
                 a.logits[(size_t)t * E + e] = v;
                 if (a.trace_logits) a.trace_logits[((size_t)l * T + t) * E + e] = v;
             }
+            // the router rows are free: request the next layer's (HBM is idle until
+            // the expert weights are known)
+            if (l + 1 < a.n_layers)
+                prefetch_router(a, l + 1, wr_s, tab_s + ((l + 1) & 1) * tab_ld, s.bias[(l + 1) & 1]);
         }
-        __syncthreads();
-        
         if (!grid_sync(a.bar, target, a.status, s_flag)) break;
         // ------------------------------------------------ T: top-K and the plan (every CTA)
         {
-            const int nch = (E + 31) / 32;
-            unsigned long long *lists = reinterpret_cast<unsigned long long *>(u_region);  // [T][nch][32]
-            if (tid < kMaxTok) s.misc[4 + tid] = 0;
-            __syncthreads();
-            for (int task = warp; task < T * nch; task += kPWarps) {
-                const int t = task / nch, ch = task % nch;
-                bool bad;
-                const unsigned long long key = topk_chunk_keys(a.logits + (size_t)t * E, E, ch, lane, bad);
-                if (__any_sync(0xffffffffu, bad) && lane == 0) s.misc[4 + t] = 1;
-                lists[((size_t)t * nch + ch) * 32 + lane] = key;
+            uint32_t *segmax = reinterpret_cast<uint32_t *>(u_region);  // [kMaxTok][kMaxSeg]
+            unsigned long long *cand =
+                reinterpret_cast<unsigned long long *>(u_region + kMaxTok * kMaxSeg * sizeof(uint32_t));
+            // expert e sits in thread e (and e - 512); segments of `seg` threads
+            const int nact = E < kPersistThreads ? E : kPersistThreads;
+            int seg = 1;
+            while (seg < 32 && (nact + 2 * seg - 1) / (2 * seg) >= 2 * K) seg *= 2;
+            while (seg < 32 && (nact + seg - 1) / seg > kMaxSeg) seg *= 2;
+            const int nseg = (nact + seg - 1) / seg;
+            const bool all_cand = E <= kCandCap;  // no threshold: every expert is a candidate
+            const bool in1 = tid < E, in2 = tid + kPersistThreads < E;
+            float v1[kMaxTok], v2[kMaxTok];
+#pragma unroll
+            for (int t = 0; t < kMaxTok; ++t) {
+                v1[t] = (t < T && in1) ? __ldcg(a.logits + (size_t)t * E + tid) : 0.f;
+                v2[t] = (t < T && in2) ? __ldcg(a.logits + (size_t)t * E + tid + kPersistThreads) : 0.f;
             }
-            __syncthreads();
-            const int kc = K < 32 ? K : 32;
-            const int C = nch * kc;  // candidates per token: the best kc of each chunk
-            if (C <= 256) {
-                // rank of each candidate among its token's candidates = its place in the top-K
-                for (int idx = tid; idx < T * C; idx += blockDim.x) {
-                    const int t = idx / C, c = idx % C;
-                    const unsigned long long *lt = lists + (size_t)t * nch * 32;
-                    const unsigned long long key = lt[(c / kc) * 32 + c % kc];
-                    int r = 0;
-                    for (int ch = 0; ch < nch; ++ch)
-                        for (int i2 = 0; i2 < kc; ++i2) r += lt[ch * 32 + i2] > key;
-                    if (r < K) s.sel[t][r] = key;
-                }
-                __syncthreads();
-            } else {
-            // merge tree: list i absorbs list i + stride (the top 32 of the union, sorted)
-            for (int stride = 1; stride < nch; stride *= 2) {
-                const int groups = (nch + 2 * stride - 1) / (2 * stride);
-                for (int task = warp; task < T * groups; task += kPWarps) {
-                    const int t = task / groups, i0 = (task % groups) * 2 * stride;
-                    if (i0 + stride < nch) {
-                        unsigned long long *la = lists + ((size_t)t * nch + i0) * 32;
-                        const unsigned long long m = warp_merge32(la[lane], la[stride * 32 + lane], lane);
-                        __syncwarp();
-                        la[lane] = m;
+            uint32_t o1[kMaxTok], o2[kMaxTok];
+#pragma unroll
+            for (int t = 0; t < kMaxTok; ++t) {
+                o1[t] = in1 ? topk_ord(v1[t]) : 0u;
+                o2[t] = in2 ? topk_ord(v2[t]) : 0u;
+                if (t < T) {
+                    const bool bad = (in1 && !isfinite(v1[t])) || (in2 && !isfinite(v2[t]));
+                    if (__any_sync(0xffffffffu, bad) && lane == 0) s.misc[4 + t] = 1;
+                    if (!all_cand) {
+                        uint32_t m = o1[t] > o2[t] ? o1[t] : o2[t];
+                        for (int d = 1; d < seg; d <<= 1) {
+                            const uint32_t o = __shfl_xor_sync(0xffffffffu, m, d);
+                            m = o > m ? o : m;
+                        }
+                        if ((tid & (seg - 1)) == 0 && tid < nact) segmax[t * kMaxSeg + tid / seg] = m;
                     }
                 }
-                __syncthreads();
             }
-            if (tid < T * 32) s.sel[tid >> 5][tid & 31] = lists[(size_t)(tid >> 5) * nch * 32 + (tid & 31)];
             __syncthreads();
+            // threshold: the K-th largest segment maximum (at least K experts reach
+            // it, so every top-K expert does); left at 0 if there are fewer than K
+            if (!all_cand) {
+                const int t = tid / kMaxSeg, j = tid % kMaxSeg;
+                if (t < T && j < nseg) {
+                    const uint32_t *sm = segmax + t * kMaxSeg;
+                    const uint32_t mv = sm[j];
+                    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+#pragma unroll 4
+                    for (int j4 = 0; j4 < nseg; j4 += 4) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(sm + j4);
+                        r0 += (j4 < nseg) & ((v.x > mv) | ((v.x == mv) & (j4 < j)));
+                        r1 += (j4 + 1 < nseg) & ((v.y > mv) | ((v.y == mv) & (j4 + 1 < j)));
+                        r2 += (j4 + 2 < nseg) & ((v.z > mv) | ((v.z == mv) & (j4 + 2 < j)));
+                        r3 += (j4 + 3 < nseg) & ((v.w > mv) | ((v.w == mv) & (j4 + 3 < j)));
+                    }
+                    if ((r0 + r1) + (r2 + r3) == K - 1) s.theta[t] = mv;
+                }
             }
+            __syncthreads();
+            const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+            for (int t = 0; t < kMaxTok; ++t) {
+                if (t < T) {
+                    const uint32_t th = s.theta[t];
+                    const bool c1 = in1 && o1[t] >= th, c2 = in2 && o2[t] >= th;
+                    const unsigned b1 = __ballot_sync(0xffffffffu, c1), b2 = __ballot_sync(0xffffffffu, c2);
+                    const int n = __popc(b1) + __popc(b2);
+                    int base = 0;
+                    if (lane == 0 && n) base = atomicAdd(&s.ncand[t], n);
+                    base = __shfl_sync(0xffffffffu, base, 0);
+                    if (c1) {
+                        const int pos = base + __popc(b1 & lt);
+                        if (pos < kCandCap) cand[t * kCandCap + pos] = topk_key_of(o1[t], tid);
+                    }
+                    if (c2) {
+                        const int pos = base + __popc(b1) + __popc(b2 & lt);
+                        if (pos < kCandCap) cand[t * kCandCap + pos] = topk_key_of(o2[t], tid + kPersistThreads);
+                    }
+                }
+            }
+            __syncthreads();
+            bool overflow = false;
+            for (int t = 0; t < T; ++t) overflow |= s.ncand[t] > kCandCap;
+            if (!overflow) {
+                // rank of each candidate among its token's candidates = its place in the top-K
+                for (int idx = tid; idx < T * kCandCap; idx += kPersistThreads) {
+                    const int t = idx / kCandCap, ci = idx % kCandCap;
+                    const int n = s.ncand[t];
+                    if (ci < n) {
+                        const unsigned long long *ct = cand + t * kCandCap;
+                        const unsigned long long key = ct[ci];
+                        int r0 = 0, r1 = 0;
+#pragma unroll 4
+                        for (int i2 = 0; i2 < n; i2 += 2) {
+                            const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(ct + i2);
+                            r0 += v.x > key;
+                            r1 += (i2 + 1 < n) & (v.y > key);
+                        }
+                        if (r0 + r1 < K) s.sel[t][r0 + r1] = key;
+                    }
+                }
+            } else {
+                topk_sort_merge(a.logits, T, E, reinterpret_cast<unsigned long long *>(u_region), s.sel);
+            }
+            __syncthreads();
             if (warp < T) {
                 const int t = warp;
                 const unsigned long long key = s.sel[t][lane];
@@ -362,12 +566,16 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
             // stable order of pairs by expert: rank = #{q : (id_q, q) < (id_p, p)}
             if (tid < P) {
                 const int ep = s.ids[tid];
-                int rank = 0;
-                for (int q = 0; q < P; ++q) {
-                    const int eq = s.ids[q];
-                    rank += (eq < ep) || (eq == ep && q < tid);
+                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+#pragma unroll 2
+                for (int q4 = 0; q4 < P; q4 += 4) {
+                    const int4 v = *reinterpret_cast<const int4 *>(s.ids + q4);
+                    r0 += (q4 < P) & ((v.x < ep) | ((v.x == ep) & (q4 < tid)));
+                    r1 += (q4 + 1 < P) & ((v.y < ep) | ((v.y == ep) & (q4 + 1 < tid)));
+                    r2 += (q4 + 2 < P) & ((v.z < ep) | ((v.z == ep) & (q4 + 2 < tid)));
+                    r3 += (q4 + 3 < P) & ((v.w < ep) | ((v.w == ep) & (q4 + 3 < tid)));
                 }
-                s.sorted[rank] = tid;
+                s.sorted[(r0 + r1) + (r2 + r3)] = tid;
             }
             __syncthreads();
             if (warp == 0) {
@@ -379,7 +587,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                     if (r < P) {
                         p = s.sorted[r];
                         e = s.ids[p];
-                        slot = s.table[e];
+                        slot = tab[e];
                         if (slot < 0) absent = true;
                         else if (slot >= Ly.capacity) oob = true;
                         else live = s.w[p] != 0.f;
@@ -419,61 +627,103 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                     s.ustart[nu] = nlive;
                     s.misc[0] = nu;
                     s.misc[1] = nlive;
+                    // down units (expert-major: unit j = expert j / dt, row tile j % dt)
+                    // split over the CTAs by down bytes: CTA c takes the units whose
+                    // byte midpoint falls in [c D / G, (c + 1) D / G)
+                    const bool sh = Ly.shared != nullptr;
+                    const long long nr_units = (long long)nu * dt;
+                    const int n_units = (int)nr_units + (sh ? dt : 0);
+                    const long long dr = L.d_tile_bytes, dsb = sh ? a.LS.d_tile_bytes : 0;
+                    const long long Dr = nr_units * dr, Dtot = Dr + (long long)dt * dsb;
+                    auto first_unit = [&](long long b) -> int {
+                        if (b <= 0) return 0;
+                        const long long x = b - dr / 2;  // routed: j*dr + dr/2 >= b
+                        const long long j = x <= 0 ? 0 : (x + dr - 1) / dr;
+                        if (j < nr_units || dsb == 0) return (int)(j < nr_units ? j : nr_units);
+                        const long long y = b - Dr - dsb / 2;  // shared: Dr + k*dsb + dsb/2 >= b
+                        const long long jj = nr_units + (y <= 0 ? 0 : (y + dsb - 1) / dsb);
+                        return (int)(jj < n_units ? jj : n_units);
+                    };
+                    s.misc[12] = first_unit(Dtot * cta / G);
+                    s.misc[13] = cta == G - 1 ? n_units : first_unit(Dtot * (cta + 1) / G);
                 }
             }
             __syncthreads();
         }
         const int nU = s.misc[0];
         const bool has_shared = Ly.shared != nullptr;
-        // the table row and router rows of the next layer (the buffers are free now)
-        if (l + 1 < a.n_layers) prefetch_router(a, l + 1, wr_s, s.table, s.bias);
-        // every weight byte this CTA will read in this layer, requested from HBM now:
-        // gate/up items (one request per item), then down tiles (one per expert and tile)
-        {
-            const int tilesF = a.L.gu_tiles;
-            const int n_items = nU * tilesF + (has_shared ? a.LS.gu_tiles : 0);
-            for (int j = cta + G * warp; j < n_items && warp < 4; j += G * 4) {
-                if (lane == 0) {
-                    const bool sh = j >= nU * tilesF;
-                    const QLayout &LL = sh ? a.LS : a.L;
-                    const uint8_t *wb = sh ? Ly.shared : Ly.arena + (long long)s.uslot[j / tilesF] * Ly.stride;
-                    const int rt = sh ? j - nU * tilesF : j % tilesF;
-                    prefetch_l2(wb + (long long)rt * LL.gu_tile_bytes, (unsigned)LL.gu_tile_bytes);
+        const int tilesF = L.gu_tiles, tilesS = has_shared ? a.LS.gu_tiles : 0;
+        const int n_items = nU * tilesF + tilesS;
+        const int j0 = s.misc[12], j1 = s.misc[13];
+        // ------------------------------------------------ weight copies of this warp
+        const int grp = warp / S_GU, q = warp % S_GU;
+        const int n_ch = L.gu_chunks;  // the shared expert has the same H chunks
+        const int cb0 = gu_chunk_begin(q, n_ch, S_GU), cb1 = gu_chunk_begin(q + 1, n_ch, S_GU);
+        const int dw = kPWarps - 1 - warp;  // down units go to the last warps first
+        auto gu_tile = [&](int j) -> const uint8_t * {
+            if (j >= nU * tilesF) return Ly.shared + (long long)(j - nU * tilesF) * a.LS.gu_tile_bytes;
+            return Ly.arena + (long long)s.uslot[j / tilesF] * Ly.stride + (long long)(j % tilesF) * L.gu_tile_bytes;
+        };
+        auto d_tile = [&](int j) -> const uint8_t * {
+            const int ti = j / dt, r = j % dt;
+            if (ti >= nU) return Ly.shared + a.LS.d_offset + (long long)r * a.LS.d_tile_bytes;
+            return Ly.arena + (long long)s.uslot[ti] * Ly.stride + L.d_offset + (long long)r * L.d_tile_bytes;
+        };
+        int pphase = 0, pm = 0, pch = cb0, pd = 0, pdch = 0;
+        auto produce = [&]() {
+            for (;;) {
+                if (pphase == 0) {
+                    if (pch >= cb1) {
+                        ++pm;
+                        pch = cb0;
+                    }
+                    const int j = cta + G * (grp + NG * pm);
+                    if (cb0 >= cb1 || j >= n_items) {
+                        pphase = 1;
+                        continue;
+                    }
+                    const int nc = cb1 - pch < pcg ? cb1 - pch : pcg;
+                    const int bytes = piece_bytes(L.gu_chunk_bytes, L.gu_half, n_ch, pch, nc);
+                    if (!ring_push(ring, gu_tile(j) + (long long)pch * L.gu_chunk_bytes, bytes, lane)) return;
+                    pch += nc;
+                } else if (pphase == 1) {
+                    const int j = j0 + dw + kPWarps * pd;
+                    if (j >= j1) {
+                        pphase = 2;
+                        return;
+                    }
+                    const QLayout &LL = j / dt >= nU ? a.LS : L;
+                    if (pdch >= LL.d_chunks) {
+                        ++pd;
+                        pdch = 0;
+                        continue;
+                    }
+                    const int nc = LL.d_chunks - pdch < pcd ? LL.d_chunks - pdch : pcd;
+                    const int bytes = piece_bytes(LL.d_chunk_bytes, LL.d_half, LL.d_chunks, pdch, nc);
+                    if (!ring_push(ring, d_tile(j) + (long long)pdch * LL.d_chunk_bytes, bytes, lane)) return;
+                    pdch += nc;
+                } else {
+                    return;
                 }
             }
-            const int n_tasks = nU + (has_shared ? 1 : 0);
-            int k = 0;
-            for (int r = cta; r < a.L.d_tiles; r += G)
-                for (int ti = 0; ti < n_tasks; ++ti, ++k) {
-                    if ((k % kPWarps) != warp || lane != 0) continue;
-                    const bool sh = ti >= nU;
-                    const QLayout &LL = sh ? a.LS : a.L;
-                    const uint8_t *wb = sh ? Ly.shared : Ly.arena + (long long)s.uslot[ti] * Ly.stride;
-                    prefetch_l2(wb + LL.d_offset + (long long)r * LL.d_tile_bytes, (unsigned)LL.d_tile_bytes);
-                }
-        }
+        };
+        produce();
         // ------------------------------------------------ GU: gate/up + activation
         {
-            const QLayout &L = a.L;
-            const int tilesF = L.gu_tiles;
-            const int tilesS = has_shared ? a.LS.gu_tiles : 0;
-            const int n_items = nU * tilesF + tilesS;
-            const int quad = warp >> 2, q = warp & 3;
-            for (int j = cta + G * quad; j < n_items; j += G * 4) {
+            float *gred = red + (size_t)grp * S_GU * 32 * 8;
+            for (int m = 0;; ++m) {
+                const int j = cta + G * (grp + NG * m);
+                if (j >= n_items) break;
                 const bool shared = j >= nU * tilesF;
-                int rt, ncols, col0 = 0;
-                const uint8_t *wbase;
-                const QLayout &LL = shared ? a.LS : a.L;
+                int ncols, col0 = 0, rt;
                 if (!shared) {
                     const int u = j / tilesF;
                     rt = j % tilesF;
                     col0 = s.ustart[u];
                     ncols = s.ustart[u + 1] - col0;
-                    wbase = Ly.arena + (long long)s.uslot[u] * Ly.stride;
                 } else {
                     rt = j - nU * tilesF;
                     ncols = T;
-                    wbase = Ly.shared;
                 }
                 // B column g: token of column g (x bf16), or hi/lo limb rows (x fp32)
                 const int jc = XF32 ? (g & 3) : g;
@@ -484,26 +734,41 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                     trow = XF32 ? ((g < 4) ? t : 4 + t) : t;
                 }
                 const BTile bt[1] = {{xs + (size_t)trow * ldx + 2 * c, valid}};
-                const int n_chunks = LL.gu_chunks;
-                const int cb0 = gu_chunk_begin(q, n_chunks), cb1 = gu_chunk_begin(q + 1, n_chunks);
-                const uint8_t *tile_ptr = wbase + (long long)rt * LL.gu_tile_bytes;
                 float acc[2][1][4] = {};
-                stream_chunks<KIND, 2, 1, Win<KIND>::GU>(tile_ptr, LL.gu_chunk_bytes, LL.cb, LL.sb, cb0, cb1,
-                                                         n_chunks, LL.gu_half, bt, shared ? a.un_s : a.un, lane,
-                                                         acc);
-                float *red = u_region + (size_t)quad * (4 * 32 * 8);
+                const uint8_t *pbase = nullptr;
+                int pnc = 0, pbytes = 0;
+                for (int ch = cb0; ch < cb1; ++ch) {
+                    const int k = (ch - cb0) % pcg;
+                    if (k == 0) {
+                        pnc = cb1 - ch < pcg ? cb1 - ch : pcg;
+                        pbytes = piece_bytes(L.gu_chunk_bytes, L.gu_half, n_ch, ch, pnc);
+                        pbase = ring_front(ring, pbytes, a.status, a.bar);
+                    }
+                    const bool half = L.gu_half && ch == n_ch - 1;
+                    const int cbh = half ? L.cb / 2 : L.cb, sbh = half ? L.sb / 2 : L.sb;
+                    const uint8_t *p = pbase + k * L.gu_chunk_bytes;
+                    ChunkRegs<KIND> rg[2];
+                    load_chunk_s<KIND>(p, p + 2 * cbh, half, lane, rg[0]);
+                    load_chunk_s<KIND>(p + cbh, p + 2 * cbh + sbh, half, lane, rg[1]);
+                    if (k == pnc - 1) {
+                        ring_pop(ring, pbytes);
+                        produce();
+                    }
+                    mma_chunk<KIND, 2, 1>(rg, half, bt, ch * 128, shared ? a.un_s : a.un, acc);
+                }
+                // the group adds the S parts in part order (as the multi-kernel k_gateup)
 #pragma unroll
-                for (int m = 0; m < 2; ++m)
+                for (int m2 = 0; m2 < 2; ++m2)
 #pragma unroll
-                    for (int e4 = 0; e4 < 4; ++e4) red[(q * 32 + lane) * 8 + m * 4 + e4] = acc[m][0][e4];
-                quad_sync(quad);
+                    for (int e4 = 0; e4 < 4; ++e4) gred[(q * 32 + lane) * 8 + m2 * 4 + e4] = acc[m2][0][e4];
+                asm volatile("bar.sync %0, %1;" ::"r"(grp + 1), "r"(S_GU * 32) : "memory");
                 if (q == 0) {
                     float v[8];
 #pragma unroll
                     for (int e8 = 0; e8 < 8; ++e8) {
-                        float sum = red[lane * 8 + e8];
+                        float sum = gred[lane * 8 + e8];
 #pragma unroll
-                        for (int w = 1; w < 4; ++w) sum += red[(w * 32 + lane) * 8 + e8];
+                        for (int w = 1; w < S_GU; ++w) sum += gred[(w * 32 + lane) * 8 + e8];
                         v[e8] = sum;
                     }
                     if (XF32) {
@@ -526,162 +791,222 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                         }
                     }
                 }
-                quad_sync(quad);
+                asm volatile("bar.sync %0, %1;" ::"r"(grp + 1), "r"(S_GU * 32) : "memory");
             }
         }
         if (!grid_sync(a.bar, target, a.status, s_flag)) break;
         // ------------------------------------------------ D: down projection + combine
         {
-            const QLayout &L = a.L;
             const int n_tasks = nU + (has_shared ? 1 : 0);
-            // h limbs of the live columns (plan order) and of the shared tokens, staged
-            // once: row i of the routed part at hst + i*ldh (hi) and hst + lo_off + i*ldh
-            // (lo); lo_off makes hi and lo rows fall on different banks
-            const int nlive = s.misc[1];
-            const bool staged = a.geom.hst_bytes != 0;
+            produce();
+            // h limbs of the experts of this CTA's units, staged once: routed plan
+            // columns [c_lo, c_hi) at hst + (i - c_lo)*ldh (hi) and hst + lo_off + ...
+            // (lo; lo_off puts hi and lo rows on different banks); the shared
+            // expert's tokens after them at hss
             const int ldh = L.F + 8, ldhs = a.LS.F + 8;
-            const int lo_off = ((nlive * ldh + 63) & ~63) + 32;
-            __nv_bfloat16 *const hss = hst + (((lo_off + nlive * ldh) + 63) & ~63);
+            int c_lo = 0, c_hi = 0;
+            bool need_sh = false;
+            if (j1 > j0) {
+                const int ti_lo = j0 / dt, ti_hi = (j1 - 1) / dt;
+                if (ti_lo < nU) {
+                    c_lo = s.ustart[ti_lo];
+                    c_hi = s.ustart[(ti_hi < nU ? ti_hi : nU - 1) + 1];
+                }
+                need_sh = ti_hi >= nU;
+            }
+            const int nrow = c_hi - c_lo;
+            const int lo_off = ((nrow * ldh + 63) & ~63) + 32;
+            const int hss_off = (lo_off + nrow * ldh + 63) & ~63;
             const int lo_off_s = ((T * ldhs + 63) & ~63) + 32;
+            const size_t need = (size_t)(hss_off + (need_sh ? lo_off_s + T * ldhs : 0)) * 2;
+            const bool staged = need <= a.geom.hst_bytes;
+            __nv_bfloat16 *const hss = hst + hss_off;
             if (staged) {
                 const int vpr = L.F / 8;  // 16-byte vectors per routed row
-                for (int idx = tid; idx < nlive * 2 * vpr; idx += blockDim.x) {
+                for (int idx = tid; idx < nrow * 2 * vpr; idx += kPersistThreads) {
                     const int i = idx / (2 * vpr), rem = idx % (2 * vpr), limb = rem / vpr, v = rem % vpr;
-                    const __nv_bfloat16 *src = (limb ? a.h_lo : a.h_hi) + (size_t)s.cols[i] * a.h_ld + v * 8;
+                    const __nv_bfloat16 *src = (limb ? a.h_lo : a.h_hi) + (size_t)s.cols[c_lo + i] * a.h_ld + v * 8;
                     *reinterpret_cast<uint4 *>(hst + (limb ? lo_off : 0) + i * ldh + v * 8) =
-                        *reinterpret_cast<const uint4 *>(src);
+                        __ldcg(reinterpret_cast<const uint4 *>(src));
                 }
-                if (has_shared) {
+                if (need_sh) {
                     const int vps = a.LS.F / 8;
-                    for (int idx = tid; idx < T * 2 * vps; idx += blockDim.x) {
+                    for (int idx = tid; idx < T * 2 * vps; idx += kPersistThreads) {
                         const int t = idx / (2 * vps), rem = idx % (2 * vps), limb = rem / vps, v = rem % vps;
                         const __nv_bfloat16 *src = (limb ? a.h_lo : a.h_hi) + (size_t)(P + t) * a.h_ld + v * 8;
                         *reinterpret_cast<uint4 *>(hss + (limb ? lo_off_s : 0) + t * ldhs + v * 8) =
-                            *reinterpret_cast<const uint4 *>(src);
+                            __ldcg(reinterpret_cast<const uint4 *>(src));
                     }
                 }
-                __syncthreads();
             }
-            for (int r = cta; r < L.d_tiles; r += G) {
-                for (int ti = warp; ti < n_tasks; ti += kPWarps) {
-                    const bool shared = ti >= nU;
-                    const QLayout &LL = shared ? a.LS : a.L;
-                    int ncols, col0 = 0;
-                    const uint8_t *wbase;
-                    if (!shared) {
-                        col0 = s.ustart[ti];
-                        ncols = s.ustart[ti + 1] - col0;
-                        wbase = Ly.arena + (long long)s.uslot[ti] * Ly.stride;
-                    } else {
-                        ncols = T;
-                        wbase = Ly.shared;
-                    }
-                    const uint8_t *tile_ptr = wbase + LL.d_offset + (long long)r * LL.d_tile_bytes;
-                    const Unpack &un = shared ? a.un_s : a.un;
-                    // B tiles: columns nb*4 + (g & 3); lanes g < 4 read hi limbs, g >= 4 lo limbs
-                    auto make_bt = [&](int nb) {
-                        const int jc = nb * 4 + (g & 3);
-                        BTile b{a.h_hi, false};
-                        if (jc < ncols) {
-                            if (staged) {
-                                b.row = shared ? hss + (g < 4 ? 0 : lo_off_s) + jc * ldhs + 2 * c
-                                               : hst + (g < 4 ? 0 : lo_off) + (col0 + jc) * ldh + 2 * c;
-                            } else {
-                                const int row = shared ? P + jc : s.cols[col0 + jc];
-                                b.row = (g < 4 ? a.h_hi : a.h_lo) + (size_t)row * a.h_ld + 2 * c;
-                            }
-                            b.valid = true;
+            __syncthreads();
+            for (int di = 0;; ++di) {
+                const int j = j0 + dw + kPWarps * di;
+                if (j >= j1) break;
+                const int ti = j / dt, r = j % dt;
+                const bool shared = ti >= nU;
+                const QLayout &LL = shared ? a.LS : L;
+                int ncols, col0 = 0;
+                if (!shared) {
+                    col0 = s.ustart[ti];
+                    ncols = s.ustart[ti + 1] - col0;
+                } else {
+                    ncols = T;
+                }
+                const Unpack &un = shared ? a.un_s : a.un;
+                // B tiles: columns nb*4 + (g & 3); lanes g < 4 read hi limbs, g >= 4 lo limbs
+                auto make_bt = [&](int nb) {
+                    const int jc = nb * 4 + (g & 3);
+                    BTile b{a.h_hi, false};
+                    if (jc < ncols) {
+                        if (staged) {
+                            b.row = shared ? hss + (g < 4 ? 0 : lo_off_s) + jc * ldhs + 2 * c
+                                           : hst + (g < 4 ? 0 : lo_off) + (col0 + jc - c_lo) * ldh + 2 * c;
+                        } else {
+                            const int row = shared ? P + jc : s.cols[col0 + jc];
+                            b.row = (g < 4 ? a.h_hi : a.h_lo) + (size_t)row * a.h_ld + 2 * c;
                         }
-                        return b;
-                    };
-                    auto emit = [&](int nb, float (&acc)[4]) {
-                        float v[4];
+                        b.valid = true;
+                    }
+                    return b;
+                };
+                auto emit = [&](int nb, float (&acc)[4]) {
+                    float v[4];
 #pragma unroll
-                        for (int e4 = 0; e4 < 4; ++e4) v[e4] = acc[e4] + __shfl_xor_sync(0xffffffffu, acc[e4], 2);
-                        if (c < 2) {
+                    for (int e4 = 0; e4 < 4; ++e4) v[e4] = acc[e4] + __shfl_xor_sync(0xffffffffu, acc[e4], 2);
+                    if (c < 2) {
 #pragma unroll
-                            for (int e4 = 0; e4 < 4; ++e4) {
-                                const int rr = g + 8 * (e4 >> 1), jj = nb * 4 + 2 * c + (e4 & 1);
-                                if (jj < ncols) {
-                                    const int row = shared ? P + jj : s.cols[col0 + jj];
-                                    ypart[row * 16 + rr] = v[e4];
-                                }
+                        for (int e4 = 0; e4 < 4; ++e4) {
+                            const int rr = g + 8 * (e4 >> 1), jj = nb * 4 + 2 * c + (e4 & 1);
+                            if (jj < ncols) {
+                                const int row = shared ? P + jj : s.cols[col0 + jj];
+                                a.yp[(size_t)row * H + r * 16 + rr] = v[e4];
                             }
                         }
-                    };
-                    if (ncols > 4) {
-                        const BTile bt[2] = {make_bt(0), make_bt(1)};
-                        float acc[1][2][4] = {};
-                        stream_chunks<KIND, 1, 2, Win<KIND>::D>(tile_ptr, LL.d_chunk_bytes, LL.cb, LL.sb, 0,
-                                                                LL.d_chunks, LL.d_chunks, LL.d_half, bt, un, lane, acc);
-                        emit(0, acc[0][0]);
-                        emit(1, acc[0][1]);
-                    } else {
-                        const BTile bt[1] = {make_bt(0)};
-                        float acc[1][1][4] = {};
-                        stream_chunks<KIND, 1, 1, Win<KIND>::D>(tile_ptr, LL.d_chunk_bytes, LL.cb, LL.sb, 0,
-                                                                LL.d_chunks, LL.d_chunks, LL.d_half, bt, un, lane, acc);
-                        emit(0, acc[0][0]);
                     }
-                }
-                __syncthreads();
-                if (tid < T * 16) {
-                    const int t = tid >> 4, rr = tid & 15;
-                    float acc = 0.f;
-                    for (int k = 0; k < K; ++k) {
-                        const int p = t * K + k;
-                        if (s.live[p]) acc = fmaf(s.w[p], ypart[p * 16 + rr], acc);
+                };
+                const int nchk = LL.d_chunks;
+                auto run = [&](auto nb_tag) {
+                    constexpr int NB = decltype(nb_tag)::value;
+                    BTile bt[NB];
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) bt[nb] = make_bt(nb);
+                    float acc[1][NB][4] = {};
+                    const uint8_t *pbase = nullptr;
+                    int pnc = 0, pbytes = 0;
+                    for (int ch = 0; ch < nchk; ++ch) {
+                        const int k = ch % pcd;
+                        if (k == 0) {
+                            pnc = nchk - ch < pcd ? nchk - ch : pcd;
+                            pbytes = piece_bytes(LL.d_chunk_bytes, LL.d_half, nchk, ch, pnc);
+                            pbase = ring_front(ring, pbytes, a.status, a.bar);
+                        }
+                        const bool half = LL.d_half && ch == nchk - 1;
+                        const int cbh = half ? LL.cb / 2 : LL.cb;
+                        const uint8_t *p = pbase + k * LL.d_chunk_bytes;
+                        ChunkRegs<KIND> rg[1];
+                        load_chunk_s<KIND>(p, p + cbh, half, lane, rg[0]);
+                        if (k == pnc - 1) {
+                            ring_pop(ring, pbytes);
+                            produce();
+                        }
+                        mma_chunk<KIND, 1, NB>(rg, half, bt, ch * 128, un, acc);
                     }
-                    if (has_shared) acc += ypart[(P + t) * 16 + rr];
-                    const size_t o = (size_t)t * H + r * 16 + rr;
-                    if (a.stack)
-                        a.resid[o] = a.resid[o] + acc;
-                    else
-                        a.y[o] = acc;
+#pragma unroll
+                    for (int nb = 0; nb < NB; ++nb) emit(nb, acc[0][nb]);
+                };
+                if (ncols > 4)
+                    run(std::integral_constant<int, 2>{});
+                else
+                    run(std::integral_constant<int, 1>{});
+                // the last unit of row tile r to arrive combines the experts in k order
+                __syncwarp();
+                int ticket = 0;
+                if (lane == 0) {
+                    __threadfence();
+                    ticket = atomicAdd(&a.d_cnt[r], 1);
                 }
-                __syncthreads();
+                ticket = __shfl_sync(0xffffffffu, ticket, 0);
+                if (ticket == n_tasks - 1) {
+                    __threadfence();
+                    for (int o = lane; o < T * 16; o += 32) {
+                        const int t = o >> 4, rr = o & 15;
+                        const size_t col = (size_t)r * 16 + rr, oo = (size_t)t * H + col;
+                        // every load first (one round trip), then the sum in k order
+                        float yv[32];
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            yv[k] = (k < K && s.live[t * K + k]) ? __ldcg(a.yp + (size_t)(t * K + k) * H + col) : 0.f;
+                        const float ysh = has_shared ? __ldcg(a.yp + (size_t)(P + t) * H + col) : 0.f;
+                        const float rv = a.stack ? __ldcg(a.resid + oo) : 0.f;
+                        float acc = 0.f;
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            if (k < K && s.live[t * K + k]) acc = fmaf(s.w[t * K + k], yv[k], acc);
+                        if (has_shared) acc += ysh;
+                        if (a.stack)
+                            a.resid[oo] = rv + acc;
+                        else
+                            a.y[oo] = acc;
+                    }
+                    if (lane == 0) a.d_cnt[r] = 0;
+                }
             }
         }
         if (a.stack && l + 1 < a.n_layers) {
             if (!grid_sync(a.bar, target, a.status, s_flag)) break;
         }
     }
+    ring_drain(ring);
     cp_async_wait_all();
 }
 
 }  // namespace
 
-PersistGeom persist_geom(int T, int H, int E, int K, int F, int F_shared, int wr_bytes, int G, size_t max_smem) {
+PersistGeom persist_geom(int kind, int T, int H, int E, int K, int F, int F_shared, int wr_bytes, int x_f32, int G,
+                         size_t max_smem) {
+    (void)K;
+    (void)F;
+    (void)F_shared;
     PersistGeom g;
     auto al = [](size_t v) { return (v + 127) & ~size_t(127); };
     const int nr = (E + G - 1) / G;
-    const int P = T * K;
-    g.off_wr = 0;
-    g.off_xs = al((size_t)nr * H * wr_bytes);
-    const size_t xs_bytes = (size_t)kMaxTok * (H + 8) * 2;
-    g.off_u = g.off_xs + al(xs_bytes);
-    const size_t topk_part = (size_t)T * ((E + 31) / 32) * 32 * 8;
-    const size_t norm_part = (size_t)T * H * 4;
-    size_t u = kRedBytes;
-    if (topk_part > u) u = topk_part;
-    if (norm_part > u) u = norm_part;
-    const size_t yp_bytes = (size_t)(P + T) * 16 * 4;
     const size_t stat = sizeof(Plan);
-    // h staging: hi and lo rows of up to P routed columns (F + 8 wide) and T shared rows
-    size_t hst = ((size_t)2 * P * (F + 8) + (F_shared ? (size_t)2 * T * (F_shared + 8) : 0) + 256) * 2;
+    g.tab_ld = (E + 3) & ~3;
+    g.off_wr = 0;
+    g.off_tab = al((size_t)nr * H * wr_bytes);
+    g.off_xs = g.off_tab + al((size_t)2 * g.tab_ld * 4);
+    const int xs_rows = x_f32 ? 8 : T;
+    const size_t xs_bytes = (size_t)xs_rows * (H + 8) * 2;
+    g.off_red = g.off_xs + al(xs_bytes);
     g.off_hst = g.off_xs;
-    g.hst_bytes = hst;
-    g.off_yp = al(g.off_hst + hst);
-    size_t dyn = g.off_u + al(u);
-    if (g.off_yp + yp_bytes > dyn) dyn = g.off_yp + yp_bytes;
-    if (dyn + stat > max_smem) {  // no room: the down phase reads h from global memory
-        g.hst_bytes = 0;
-        g.off_yp = g.off_xs;
-        dyn = g.off_u + al(u);
-        if (g.off_yp + yp_bytes > dyn) dyn = g.off_yp + yp_bytes;
+    g.hst_bytes = al(xs_bytes) + kRedBytes;  // h staging reuses xs + red
+    g.off_ring = g.off_xs + g.hst_bytes;
+    g.off_u = g.off_ring;
+    const size_t topk_fast = (size_t)kMaxTok * kMaxSeg * 4 + (size_t)T * kCandCap * 8;
+    const size_t topk_sort = (size_t)T * ((E + 31) / 32) * 32 * 8;
+    const size_t norm = (size_t)T * H * 4;
+    size_t u = topk_fast > topk_sort ? topk_fast : topk_sort;
+    if (norm > u) u = norm;
+    const int gu_chunk = kind == MOE_Q2_64 ? 1152 : 2304;  // the largest piece is one gate/up chunk or more
+    const long long room = (long long)max_smem - (long long)stat - (long long)g.off_ring;
+    long long per_warp = room / (kPersistThreads / 32);
+    if (per_warp > kMaxRingBytes) per_warp = kMaxRingBytes;
+    per_warp &= ~15LL;
+    if (per_warp < gu_chunk) {  // cannot hold one gate/up chunk per warp
+        g.ring_bytes = 0;
+        g.dyn_bytes = g.bytes = (size_t)-1;
+        return g;
     }
-    g.dyn_bytes = dyn;
-    g.bytes = dyn + stat;
+    g.ring_bytes = (int)per_warp;
+    size_t tail = (size_t)g.ring_bytes * (kPersistThreads / 32);
+    if (u > tail) tail = u;
+    g.dyn_bytes = g.off_ring + al(tail);
+    g.bytes = g.dyn_bytes + stat;
+    if (g.bytes > max_smem) {
+        g.ring_bytes = 0;
+        g.dyn_bytes = g.bytes = (size_t)-1;
+    }
     return g;
 }
 
@@ -691,7 +1016,7 @@ int launch_decode_persistent(const PersistArgs &a, int G, cudaStream_t s) {
         kern = a.x_f32 ? (const void *)k_decode<MOE_Q2_64, true> : (const void *)k_decode<MOE_Q2_64, false>;
     else
         kern = a.x_f32 ? (const void *)k_decode<MOE_Q4_32, true> : (const void *)k_decode<MOE_Q4_32, false>;
-    MOE_CUDA_TRY(cudaMemsetAsync(a.bar, 0, 2 * sizeof(unsigned), s));
+    MOE_CUDA_TRY(cudaMemsetAsync(a.bar, 0, (size_t)a.sync_words * sizeof(unsigned), s));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(kPersistThreads);
@@ -716,12 +1041,12 @@ int persist_max_ctas(int smem_bytes, int *G) {
         *G = 0;
         return MOE_OK;
     }
-    int per_sm = 0;
-    MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode<MOE_Q2_64, false>, kPersistThreads,
-                                                               smem_bytes - (int)sizeof(Plan)));
-    int per_sm2 = 0;
-    MOE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm2, k_decode<MOE_Q4_32, false>, kPersistThreads,
-                                                               smem_bytes - (int)sizeof(Plan)));
+    int per_sm = 0, per_sm2 = 0;
+    const int dyn = smem_bytes - (int)sizeof(Plan);
+    MOE_CUDA_TRY(
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode<MOE_Q2_64, false>, kPersistThreads, dyn));
+    MOE_CUDA_TRY(
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm2, k_decode<MOE_Q4_32, false>, kPersistThreads, dyn));
     if (per_sm2 < per_sm) per_sm = per_sm2;
     *G = per_sm >= 1 ? sms : 0;
     return MOE_OK;

@@ -26,7 +26,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kWarps = kGuSplit;
+constexpr int kWarps = 4;  // down: one 16-row tile per warp
 
 // Stream chunks [c_begin, c_end) of one tile through a window of W chunks held
 // in registers (loads for the next W chunks are in flight while one computes).
@@ -101,7 +101,8 @@ __device__ __forceinline__ bool resolve_task(const ExpertArgs &a, int tiles_r, i
 }
 
 template <int KIND, bool XF32>
-__global__ void __launch_bounds__(32 * kWarps) k_gateup(ExpertArgs a) {
+__global__ void __launch_bounds__(32 * GuSplit<KIND>::S) k_gateup(ExpertArgs a) {
+    constexpr int NW = GuSplit<KIND>::S;
     extern __shared__ __align__(16) uint8_t smem[];
     Task tk;
     if (!resolve_task(a, a.src.L.gu_tiles, a.src.shared ? a.src.LS.gu_tiles : 1, tk)) return;
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(32 * kWarps) k_gateup(ExpertArgs a) {
     const int g = lane >> 2, c = lane & 3;
     const BTile bt[1] = {{xs + (size_t)g * ldx + 2 * c, true}};
     const int n_chunks = L.gu_chunks;
-    const int c_begin = gu_chunk_begin(warp, n_chunks), c_end = gu_chunk_begin(warp + 1, n_chunks);
+    const int c_begin = gu_chunk_begin(warp, n_chunks, NW), c_end = gu_chunk_begin(warp + 1, n_chunks, NW);
     const uint8_t *tile_ptr = tk.wbase + (long long)tk.tile * L.gu_tile_bytes;
     float acc3[2][1][4] = {};
     stream_chunks<KIND, 2, 1, 2>(tile_ptr, L.gu_chunk_bytes, L.cb, L.sb, c_begin, c_end, n_chunks, L.gu_half, bt,
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(32 * kWarps) k_gateup(ExpertArgs a) {
     for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[m][q] = acc3[m][0][q];
-    // fixed-order sum over the 4 warps
+    // fixed-order sum over the NW warps
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(32 * kWarps) k_gateup(ExpertArgs a) {
     for (int q = 0; q < 8; ++q) {
         float s = red[lane * 8 + q];
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) s += red[(w * 32 + lane) * 8 + q];
+        for (int w = 1; w < NW; ++w) s += red[(w * 32 + lane) * 8 + q];
         v[q] = s;
     }
     if constexpr (XF32) {
@@ -260,22 +261,16 @@ __global__ void __launch_bounds__(256) k_combine(const float *__restrict__ yp, c
     *yt = accumulate ? *yt + acc : acc;
 }
 
-__global__ void __launch_bounds__(256) k_rmsnorm_bf16(const float *__restrict__ x, int H, float eps,
-                                                      __nv_bfloat16 *__restrict__ out) {
-    __shared__ float ws[8];
+__global__ void __launch_bounds__(kNormThreads) k_rmsnorm_bf16(const float *__restrict__ x, int H, float eps,
+                                                               __nv_bfloat16 *__restrict__ out) {
+    __shared__ float ws[kNormWarps];
     const int t = blockIdx.x, tid = threadIdx.x;
     const float *xt = x + (size_t)t * H;
-    float s = 0.f;
-    for (int h = tid; h < H; h += 256) s = fmaf(xt[h], xt[h], s);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float s = rms_partial(xt, H, tid);
     if ((tid & 31) == 0) ws[tid >> 5] = s;
     __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) tot += ws[w];
-    const float r = 1.0f / sqrtf(tot / (float)H + eps);
-    for (int h = tid; h < H; h += 256) out[(size_t)t * H + h] = __float2bfloat16_rn(xt[h] * r);
+    const float r = rms_scale(ws, H, eps);
+    for (int h = tid; h < H; h += kNormThreads) out[(size_t)t * H + h] = __float2bfloat16_rn(xt[h] * r);
 }
 
 }  // namespace
@@ -284,10 +279,11 @@ int launch_gateup(const ExpertArgs &a, moe_dtype xt, cudaStream_t s) {
     const int tasks = a.max_routed * a.src.L.gu_tiles + (a.src.shared ? a.n_shared * a.src.LS.gu_tiles : 0);
     if (tasks == 0) return MOE_OK;
     const int H = a.src.L.H;
-    const size_t smem = (size_t)8 * (H + 8) * 2 + (size_t)kWarps * 32 * 8 * 4;
+    const int NW = gu_split(a.src.L.kind);
+    const size_t smem = (size_t)8 * (H + 8) * 2 + (size_t)NW * 32 * 8 * 4;
 #define MOE_GU_CASE(KIND, XF)                                                                          \
     {                                                                                                  \
-        k_gateup<KIND, XF><<<tasks, 32 * kWarps, smem, s>>>(a);                                        \
+        k_gateup<KIND, XF><<<tasks, 32 * GuSplit<KIND>::S, smem, s>>>(a);                              \
     }
     const bool f32 = xt == MOE_F32;
     if (a.src.L.kind == MOE_Q2_64) {
@@ -338,7 +334,7 @@ int launch_combine(const float *yp, const float *w, const int32_t *live, int T, 
 
 int launch_rmsnorm_bf16(const float *x, int T, int H, float eps, __nv_bfloat16 *out, cudaStream_t s) {
     if (T == 0) return MOE_OK;
-    k_rmsnorm_bf16<<<T, 256, 0, s>>>(x, H, eps, out);
+    k_rmsnorm_bf16<<<T, kNormThreads, 0, s>>>(x, H, eps, out);
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }

@@ -28,9 +28,12 @@ def ctx(torch):
 def _both_paths(ctx, g, x):
     L.moe_ctx_set_option(ctx, L.OPT_PERSISTENT_DECODE, 1)
     a = g.forward(x)
+    # the comparison means something only if the persistent kernel really ran
+    assert L.moe_ctx_get_option(ctx, L.OPT_LAST_PATH) == 1
     L.moe_ctx_set_option(ctx, L.OPT_PERSISTENT_DECODE, 0)
     try:
         b = g.forward(x)
+        assert L.moe_ctx_get_option(ctx, L.OPT_LAST_PATH) == 0
     finally:
         L.moe_ctx_set_option(ctx, L.OPT_PERSISTENT_DECODE, 1)
     return a, b
@@ -67,8 +70,10 @@ def test_t_invariance_across_the_path_boundary(torch, ctx):
     try:
         x = to_dev(C.activations(cfg, 9, step=333))
         y9, l9, i9 = g.forward(x)
+        assert L.moe_ctx_get_option(ctx, L.OPT_LAST_PATH) == 0
         for t in (0, 4, 8):
             y1, l1, i1 = g.forward(x[t:t + 1].contiguous())
+            assert L.moe_ctx_get_option(ctx, L.OPT_LAST_PATH) == 1
             assert torch.equal(y1[0], y9[t]) and torch.equal(l1[0], l9[t]) and torch.equal(i1[0], i9[t])
     finally:
         g.close()
@@ -88,6 +93,7 @@ def test_persistent_stack_equals_layer_by_layer(torch, ctx, T):
         tin = torch.empty(n, T, cfg.H, dtype=torch.bfloat16, device="cuda")
         tlg = torch.empty(n, T, cfg.E, device="cuda")
         L.moe_stack_forward(g.ctx, descs, ra, 1e-6, ws, tin, tlg)
+        assert L.moe_ctx_get_option(ctx, L.OPT_LAST_PATH) == 1
         assert L.moe_status(ctx) == 0
         # multi-kernel path
         L.moe_ctx_set_option(ctx, L.OPT_PERSISTENT_DECODE, 0)
@@ -120,3 +126,16 @@ def test_persistent_absent_expert(torch, ctx):
         assert not torch.equal(y1, y)
     finally:
         g.close()
+
+
+def test_option_query(torch, ctx):
+    assert L.moe_ctx_get_option(ctx, L.OPT_PERSISTENT_DECODE) == 1
+    L.moe_ctx_set_option(ctx, L.OPT_PERSISTENT_DECODE, 0)
+    try:
+        assert L.moe_ctx_get_option(ctx, L.OPT_PERSISTENT_DECODE) == 0
+    finally:
+        L.moe_ctx_set_option(ctx, L.OPT_PERSISTENT_DECODE, 1)
+    with pytest.raises(L.MoeError):
+        L.moe_ctx_set_option(ctx, L.OPT_LAST_PATH, 1)
+    with pytest.raises(L.MoeError):
+        L.moe_ctx_get_option(ctx, 99)
