@@ -51,6 +51,31 @@ def parse():
     return ap.parse_args()
 
 
+# DRAM traffic of k_decode per layer from one ncu capture (profiles/k_decode_q2_stack48_T1.md:
+# 4-layer chain, T=1, dram__bytes_read.sum + dram__bytes_write.sum = 65,948,928 + 917,760 B);
+# traffic grows in proportion to the layers. It holds only for the kernel sources it
+# was taken on: any change to them makes the figure stale, and it is reported as null.
+TRAFFIC_REF = {"T": 1, "bytes_per_layer": (65_948_928 + 917_760) / 4,
+               "sources_sha256": "22d1820123f28217c0ff146ab5bb1590747ee412748b2f18c3214eb8e7754bc3"}
+KERNEL_SOURCES = ["quantized_expert_ffn_gb300/csrc/decode_persistent.cu",
+                  "quantized_expert_ffn_gb300/csrc/decode_persistent.cuh",
+                  "quantized_expert_ffn_gb300/csrc/decode_common.cuh",
+                  "quantized_expert_ffn_gb300/csrc/moe_internal.cuh"]
+
+
+def measured_traffic(T: int, layers: int):
+    """DRAM bytes per launch of the step kernel, or None if no capture matches."""
+    import hashlib
+    h = hashlib.sha256()
+    root = os.path.dirname(os.path.abspath(__file__))
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(root, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != TRAFFIC_REF["sources_sha256"] or T != TRAFFIC_REF["T"]:
+        return None
+    return TRAFFIC_REF["bytes_per_layer"] * layers
+
+
 def peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -169,6 +194,20 @@ def run_ours(args, rank, world, local_rank):
     stream.synchronize()
     assert L.moe_status(ctx, stream) == 0
     path = "persistent" if L.moe_ctx_get_option(ctx, L.OPT_LAST_PATH) == 1 else "multi-kernel"
+    # distinct experts per layer (the bytes a window really streams), from a traced pass
+    tlg = torch.empty(args.layers, T, cfg.E, dtype=torch.float32, device="cuda")
+    tin = torch.empty(args.layers, T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(stream):
+        L.moe_stack_forward(ctx, st.descs, resid.clone(), EPS, ws, tin, tlg)
+    stream.synchronize()
+    lg = tlg.cpu().numpy()
+    distinct = []
+    for l in range(args.layers):
+        chosen = set()
+        for t in range(T):
+            order = np.lexsort((np.arange(cfg.E), -lg[l, t]))  # logit descending, index ascending
+            chosen.update(int(e) for e in order[:cfg.K])
+        distinct.append(len(chosen))
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         L.moe_stack_forward(ctx, st.descs, resid, EPS, ws)
@@ -228,7 +267,8 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
     ms, e2e_ms_max = float(times[0]), float(times[1])
-    return dict(ms=ms, e2e_ms=e2e_ms_max, layer_ms=layer_ms, clocks=clocks, status=status, cfg=cfg, path=path)
+    return dict(ms=ms, e2e_ms=e2e_ms_max, layer_ms=layer_ms, clocks=clocks, status=status, cfg=cfg, path=path,
+                distinct=distinct)
 
 
 # ------------------------------------------------------------------ oracle (CPU)
@@ -305,12 +345,13 @@ def main():
     hbm_peak = pk["hbm_gbs"] if pk else 6800.0
     expert_bytes = cfg.expert_bytes()
     router_bytes = cfg.E * cfg.H * 2
-    # algorithmic bytes of one layer call at T=1: K distinct experts + the router matrix
-    # (for T > 1 the distinct experts per layer vary; K*T is their upper bound)
-    layer_bytes = cfg.K * T * expert_bytes + router_bytes
-    graph_layer_ms = r["ms"] / args.steps / args.layers
-    achieved = layer_bytes / (graph_layer_ms / 1e3) / 1e9
-    step_expert_gbs = args.layers * cfg.K * expert_bytes / (r["ms"] / args.steps / 1e3) / 1e9
+    # algorithmic bytes of one step (= one launch of the persistent kernel): per layer the
+    # distinct experts of the window plus the router matrix
+    step_expert_bytes = sum(r["distinct"]) * expert_bytes
+    step_bytes = step_expert_bytes + args.layers * router_bytes
+    step_s = r["ms"] / args.steps / 1e3
+    achieved = step_bytes / step_s / 1e9
+    step_expert_gbs = step_expert_bytes / step_s / 1e9
     # kernels of ours per step: the persistent path runs the whole 48-layer chain as
     # one cooperative kernel (plus a memset of its barrier words); the multi-kernel
     # path runs rmsnorm, router, top-k, bucket, plan, gate/up, down, combine per layer
@@ -321,15 +362,19 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 mma / fp32 accumulate (Q2_0 weights)",
         "data": "synthetic", "config": cfgj,
         "stack_tokens_per_s": n_gpus * T * args.steps / (r["ms"] / 1e3),
-        "expert_weight_gbs": step_expert_gbs if T == 1 else None,
-        "expert_weight_frac_of_hbm": (step_expert_gbs / hbm_peak) if T == 1 else None,
+        "expert_weight_gbs": step_expert_gbs,
+        "expert_weight_frac_of_hbm": step_expert_gbs / hbm_peak,
+        "distinct_experts_per_layer": float(np.mean(r["distinct"])),
         "eager_layer_ms": r["layer_ms"],
-        "roofline": {"kernel": ("k_decode (persistent, one launch per step), per layer" if r["path"] == "persistent"
-                                else "one MoE layer call (8 launches, in the captured step graph)"),
+        "roofline": {"kernel": ("k_decode: one cooperative launch runs the whole chain of layers"
+                                if r["path"] == "persistent"
+                                else "the step's 8-kernel layer calls, in the captured step graph"),
                      "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak,
+                     "traffic": (measured_traffic(T, args.layers) if r["path"] == "persistent" else None),
                      "peak_source": "measured" if pk else "fallback",
-                     "algorithmic_bytes_per_launch": layer_bytes},
+                     "algorithmic_bytes_per_launch": step_bytes,
+                     "algorithmic_bytes": "per layer: distinct experts x 1,382,400 B + router 2,621,440 B"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * cfg.H * 4,
                 "d2h_bytes_per_step": T * cfg.H * 4},
         "gpu_launches": launches_per_step * args.steps,
