@@ -112,14 +112,27 @@ MOE_API int moe_ctx_destroy(moe_ctx *ctx);
 #define MOE_OPT_PERSISTENT_DECODE 1
 MOE_API int moe_ctx_set_option(moe_ctx *ctx, int option, int value);
 
-/* Read a context option into *value. Besides MOE_OPT_PERSISTENT_DECODE:
- * MOE_OPT_LAST_PATH (read only): 1 if the last moe_layer_forward*,
- * moe_layer_forward_static or moe_stack_forward* call on this context ran the
- * persistent kernel, 0 if it ran the multi-kernel path (or no such call yet).
+/* Read a context option into *value. Besides the settable options:
+ * MOE_OPT_LAST_PATH (read only): which path the last moe_layer_forward*,
+ * moe_layer_forward_static, moe_stack_forward* or moe_expert_ffn call on this
+ * context ran for its experts: 1 the persistent decode kernel, 2 the tensor-core
+ * (tcgen05) grouped GEMMs, 0 the multi-kernel mma.sync path (or no call yet).
  * MOE_ERR_ARG for an unknown option or a null pointer; setting
  * MOE_OPT_LAST_PATH is MOE_ERR_ARG too. */
 #define MOE_OPT_LAST_PATH 2
 MOE_API int moe_ctx_get_option(moe_ctx *ctx, int option, int *value);
+
+/* MOE_OPT_PREFILL_MIN_T (default 64, settable, >= 1): windows of at least this
+ * many tokens run their Q4 experts (routed and shared, H a multiple of 128) as
+ * grouped GEMMs on the tensor cores (kairos-engine README, "Prefill and decode are
+ * different machines"): weights dequantised to fp16 (w = fp16(d*(q-8)), one
+ * rounding), x and h in fp16, fp32 accumulation. Those results differ from the
+ * mma.sync path by that rounding (both stay within the oracle's tolerance).
+ * Q2_0 experts and smaller windows keep the mma.sync path. The router of such a
+ * window (bf16 x and Wr, any format) is a tensor-core GEMM too: its logits can
+ * differ from the per-row CUDA-core order in the last bits, and moe_router_topk
+ * follows the same rule, so a window routes identically through either entry. */
+#define MOE_OPT_PREFILL_MIN_T 3
 
 /* Synchronise `stream`, then read and clear the device status bits into *bits.
  * Returns MOE_OK even when bits are set; the caller inspects them. */

@@ -140,6 +140,7 @@ def moe_ctx_destroy(ctx: int):
 
 OPT_PERSISTENT_DECODE = 1
 OPT_LAST_PATH = 2
+OPT_PREFILL_MIN_T = 3
 
 
 def moe_ctx_set_option(ctx: int, option: int, value: int):

@@ -7,13 +7,15 @@
 #include <vector>
 
 #include "decode_persistent.cuh"
+#include "prefill_gemm.cuh"
 #include "moe_internal.cuh"
 
 struct moe_ctx {
     int device;
     uint32_t *d_status;
-    int persistent;  // MOE_OPT_PERSISTENT_DECODE
-    int last_path;   // MOE_OPT_LAST_PATH
+    int persistent;   // MOE_OPT_PERSISTENT_DECODE
+    int last_path;    // MOE_OPT_LAST_PATH
+    int prefill_min;  // MOE_OPT_PREFILL_MIN_T
     int max_smem;    // opt-in shared memory per block
 };
 
@@ -86,7 +88,7 @@ int check_dims(int H, int F) {
 // Workspace carving for one layer call of up to T tokens.
 struct WsLayout {
     size_t logits, ids, w, counts, offsets, perm, active, n_active, live, cols, groups_gu, groups_d, n_groups, h, yp,
-        u, bar, total;
+        u, x16, bar, total;
     int sync_words;  // persistent path: barrier words + down tile counters
     int max_routed_gu, max_routed_d, max_shared, h_ld;
 };
@@ -119,6 +121,7 @@ WsLayout ws_layout(const moe_layer_desc *d, int T, int nc_gu) {
     W.h = take((P + T) * (size_t)W.h_ld * 4);
     W.yp = take((P + T) * (size_t)d->H * 4);
     W.u = take((size_t)T * d->H * 2);
+    W.x16 = take((size_t)T * d->H * 2);
     W.sync_words = 4 + d->H / 16;
     W.bar = take((size_t)W.sync_words * 4);
     W.total = o;
@@ -154,12 +157,44 @@ int check_ws(void *ws, size_t ws_bytes, size_t need) {
     return MOE_OK;
 }
 
+// Router logits: windows of at least MOE_OPT_PREFILL_MIN_T tokens with bf16 x and
+// Wr run the GEMM on the tensor cores (fp32 accumulation in tensor memory); other
+// windows use the CUDA-core kernel with the canonical per-row order.
+int router_logits(moe_ctx *ctx, const void *x, moe_dtype xt, int T, int H, const void *Wr, moe_dtype wt,
+                  const float *bias, int E, float *logits, cudaStream_t s) {
+    if (T >= ctx->prefill_min && xt == MOE_BF16 && wt == MOE_BF16 && umma_router_supported(H) &&
+        (size_t)ctx->max_smem >= umma_smem_bytes() && (uintptr_t)x % 16 == 0 && (uintptr_t)Wr % 16 == 0) {
+        int sms = 0;
+        MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device));
+        UmmaArgs ua;
+        memset(&ua, 0, sizeof ua);
+        ua.mode = 2;
+        ua.wr = (const __nv_bfloat16 *)Wr;
+        ua.xb = (const __nv_bfloat16 *)x;
+        ua.bias = bias;
+        ua.logits = logits;
+        ua.E = E;
+        ua.H = H;
+        ua.T = T;
+        ua.n_mt = (E + 127) / 128;
+        ua.status = ctx->d_status;
+        const int tiles = ua.n_mt * ((T + 255) / 256);
+        return launch_umma(ua, tiles < sms ? tiles : sms, s);
+    }
+    return launch_router_logits(x, xt, T, H, Wr, wt, bias, E, logits, s);
+}
+
 // Steps 4-6 (plan, experts, combine) given ids, w, offsets, perm.
 int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype xt, int T, const int32_t *ids,
                 const float *w, const int32_t *offsets, const int32_t *perm, float *y, int accumulate,
                 uint8_t *ws, const WsLayout &W, cudaStream_t s) {
     const moe_slots *sl = d->slots;
-    const int nc_gu = xt == MOE_F32 ? 4 : 8;
+    // prefill-sized windows of Q4 experts: tcgen05 grouped GEMMs on column groups of
+    // up to 256 live pairs; otherwise the mma.sync kernels on groups of 8 (4) columns
+    const bool umma = T >= ctx->prefill_min && umma_supported(sl->layout) &&
+                      (!d->shared || umma_supported(d->shared->layout)) &&
+                      (size_t)ctx->max_smem >= umma_smem_bytes();
+    const int nc_gu = umma ? 256 : (xt == MOE_F32 ? 4 : 8);
     PlanArgs pa;
     pa.ids = ids;
     pa.w = w;
@@ -172,7 +207,7 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
     pa.K = d->K;
     pa.E = d->E;
     pa.nc_gu = nc_gu;
-    pa.nc_d = 4;
+    pa.nc_d = umma ? 256 : 4;
     pa.max_routed_gu = W.max_routed_gu;
     pa.max_routed_d = W.max_routed_d;
     pa.has_shared = d->shared != nullptr;
@@ -208,6 +243,45 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
     ea.un = make_unpack(sl->fmt.zero_point);
     ea.un_s = d->shared ? make_unpack(d->shared->fmt.zero_point) : ea.un;
     ea.status = ctx->d_status;
+    if (umma) {
+        // x -> fp16 rows, then the gate/up GEMM (h as fp16 in plan-column rows) and
+        // the down GEMM (y_pair), then the k-ordered combine
+        __half *x16 = (__half *)(ws + W.x16);
+        rc = launch_to_f16(x, xt == MOE_F32 ? 1 : 0, (size_t)T * d->H, x16, s);
+        if (rc) return rc;
+        int sms = 0;
+        MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device));
+        UmmaArgs ua;
+        ua.mode = 0;
+        ua.groups = pa.groups_gu;
+        ua.n_groups = pa.n_groups;
+        ua.max_routed = W.max_routed_gu;
+        ua.n_shared = d->shared ? (T + nc_gu - 1) / nc_gu : 0;
+        ua.n_mt = sl->layout.F / 64;
+        ua.n_mt_s = d->shared ? d->shared->layout.F / 64 : 0;
+        ua.cols = pa.cols;
+        ua.T = T;
+        ua.K = d->K;
+        ua.act = d->act;
+        ua.src = ea.src;
+        ua.x16 = x16;
+        ua.h16 = (__half *)(ws + W.h);
+        ua.h16_ld = W.h_ld;
+        ua.yp = ea.yp;
+        ua.status = ctx->d_status;
+        rc = launch_umma(ua, sms, s);
+        if (rc) return rc;
+        ua.mode = 1;
+        ua.groups = pa.groups_d;
+        ua.n_groups = pa.n_groups + 1;
+        ua.max_routed = W.max_routed_d;
+        ua.n_mt = sl->layout.H / 128;
+        ua.n_mt_s = d->shared ? d->shared->layout.H / 128 : 0;
+        rc = launch_umma(ua, sms, s);
+        if (rc) return rc;
+        ctx->last_path = 2;
+        return launch_combine(ea.yp, w, pa.live, T, d->K, d->H, d->shared != nullptr, accumulate, y, s);
+    }
     // gate/up
     ea.groups = pa.groups_gu;
     ea.n_groups = pa.n_groups;
@@ -326,7 +400,7 @@ int layer_core(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype x
     float *logits = logits_out ? logits_out : (float *)(ws + W.logits);
     int32_t *ids = ids_out ? ids_out : (int32_t *)(ws + W.ids);
     float *w = (float *)(ws + W.w);
-    int rc = launch_router_logits(x, xt, T, d->H, d->Wr, d->wr_dtype, d->bias, d->E, logits, s);
+    int rc = router_logits(ctx, x, xt, T, d->H, d->Wr, d->wr_dtype, d->bias, d->E, logits, s);
     if (rc) return rc;
     rc = launch_topk(logits, T, d->E, d->K, ids, w, ctx->d_status, s);
     if (rc) return rc;
@@ -395,7 +469,7 @@ int moe_ctx_create(int device, moe_ctx **out) {
         return set_error(MOE_ERR_CUDA, "no CUDA device %d (%d visible)", device, n);
     DeviceGuard g(device);
     if (!g.ok) return set_error(MOE_ERR_CUDA, "cudaSetDevice(%d) failed", device);
-    moe_ctx *c = new moe_ctx{device, nullptr, 1, 0, 0};
+    moe_ctx *c = new moe_ctx{device, nullptr, 1, 0, 64, 0};
     cudaError_t e = cudaMalloc(&c->d_status, sizeof(uint32_t));
     if (e != cudaSuccess) {
         delete c;
@@ -418,6 +492,7 @@ int moe_ctx_create(int device, moe_ctx **out) {
     if (!rc) rc = init_expert_attributes(max_smem);
     if (!rc) rc = init_repack_attributes(max_smem);
     if (!rc) rc = init_persist_attributes(max_smem);
+    if (!rc) rc = init_umma_attributes(max_smem);
     c->max_smem = max_smem;
     if (rc) {
         cudaFree(c->d_status);
@@ -445,6 +520,11 @@ int moe_ctx_set_option(moe_ctx *ctx, int option, int value) {
         return MOE_OK;
     }
     if (option == MOE_OPT_LAST_PATH) return set_error(MOE_ERR_ARG, "option %d is read only", option);
+    if (option == MOE_OPT_PREFILL_MIN_T) {
+        if (value < 1) return set_error(MOE_ERR_ARG, "MOE_OPT_PREFILL_MIN_T must be >= 1, got %d", value);
+        ctx->prefill_min = value;
+        return MOE_OK;
+    }
     return set_error(MOE_ERR_ARG, "unknown option %d", option);
 }
 
@@ -456,6 +536,10 @@ int moe_ctx_get_option(moe_ctx *ctx, int option, int *value) {
     }
     if (option == MOE_OPT_LAST_PATH) {
         *value = ctx->last_path;
+        return MOE_OK;
+    }
+    if (option == MOE_OPT_PREFILL_MIN_T) {
+        *value = ctx->prefill_min;
         return MOE_OK;
     }
     return set_error(MOE_ERR_ARG, "unknown option %d", option);
@@ -633,7 +717,7 @@ int moe_router_topk(moe_ctx *ctx, const void *x, moe_dtype xt, int T, int H, con
     const cudaStream_t s = (cudaStream_t)stream;
     float *logits = logits_out;
     if (!logits) return set_error(MOE_ERR_ARG, "logits_out is required by this implementation (pass a [T][E] buffer)");
-    int rc = launch_router_logits(x, xt, T, H, Wr, wt, bias, E, logits, s);
+    int rc = router_logits(ctx, x, xt, T, H, Wr, wt, bias, E, logits, s);
     if (rc) return rc;
     return launch_topk(logits, T, E, K, ids, w, ctx->d_status, s);
 }

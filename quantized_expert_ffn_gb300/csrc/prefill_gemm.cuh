@@ -1,0 +1,47 @@
+// prefill_gemm.cuh -- arguments of the tcgen05 grouped GEMMs for prefill windows.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+// One launch runs the gate/up GEMM (mode 0: h = act(gate) * up, fp16, row = plan
+// column) or the down GEMM (mode 1: y_pair rows, fp32) over every column group of
+// the plan (groups of at most 256 live columns of one expert; the shared expert's
+// groups start at max_routed) and every 128-row M-tile of the weights; or the
+// router GEMM (mode 2: logits = Wr x + bias, bf16 operands) over 128-expert by
+// 256-token tiles.
+struct UmmaArgs {
+    int mode;
+    // mode 2
+    const __nv_bfloat16 *wr;  // [E][H]
+    const __nv_bfloat16 *xb;  // [T][H]
+    const float *bias;        // [E] or null
+    float *logits;            // [T][E]
+    int E, H;
+    const Group *groups;
+    const int32_t *n_groups;  // routed group count (device)
+    int max_routed, n_shared;
+    int n_mt, n_mt_s;         // M-tiles per routed / shared group
+    const int32_t *cols;      // plan columns: pair p >= 0, shared token -(t + 1)
+    int T, K, act;
+    ExpertSrc src;
+    const __half *x16;        // gate/up B rows: [T][H] fp16
+    __half *h16;              // [P + T][h16_ld] fp16, row = plan column
+    int h16_ld;
+    float *yp;                // [P + T][H] fp32: row p for pair p, P + t for the shared expert
+    uint32_t *status;
+};
+
+// The GEMMs run for Q4 layouts whose H is a multiple of 128 and F of 64.
+bool umma_supported(const QLayout &L);
+// The router GEMM runs for bf16 x and Wr with H a multiple of 64.
+bool umma_router_supported(int H);
+int launch_umma(const UmmaArgs &a, int n_ctas, cudaStream_t s);
+int launch_to_f16(const void *x, int xf32, size_t n, __half *out, cudaStream_t s);
+int init_umma_attributes(int max_smem);
+size_t umma_smem_bytes();
+
+}  // namespace moe

@@ -10,17 +10,18 @@ namespace moe {
 
 namespace {
 
-constexpr int kRouterTok = 8;  // tokens per CTA
-constexpr int kRouterExp = 2;  // experts per CTA (4 warps each)
+constexpr int kRouterTok = 8;   // tokens per CTA
+constexpr int kRouterExp = 16;  // experts per CTA (one warp each)
 
-// grid (ceil(E/2), ceil(T/8)), 256 threads: 4 warps per expert row with the
-// canonical order of router_partial / combine_router4.
+// grid (ceil(E/16), ceil(T/8)), 512 threads: warp w owns expert row 16 bx + w and
+// computes the four 128-lane slot partials of the canonical order (router_partial
+// with L = 32q + lane, q = 0..3) one after another, then combine_router4. The
+// x rows staged in shared memory serve 16 experts.
 template <typename XT, typename WT>
-__global__ void __launch_bounds__(256) k_router_logits(const XT *__restrict__ x, const WT *__restrict__ Wr,
-                                                       const float *__restrict__ bias, int T, int H, int E,
-                                                       float *__restrict__ logits) {
+__global__ void __launch_bounds__(32 * kRouterExp) k_router_logits(const XT *__restrict__ x, const WT *__restrict__ Wr,
+                                                                   const float *__restrict__ bias, int T, int H, int E,
+                                                                   float *__restrict__ logits) {
     extern __shared__ __align__(16) float xs[];  // [8][H]
-    __shared__ float part[kRouterExp][4][kRouterTok];
     const int t0 = blockIdx.y * kRouterTok;
     const int nt = min(kRouterTok, T - t0);
     for (int i = threadIdx.x; i < nt * H / 8; i += blockDim.x) {
@@ -32,10 +33,11 @@ __global__ void __launch_bounds__(256) k_router_logits(const XT *__restrict__ x,
     }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int er = warp >> 2, q = warp & 3;
-    const int e = blockIdx.x * kRouterExp + er;
-    if (e < E) {
-        float acc[kRouterTok];
+    const int e = blockIdx.x * kRouterExp + warp;
+    if (e >= E) return;
+    float part[4][kRouterTok];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
         router_partial<WT, kRouterTok>(Wr + (size_t)e * H, H, 32 * q + lane, nt,
                                        [&](int t, int h, float v[8]) {
                                            const float4 xa = *reinterpret_cast<const float4 *>(&xs[t * H + h]);
@@ -43,17 +45,13 @@ __global__ void __launch_bounds__(256) k_router_logits(const XT *__restrict__ x,
                                            v[0] = xa.x; v[1] = xa.y; v[2] = xa.z; v[3] = xa.w;
                                            v[4] = xb.x; v[5] = xb.y; v[6] = xb.z; v[7] = xb.w;
                                        },
-                                       acc);
-        if (lane == 0)
-            for (int t = 0; t < nt; ++t) part[er][q][t] = acc[t];
-    }
-    __syncthreads();
-    if (threadIdx.x < kRouterExp * kRouterTok) {
-        const int er2 = threadIdx.x / kRouterTok, t = threadIdx.x % kRouterTok;
-        const int e2 = blockIdx.x * kRouterExp + er2;
-        if (e2 < E && t < nt) {
-            float p4[4] = {part[er2][0][t], part[er2][1][t], part[er2][2][t], part[er2][3][t]};
-            logits[(size_t)(t0 + t) * E + e2] = combine_router4(p4) + (bias ? bias[e2] : 0.f);
+                                       part[q]);
+    // every lane holds the four warp-reduced slot sums; lane t writes token t
+#pragma unroll
+    for (int t = 0; t < kRouterTok; ++t) {
+        if (t < nt && lane == t) {
+            const float p4[4] = {part[0][t], part[1][t], part[2][t], part[3][t]};
+            logits[(size_t)(t0 + t) * E + e] = combine_router4(p4) + (bias ? bias[e] : 0.f);
         }
     }
 }
@@ -104,7 +102,7 @@ int launch_router_logits(const void *x, moe_dtype xt, int T, int H, const void *
     if (smem > 200 * 1024) return set_error(MOE_ERR_SHAPE, "router: H=%d too large", H);
 #define MOE_ROUTER_CASE(XT, WT)                                                                     \
     {                                                                                               \
-        k_router_logits<XT, WT><<<grid, 256, smem, s>>>((const XT *)x, (const WT *)Wr, bias, T, H, E, logits); \
+        k_router_logits<XT, WT><<<grid, 32 * kRouterExp, smem, s>>>((const XT *)x, (const WT *)Wr, bias, T, H, E, logits); \
     }
     if (xt == MOE_F32 && wt == MOE_F32) MOE_ROUTER_CASE(float, float)
     else if (xt == MOE_F32 && wt == MOE_BF16) MOE_ROUTER_CASE(float, __nv_bfloat16)

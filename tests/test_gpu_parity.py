@@ -36,7 +36,7 @@ def _x(cfg, T, step=0):
 # ------------------------------------------------------------------ router + top-k
 
 @pytest.mark.parametrize("name,T", [("tiny", 4), ("q2_layer", 1), ("q2_layer", 4), ("gemma_layer", 8),
-                                    ("gemma_layer", 37)])
+                                    ("gemma_layer", 37), ("q2_layer", 100), ("gemma_layer", 300)])
 def test_router_topk_matches_oracle(torch, ctx, name, T):
     cfg = C.CONFIGS[name]
     x = _x(cfg, T, step=3)
