@@ -117,11 +117,11 @@ WsLayout ws_layout(const moe_layer_desc *d, int T, int nc_gu) {
     W.cols = take((P + T) * 4);
     W.groups_gu = take((size_t)max_groups * sizeof(Group));
     W.groups_d = take((size_t)max_groups * sizeof(Group));
-    W.n_groups = take(8);
+    W.n_groups = take(16);
     W.h = take((P + T) * (size_t)W.h_ld * 4);
     W.yp = take((P + T) * (size_t)d->H * 4);
     W.u = take((size_t)T * d->H * 2);
-    W.x16 = take((size_t)T * d->H * 2);
+    W.x16 = take((P + T) * (size_t)d->H * 2);  // x in plan-column order (tensor-core path)
     W.sync_words = 4 + d->H / 16;
     W.bar = take((size_t)W.sync_words * 4);
     W.total = o;
@@ -178,6 +178,11 @@ int router_logits(moe_ctx *ctx, const void *x, moe_dtype xt, int T, int H, const
         ua.T = T;
         ua.n_mt = (E + 127) / 128;
         ua.status = ctx->d_status;
+        int rc = make_tmap_2d(&ua.tmap_b, x, true, (unsigned long long)T, (unsigned long long)H,
+                              (unsigned long long)H * 2);
+        if (!rc) rc = make_tmap_2d(&ua.tmap_a, Wr, true, (unsigned long long)E, (unsigned long long)H,
+                                   (unsigned long long)H * 2, 128);
+        if (rc) return rc;
         const int tiles = ua.n_mt * ((T + 255) / 256);
         return launch_umma(ua, tiles < sms ? tiles : sms, s);
     }
@@ -246,12 +251,14 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
     if (umma) {
         // x -> fp16 rows, then the gate/up GEMM (h as fp16 in plan-column rows) and
         // the down GEMM (y_pair), then the k-ordered combine
+        const int maxc = (int)(T * d->K + T);
         __half *x16 = (__half *)(ws + W.x16);
-        rc = launch_to_f16(x, xt == MOE_F32 ? 1 : 0, (size_t)T * d->H, x16, s);
+        rc = launch_gather_f16(pa.cols, pa.n_groups + 2, x, xt == MOE_F32 ? 1 : 0, d->K, d->H, maxc, x16, s);
         if (rc) return rc;
         int sms = 0;
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device));
         UmmaArgs ua;
+        memset(&ua, 0, sizeof ua);
         ua.mode = 0;
         ua.groups = pa.groups_gu;
         ua.n_groups = pa.n_groups;
@@ -269,7 +276,13 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
         ua.h16_ld = W.h_ld;
         ua.yp = ea.yp;
         ua.status = ctx->d_status;
+        rc = make_tmap_2d(&ua.tmap_b, x16, false, (unsigned long long)maxc, (unsigned long long)d->H,
+                          (unsigned long long)d->H * 2);
+        if (rc) return rc;
         rc = launch_umma(ua, sms, s);
+        if (rc) return rc;
+        rc = make_tmap_2d(&ua.tmap_b, ua.h16, false, (unsigned long long)maxc, (unsigned long long)W.h_ld,
+                          (unsigned long long)W.h_ld * 2);
         if (rc) return rc;
         ua.mode = 1;
         ua.groups = pa.groups_d;

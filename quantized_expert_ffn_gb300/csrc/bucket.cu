@@ -175,6 +175,7 @@ __global__ void __launch_bounds__(kBucketThreads) k_plan(PlanArgs a) {
     if (tid == 0) {
         a.n_groups[0] = tot_gu;
         a.n_groups[1] = tot_d;
+        a.n_groups[2] = nlive + (a.has_shared ? a.T : 0);  // plan columns
     }
     if (a.has_shared) {
         for (int t = tid; t < a.T; t += blockDim.x) a.cols[nlive + t] = -(t + 1);

@@ -247,7 +247,7 @@ struct PlanArgs {
     int32_t *live;   // [T*K] 1 if the pair does expert work
     int32_t *cols;   // [T*K + T]
     Group *groups_gu, *groups_d;
-    int32_t *n_groups;  // [2] routed group counts (gate/up, down)
+    int32_t *n_groups;  // [3] routed group counts (gate/up, down), plan columns
     uint32_t *status;
 };
 

@@ -8,12 +8,13 @@
 //
 //   D[128 weight rows][<=256 tokens] += A[128][64] * B[<=256][64]^T per stage
 //
-//   A  128 rows of Q4 weights, dequantised by 4 producer warps from the packed
-//      layout (codes + per-32 fp16 scales, copied in with cp.async) into fp16
-//      w = fp16(d * (q - 8)) (one rounding; q - 8 is exact), stored K-major with
-//      the 128-byte swizzle the MMA descriptor names;
-//   B  the group's token rows, 64 fp16 each per stage, gathered with cp.async
-//      (gate/up: rows of x converted to fp16; down: rows of h in plan order);
+//   A  128 rows of Q4 weights: one TMA warp brings each 128-k chunk of the packed
+//      layout (codes + per-32 fp16 scales) in with bulk copies; 8 dequant warps turn
+//      it into fp16 w = fp16(d * (q - 8)) (one rounding; q - 8 is exact) and store
+//      it with stmatrix, K-major with the 128-byte swizzle the MMA descriptor names;
+//   B  the group's rows, 64 fp16 each per stage, loaded by the TMA warp through a
+//      tensor map in boxes of 32 rows (gate/up: x gathered into plan order and
+//      converted to fp16 once per layer; down: h in plan order);
 //   MMA one thread issues 4 x tcgen05.mma (K = 16 each) per stage and commits to
 //      the stage's "empty" barrier; after the last stage it commits the tile to an
 //      "accumulator full" barrier; two accumulators of 256 TMEM columns alternate;
@@ -26,6 +27,8 @@
 // CTAs (one per SM) take tiles round-robin. Every barrier wait gives up after
 // about a second (MOE_STATUS_TIMEOUT) and the CTA stops; the TMEM it allocated is
 // released on every path.
+#include <cudaTypedefs.h>
+
 #include "decode_common.cuh"
 #include "prefill_gemm.cuh"
 
@@ -33,21 +36,29 @@ namespace moe {
 
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;  // A/B ring of MMA stages
-constexpr int kPStages = 6, kPLead = 4, kBLead = 2;          // packed-weight ring; load lead (items)
-constexpr int kProdWarps = 8, kMmaWarp = 8, kEpiWarps = 4;
-constexpr int kThreads = 32 * (kProdWarps + 1 + kEpiWarps);  // 416
-constexpr int kProdThreads = 32 * kProdWarps;
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kAStages = 4, kBStages = 4;  // A (dequantised locally) and B (TMA from L2) rings
+constexpr int kPSlots = 3;                                   // packed ring: one 128-k chunk per slot
+constexpr int kBoxRows = 256;                                // rows per B box (32 KB: one box per stage)
+constexpr int kABoxRows = 128;                               // rows per router A box
+// two groups of 8 dequant warps take alternate stages (two stages in flight)
+// one TMA warp for the packed weights, one for the B rows (each blocks only on its own
+// barriers)
+constexpr int kDqWarps = 16, kTmaWarp = 16, kTmaBWarp = 17, kMmaWarp = 18, kEpiWarps = 4;
+constexpr int kThreads = 32 * (kDqWarps + 3 + kEpiWarps);  // 736
+constexpr int kDqThreads = 32 * kDqWarps;
+constexpr int kDqGroup = kDqThreads / 2;
 constexpr int kATile = kBM * kBK * 2;      // 16 KB
 constexpr int kBTile = kBN * kBK * 2;      // 32 KB
-constexpr int kPacked = 4608;              // packed codes + scales of one stage (Q4, 128 rows x 64)
+constexpr int kPacked = 9216;              // packed codes + scales of one 128-k chunk (Q4, 128 rows)
 constexpr int kTmemCols = 512;             // two 256-column fp32 accumulators
+constexpr int kTileCache = 96;             // tile descriptors staged in shared memory per CTA
 constexpr long long kSpin = 2000000000LL;  // about 1 s
 
 constexpr size_t kSmemA = 0;
-constexpr size_t kSmemB = kSmemA + (size_t)kStages * kATile;
-constexpr size_t kSmemP = kSmemB + (size_t)kStages * kBTile;
-constexpr size_t kSmemBytes = kSmemP + (size_t)kPStages * kPacked;  // 224,256
+constexpr size_t kSmemB = kSmemA + (size_t)kAStages * kATile;
+constexpr size_t kSmemP = kSmemB + (size_t)kBStages * kBTile;
+constexpr size_t kSmemBytes = kSmemP + (size_t)kPSlots * kPacked;  // 219,136
 static_assert(kSmemB % 1024 == 0 && kSmemP % 16 == 0, "swizzled tiles need 1024-byte alignment");
 
 __device__ __forceinline__ unsigned su32(const void *p) { return (unsigned)__cvta_generic_to_shared(p); }
@@ -82,6 +93,43 @@ __device__ __forceinline__ bool mbar_try(uint64_t *m, unsigned parity) {
     unsigned ok;
     asm volatile(
         "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(su32(m)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *m, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(m)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *m) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     su32(dst)),
+                 "l"(src), "r"(bytes), "r"(su32(m))
+                 : "memory");
+}
+// One box (64 elements x the map's box rows, 128-byte swizzle) of a 2-D tensor map at column
+// c0 (a multiple of 64) and row c1.
+__device__ __forceinline__ void tma_box(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *m) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(su32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(su32(m))
+        : "memory");
+}
+// Four 8x8 matrices of 16-bit elements, one register of each per lane in the
+// mma fragment layout; lane l gives the address of row l % 8 of matrix l / 8.
+__device__ __forceinline__ void stmatrix4(void *row_addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(su32(row_addr)), "r"(r0),
+                 "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
+// Non-blocking check of a barrier phase (try_wait may suspend the thread for a while).
+__device__ __forceinline__ bool mbar_test(uint64_t *m, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
         : "=r"(ok)
         : "r"(su32(m)), "r"(parity)
         : "memory");
@@ -178,35 +226,32 @@ __device__ __forceinline__ bool tile_info(const UmmaArgs &a, int n_routed, int t
     return true;
 }
 
-// Where the packed bytes of stage s of tile ti come from: piece i (16 bytes, 0..287)
-// of the 4,608-byte stage image.
-__device__ __forceinline__ const uint8_t *packed_src(const UmmaArgs &a, const TileInfo &ti, const uint8_t *wbase,
-                                                     int s, int i) {
+// The packed image of 128-k chunk c of tile ti (slot layout): gate/up: 4 row tiles
+// x their whole chunk [gate codes 1024 | up codes 1024 | gate scales 128 | up scales
+// 128] at 2,304-byte strides; down: 8 row tiles x [codes 1024 | scales 128] at
+// 1,152-byte strides (a last half chunk [codes 512 | scales 64]). Piece j: source
+// and bytes.
+__device__ __forceinline__ const uint8_t *chunk_piece(const UmmaArgs &a, const TileInfo &ti, const uint8_t *wbase,
+                                                      int c, int j, int &bytes) {
     const QLayout &L = ti.shared ? a.src.LS : a.src.L;
-    const int c = s >> 1, h = s & 1;
     if (a.mode == 0) {
-        // 4 gate/up row tiles x [gate codes 512 | up codes 512 | gate scales 64 | up scales 64]
-        const int j = i / 72, pp = i % 72;
-        const uint8_t *ch = wbase + (long long)(4 * ti.mt + j) * L.gu_tile_bytes + (long long)c * L.gu_chunk_bytes;
-        if (pp < 32) return ch + h * 512 + 16 * pp;
-        if (pp < 64) return ch + L.cb + h * 512 + 16 * (pp - 32);
-        if (pp < 68) return ch + 2 * L.cb + h * 64 + 16 * (pp - 64);
-        return ch + 2 * L.cb + L.sb + h * 64 + 16 * (pp - 68);
+        bytes = L.gu_chunk_bytes;
+        return wbase + (long long)(4 * ti.mt + j) * L.gu_tile_bytes + (long long)c * L.gu_chunk_bytes;
     }
-    // down: 8 row tiles x [codes 512 | scales 64]; the last chunk of a row may be half
-    const int j = i / 36, pp = i % 36;
-    const uint8_t *ch = wbase + L.d_offset + (long long)(8 * ti.mt + j) * L.d_tile_bytes + (long long)c * L.d_chunk_bytes;
-    const bool half_chunk = L.d_half && c == L.d_chunks - 1;
-    if (pp < 32) return ch + h * 512 + 16 * pp;
-    return ch + (half_chunk ? L.cb / 2 : L.cb) + h * 64 + 16 * (pp - 32);
+    const bool half = L.d_half && c == L.d_chunks - 1;
+    bytes = half ? L.d_chunk_bytes / 2 : L.d_chunk_bytes;
+    return wbase + L.d_offset + (long long)(8 * ti.mt + j) * L.d_tile_bytes + (long long)c * L.d_chunk_bytes;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ UmmaArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], accf_bar[2], acce_bar[2];
+    __shared__ __align__(8) uint64_t fullA[kAStages], emptyA[kAStages], fullB[kBStages], emptyB[kBStages];
+    __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2];
+    __shared__ __align__(8) uint64_t pfull_bar[kPSlots], pempty_bar[kPSlots];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     __shared__ int epi_rows[kEpiWarps][kBN];  // down epilogue: output row of each column, per warp
+    __shared__ TileInfo tiles_s[kTileCache];  // this CTA's tiles (the first kTileCache of them)
     uint8_t *const sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x;
@@ -215,9 +260,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
     const int P = a.T * a.K;
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full_bar[s], kProdThreads);
-            mbar_init(&empty_bar[s], 1);
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(&fullA[s], a.mode == 2 ? 1 : kDqGroup);  // the TMA thread, or one dequant group
+            mbar_init(&emptyA[s], 1);
+        }
+        for (int s = 0; s < kBStages; ++s) {
+            mbar_init(&fullB[s], 1);  // the TMA thread (with bytes)
+            mbar_init(&emptyB[s], 1);
+        }
+        for (int s = 0; s < kPSlots; ++s) {
+            mbar_init(&pfull_bar[s], 1);
+            mbar_init(&pempty_bar[s], kDqThreads);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf_bar[b], 1);
@@ -225,6 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         }
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // this CTA's tiles t = blockIdx.x + G i: descriptors staged once (one round trip)
+    for (int i = tid; i < kTileCache; i += kThreads) {
+        const int t = blockIdx.x + G * i;
+        TileInfo ti;
+        if (t < n_tiles && tile_info(a, n_routed, t, ti)) tiles_s[i] = ti;
     }
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)),
@@ -236,6 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base;
+
+    auto get_tile = [&](int t, TileInfo &ti) -> bool {
+        const int i = (t - (int)blockIdx.x) / G;
+        if (i < kTileCache) {
+            ti = tiles_s[i];
+            return true;
+        }
+        return tile_info(a, n_routed, t, ti);
+    };
 
     // bounded wait on a barrier phase; on timeout every role of the CTA stops
     auto wait = [&](uint64_t *m, unsigned parity) -> bool {
@@ -252,161 +320,148 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         return true;
     };
 
-    if (warp < kProdWarps) {
-        // ---------------------------------------------------------------- producers
-        // Items are the (tile, stage) pairs of this CTA in order. Iteration `it` requests
-        // the packed weights of item it + kPLead and the B rows of item it + kBLead (one
-        // commit group each, empty groups past the end), then dequantises item it.
-        struct Cursor {
-            int t, s, nk;
-            TileInfo ti;
-            bool ok;
-        };
-        auto first = [&](Cursor &cu) {
-            cu.t = blockIdx.x;
-            cu.s = 0;
-            cu.ok = cu.t < n_tiles && tile_info(a, n_routed, cu.t, cu.ti);
-            cu.nk = cu.ok ? cu.ti.nk : 0;
-        };
-        auto next = [&](Cursor &cu) {
-            if (++cu.s < cu.nk) return;
-            cu.t += G;
-            cu.s = 0;
-            cu.ok = cu.t < n_tiles && tile_info(a, n_routed, cu.t, cu.ti);
-            cu.nk = cu.ok ? cu.ti.nk : 0;
-        };
-        auto wbase_of = [&](const TileInfo &ti) -> const uint8_t * {
-            return ti.shared ? a.src.shared : a.src.arena_base + (long long)ti.grp.slot * a.src.slot_stride;
-        };
-        Cursor cpk, cb, cd;
-        first(cpk);
-        first(cb);
-        first(cd);
-        int ip = 0, ib = 0;
-        const int pc = tid & 7;          // 16-byte piece of a 128-byte B row
-        int brow[kBN / 32];              // element offsets of this thread's B rows (-1: zero)
-        int brow_tile = -1;
-        const uint16_t *bsrc = a.mode == 0   ? reinterpret_cast<const uint16_t *>(a.x16)
-                               : a.mode == 1 ? reinterpret_cast<const uint16_t *>(a.h16)
-                                             : reinterpret_cast<const uint16_t *>(a.xb);
-        auto issue_packed = [&]() {
-            if (cpk.ok && a.mode != 2) {
-                uint8_t *pk = sm + kSmemP + (size_t)(ip % kPStages) * kPacked;
-                const uint8_t *wb = wbase_of(cpk.ti);
-                for (int i = tid; i < kPacked / 16; i += kProdThreads)
-                    cp16(pk + 16 * i, packed_src(a, cpk.ti, wb, cpk.s, i), true);
-                next(cpk);
+    auto wbase_of = [&](const TileInfo &ti) -> const uint8_t * {
+        return ti.shared ? a.src.shared : a.src.arena_base + (long long)ti.grp.slot * a.src.slot_stride;
+    };
+    if (warp == kTmaWarp || warp == kTmaBWarp) {
+        // ---------------------------------------------------------------- TMA warps
+        // warp kTmaWarp: the packed chunk of stages s, s + 1 of each tile (HBM, up to
+        // kPSlots chunks ahead); warp kTmaBWarp: the B rows of each stage (L2, up to
+        // kBStages ahead) and, for the router, the A rows.
+        if (lane == 0) {
+            const bool packed = warp == kTmaWarp;
+            if (!packed) {
+                asm volatile("prefetch.tensormap [%0];" ::"l"(&a.tmap_b) : "memory");
+                if (a.mode == 2) asm volatile("prefetch.tensormap [%0];" ::"l"(&a.tmap_a) : "memory");
             }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-            ++ip;
-        };
-        auto issue_b = [&]() -> bool {
-            if (cb.ok) {
-                const int b = ib % kStages;
-                if (ib >= kStages && !wait(&empty_bar[b], ((ib / kStages) - 1) & 1)) return false;
-                if (cb.t != brow_tile) {
-                    const TileInfo &ti = cb.ti;
-                    const QLayout &L = ti.shared ? a.src.LS : a.src.L;
-#pragma unroll
-                    for (int r = 0; r < kBN / 32; ++r) {
-                        const int n = (tid >> 3) + 32 * r;
-                        int off = -1;
-                        if (n < ti.grp.ncols)
-                            off = a.mode == 0   ? col_token(a.cols[ti.grp.col0 + n], a.K) * L.H
-                                  : a.mode == 1 ? (ti.grp.col0 + n) * a.h16_ld
-                                                : (ti.grp.col0 + n) * a.H;
-                        brow[r] = off;
-                    }
-                    brow_tile = cb.t;
-                }
-                uint8_t *sB = sm + kSmemB + (size_t)b * kBTile;
-#pragma unroll
-                for (int r = 0; r < kBN / 32; ++r) {
-                    const int n = (tid >> 3) + 32 * r;
-                    const int off = brow[r];
-                    cp16(sB + sw128(n, 8 * pc), bsrc + (off < 0 ? 0 : off) + cb.s * kBK + 8 * pc, off >= 0);
-                }
-                if (a.mode == 2) {
-                    // router rows 128 mt .. + 127 (A), copied as they are (bf16)
-                    uint8_t *sA = sm + kSmemA + (size_t)b * kATile;
-#pragma unroll
-                    for (int r = 0; r < kBM / 32; ++r) {
-                        const int n = (tid >> 3) + 32 * r, e = kBM * cb.ti.mt + n;
-                        const bool valid = e < a.E;
-                        cp16(sA + sw128(n, 8 * pc), a.wr + (size_t)(valid ? e : 0) * a.H + cb.s * kBK + 8 * pc, valid);
+            int it = 0, ch = 0;
+            bool good = !(packed && a.mode == 2);
+            for (int t = blockIdx.x; t < n_tiles && good; t += G) {
+                TileInfo ti;
+                if (!get_tile(t, ti)) break;
+                const uint8_t *wb = a.mode == 2 ? nullptr : wbase_of(ti);
+                for (int s2 = 0; s2 < ti.nk && good; ++s2, ++it) {
+                    if (packed) {
+                        if (s2 & 1) continue;
+                        const int ps = ch % kPSlots;
+                        if (ch >= kPSlots && !wait(&pempty_bar[ps], ((ch / kPSlots) - 1) & 1)) {
+                            good = false;
+                            break;
+                        }
+                        int bytes = 0, tot = 0;
+                        const int npieces = a.mode == 0 ? 4 : 8;
+                        const uint8_t *src[8];
+                        int nb[8];
+                        for (int j = 0; j < npieces; ++j) {
+                            src[j] = chunk_piece(a, ti, wb, s2 >> 1, j, bytes);
+                            nb[j] = bytes;
+                            tot += bytes;
+                        }
+                        mbar_expect_tx(&pfull_bar[ps], (unsigned)tot);
+                        uint8_t *dst = sm + kSmemP + (size_t)ps * kPacked;
+                        const int stride = a.mode == 0 ? 2304 : 1152;
+                        for (int j = 0; j < npieces; ++j) bulk_g2s(dst + j * stride, src[j], (unsigned)nb[j], &pfull_bar[ps]);
+                        ++ch;
+                    } else {
+                        const int bb = it % kBStages;
+                        if (it >= kBStages && !wait(&emptyB[bb], ((it / kBStages) - 1) & 1)) {
+                            good = false;
+                            break;
+                        }
+                        mbar_expect_tx(&fullB[bb], (unsigned)(kBoxRows * kBK * 2));
+                        tma_box(sm + kSmemB + (size_t)bb * kBTile, &a.tmap_b, s2 * kBK, ti.grp.col0, &fullB[bb]);
+                        if (a.mode == 2) {
+                            const int ba = it % kAStages;
+                            if (it >= kAStages && !wait(&emptyA[ba], ((it / kAStages) - 1) & 1)) {
+                                good = false;
+                                break;
+                            }
+                            mbar_expect_tx(&fullA[ba], (unsigned)(kABoxRows * kBK * 2));
+                            tma_box(sm + kSmemA + (size_t)ba * kATile, &a.tmap_a, s2 * kBK, kBM * ti.mt, &fullA[ba]);
+                        }
                     }
                 }
-                next(cb);
             }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-            ++ib;
-            return true;
-        };
+        }
+        __syncwarp();
+    } else if (warp < kDqWarps) {
+        // ---------------------------------------------------------------- dequant warps
+        // Stage s of a tile dequantises half s & 1 of chunk s / 2 into the A tile; item
+        // `it` belongs to group it % 2, and warp w of a group takes one 16-row slice
+        // (gate/up tile w / 2, gate if w is even; down tile w).
+        const int g = lane >> 2;
+        const int grp = warp >> 3, lw = warp & 7;
+        // stmatrix row addresses: lane l gives row l % 8 of matrix l / 8 (matrices:
+        // rows 0-7 / 8-15 x k 0-7 / 8-15 of a 16 x 16 k-step)
+        const int mrow = (lane & 7) + 8 * ((lane >> 3) & 1), mk = 8 * (lane >> 4);
+        int it = 0, ch = 0;
         bool good = true;
-        // prologue: the groups of iterations -kPLead .. -1
-        for (int j = -kPLead; j < 0 && good; ++j) {
-            issue_packed();
-            if (j + kBLead >= 0) good = issue_b();
-            else asm volatile("cp.async.commit_group;" ::: "memory");
-        }
-        for (int it = 0; cd.ok && good; ++it) {
-            issue_packed();
-            if (!issue_b()) break;
-            // B rows of item `it` were the second group of iteration it - kBLead (its
-            // packed weights are older): they have landed once at most the 2 * kBLead
-            // newer groups are pending; every producer thread reads packed bytes that
-            // others copied, so all of them wait
-            asm volatile("cp.async.wait_group %0;" ::"n"(2 * kBLead) : "memory");
-            asm volatile("bar.sync 1, %0;" ::"n"(kProdThreads) : "memory");
-            const int b = it % kStages;
-            if (a.mode == 2) {  // nothing to dequantise
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(&full_bar[b]);
-                next(cd);
-                continue;
-            }
-            const uint8_t *pk = sm + kSmemP + (size_t)(it % kPStages) * kPacked;
-            uint8_t *sA = sm + kSmemA + (size_t)b * kATile;
-            const int g = lane >> 2, c = lane & 3;
-            // warp w dequantises one 16-row slice: gate/up tile w/2 (gate if w even, up if
-            // odd), or down tile w
-            int row0, off_codes, off_scales;
-            if (a.mode == 0) {
-                const int j = warp >> 1, jm = warp & 1;
-                row0 = 32 * j + 16 * jm;
-                off_codes = j * 1152 + jm * 512;
-                off_scales = j * 1152 + 1024 + jm * 64;
-            } else {
-                row0 = 16 * warp;
-                off_codes = warp * 576;
-                off_scales = warp * 576 + 512;
-            }
-            const uint4 wv = *reinterpret_cast<const uint4 *>(pk + off_codes + 16 * lane);
-            const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-            // scales of rows g (low half) and g + 8 (high half) for the stage's two blocks
-            const uint32_t s0 = *reinterpret_cast<const uint32_t *>(pk + off_scales + 4 * g);
-            const uint32_t s1 = *reinterpret_cast<const uint32_t *>(pk + off_scales + 4 * (8 + g));
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t sw = i < 2 ? s0 : s1;  // block i / 2
-                const uint32_t d_lo = (sw & 0xFFFFu) * 0x10001u, d_hi = (sw >> 16) * 0x10001u;
-                uint32_t q[4];
-                q4_pairs(words[i], q);
-#pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    // nibble pair p: row g + 8 (p & 1), k = 16 i + 2 c + 8 (p >> 1) (+1)
-                    const int r = row0 + g + 8 * (p & 1);
-                    const int k = 16 * i + 2 * c + 8 * (p >> 1);
-                    *reinterpret_cast<uint32_t *>(sA + sw128(r, k)) = hmul2u(q[p], (p & 1) ? d_hi : d_lo);
+        for (int t = blockIdx.x; t < n_tiles && good; t += G) {
+            TileInfo ti;
+            if (!get_tile(t, ti)) break;
+            const QLayout &L = ti.shared ? a.src.LS : a.src.L;
+            if (a.mode == 2) break;  // the router has nothing to dequantise
+            for (int s2 = 0; s2 < ti.nk; ++s2, ++it) {
+                const int b = it % kAStages;
+                const int ps = ch % kPSlots;
+                const bool single = (s2 & 1) == 0 && s2 == ti.nk - 1;  // a chunk of one stage
+                const bool chunk_done = (s2 & 1) == 1 || s2 == ti.nk - 1;
+                if ((it & 1) != grp) {
+                    if (chunk_done) ++ch;
+                    continue;
                 }
+                if (!wait(&pfull_bar[ps], (ch / kPSlots) & 1)) {
+                    good = false;
+                    break;
+                }
+                // the A tile of this buffer is free once the MMA of item it - kAStages is done
+                if (it >= kAStages && !wait(&emptyA[b], ((it / kAStages) - 1) & 1)) {
+                    good = false;
+                    break;
+                }
+                if (a.mode != 2) {
+                    const uint8_t *pk = sm + kSmemP + (size_t)ps * kPacked;
+                    uint8_t *sA = sm + kSmemA + (size_t)b * kATile;
+                    const int h = s2 & 1;
+                    int row0, off_codes, off_scales;
+                    if (a.mode == 0) {
+                        const int j = lw >> 1, jm = lw & 1;
+                        row0 = 32 * j + 16 * jm;
+                        off_codes = j * 2304 + jm * 1024 + h * 512;
+                        off_scales = j * 2304 + 2048 + jm * 128 + h * 64;
+                    } else {
+                        const bool half = L.d_half && (s2 >> 1) == L.d_chunks - 1;
+                        row0 = 16 * lw;
+                        off_codes = lw * 1152 + h * 512;
+                        off_scales = lw * 1152 + (half ? 512 : 1024) + h * 64;
+                    }
+                    const uint4 wv = *reinterpret_cast<const uint4 *>(pk + off_codes + 16 * lane);
+                    const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+                    // scales of rows g (low half) and g + 8 (high half) for the stage's blocks
+                    const uint32_t s0 = *reinterpret_cast<const uint32_t *>(pk + off_scales + 4 * g);
+                    const uint32_t s1 = *reinterpret_cast<const uint32_t *>(pk + off_scales + 4 * (8 + g));
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t sw = i < 2 ? s0 : s1;  // block i / 2
+                        const uint32_t d_lo = (sw & 0xFFFFu) * 0x10001u, d_hi = (sw >> 16) * 0x10001u;
+                        uint32_t q[4];
+                        q4_pairs(words[i], q);
+                        // q[p] is fragment register p of k-step i: rows g (+8 for odd p),
+                        // k = 16 i + 2c (+8 for p >= 2)
+                        stmatrix4(sA + sw128(row0 + mrow, 16 * i + mk), hmul2u(q[0], d_lo), hmul2u(q[1], d_hi),
+                                  hmul2u(q[2], d_lo), hmul2u(q[3], d_hi));
+                    }
+                    // generic-proxy writes -> visible to the tensor cores' async proxy
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                mbar_arrive(&fullA[b]);
+                // this half of the chunk is no longer needed (a chunk of one stage counts for
+                // both halves)
+                mbar_arrive(&pempty_bar[ps]);
+                if (single) mbar_arrive(&pempty_bar[ps]);
+                if (chunk_done) ++ch;
             }
-            // the generic-proxy writes (dequantised A, cp.async B) become visible to the
-            // tensor cores' async proxy before the stage is marked full
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(&full_bar[b]);
-            next(cd);
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -416,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
             unsigned last_par = 0;
             for (int t = blockIdx.x; t < n_tiles && good; t += G, ++ti_local) {
                 TileInfo ti;
-                if (!tile_info(a, n_routed, t, ti)) break;
+                if (!get_tile(t, ti)) break;
                 const int ab = ti_local & 1;
                 if (ti_local >= 2 && !wait(&acce_bar[ab], ((ti_local >> 1) - 1) & 1)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -424,13 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                 const uint32_t idesc = idesc_f16(n, a.mode == 2);
                 const uint32_t dt = tmem + (uint32_t)(256 * ab);
                 for (int s = 0; s < ti.nk; ++s, ++it) {
-                    const int b = it % kStages;
-                    if (!wait(&full_bar[b], (it / kStages) & 1)) {
+                    const int ba = it % kAStages, b = it % kBStages;
+                    if (!wait(&fullB[b], (it / kBStages) & 1) || !wait(&fullA[ba], (it / kAStages) & 1)) {
                         good = false;
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const unsigned aa = su32(sm + kSmemA + (size_t)b * kATile);
+                    const unsigned aa = su32(sm + kSmemA + (size_t)ba * kATile);
                     const unsigned bb = su32(sm + kSmemB + (size_t)b * kBTile);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -443,10 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                             : "memory");
                     }
                     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                     su32(&empty_bar[b]))
+                                     su32(&emptyA[ba]))
+                                 : "memory");
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                     su32(&emptyB[b]))
                                  : "memory");
                     last_b = b;
-                    last_par = (unsigned)(it / kStages) & 1u;
+                    last_par = (unsigned)(it / kBStages) & 1u;
                 }
                 if (!good) break;
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -456,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
             // every MMA this thread issued has completed before TMEM can be released
             if (last_b >= 0) {
                 const long long t0 = clock64();
-                while (!mbar_try(&empty_bar[last_b], last_par) && clock64() - t0 < kSpin) {
+                while (!mbar_try(&emptyB[last_b], last_par) && clock64() - t0 < kSpin) {
                 }
             }
         }
@@ -467,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         int ti_local = 0;
         for (int t = blockIdx.x; t < n_tiles; t += G, ++ti_local) {
             TileInfo ti;
-            if (!tile_info(a, n_routed, t, ti)) break;
+            if (!get_tile(t, ti)) break;
             const int ab = ti_local & 1;
             if (!wait(&accf_bar[ab], (ti_local >> 1) & 1)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -555,13 +613,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
     }
 }
 
-// x (bf16 or fp32) -> fp16 rows
-__global__ void k_to_f16(const void *x, int xf32, size_t n, __half *out) {
-    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const float v = xf32 ? reinterpret_cast<const float *>(x)[i]
-                         : __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(x)[i]);
-    out[i] = __float2half_rn(v);
+// x (bf16 or fp32) -> fp16 rows in plan-column order: one thread per 8 elements
+__global__ void k_gather_f16(const int32_t *__restrict__ cols, const int32_t *__restrict__ n_cols,
+                             const void *__restrict__ x, int xf32, int K, int H, int max_rows, __half *__restrict__ out) {
+    const int per_row = H / 8;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const int row = (int)(i / per_row), v = (int)(i % per_row);
+    if (row >= max_rows || row >= *n_cols) return;
+    const int cv = cols[row];
+    const int t = cv >= 0 ? cv / K : -cv - 1;
+    float f[8];
+    if (xf32) {
+        const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + (size_t)t * H + 8 * v);
+        const float4 a0 = p[0], a1 = p[1];
+        f[0] = a0.x; f[1] = a0.y; f[2] = a0.z; f[3] = a0.w; f[4] = a1.x; f[5] = a1.y; f[6] = a1.z; f[7] = a1.w;
+    } else {
+        const uint4 w = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H + 8 * v);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f[2 * j] = __uint_as_float(ww[j] << 16);
+            f[2 * j + 1] = __uint_as_float(ww[j] & 0xFFFF0000u);
+        }
+    }
+    __align__(16) __half o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = __float2half_rn(f[j]);
+    *reinterpret_cast<uint4 *>(out + (size_t)row * H + 8 * v) = *reinterpret_cast<const uint4 *>(o);
 }
 
 }  // namespace
@@ -576,10 +654,39 @@ int launch_umma(const UmmaArgs &a, int n_ctas, cudaStream_t s) {
     return MOE_OK;
 }
 
-int launch_to_f16(const void *x, int xf32, size_t n, __half *out, cudaStream_t s) {
+int launch_gather_f16(const int32_t *cols, const int32_t *n_cols, const void *x, int xf32, int K, int H, int max_rows,
+                      __half *out, cudaStream_t s) {
+    const long long n = (long long)max_rows * (H / 8);
     if (n == 0) return MOE_OK;
-    k_to_f16<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(x, xf32, n, out);
+    k_gather_f16<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(cols, n_cols, x, xf32, K, H, max_rows, out);
     MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, unsigned long long rows, unsigned long long cols,
+                 unsigned long long row_stride_bytes, int box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if ((uintptr_t)base % 16 || row_stride_bytes % 16)
+        return set_error(MOE_ERR_ARG, "tensor map base / row stride not 16-byte aligned");
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    if (box_rows <= 0) box_rows = kBoxRows;
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return MOE_OK;
 }
 

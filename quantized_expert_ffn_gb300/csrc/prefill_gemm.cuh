@@ -1,6 +1,7 @@
 // prefill_gemm.cuh -- arguments of the tcgen05 grouped GEMMs for prefill windows.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the encoder is reached through the runtime's driver entry point)
 #include <cuda_fp16.h>
 
 #include "moe_internal.cuh"
@@ -14,6 +15,10 @@ namespace moe {
 // router GEMM (mode 2: logits = Wr x + bias, bf16 operands) over 128-expert by
 // 256-token tiles.
 struct UmmaArgs {
+    // 2-D tensor maps (128-byte swizzle): B rows (mode 0: x in plan
+    // order, fp16; mode 1: h; mode 2: x, bf16) and, for mode 2, the router rows
+    alignas(64) CUtensorMap tmap_b;
+    alignas(64) CUtensorMap tmap_a;
     int mode;
     // mode 2
     const __nv_bfloat16 *wr;  // [E][H]
@@ -28,7 +33,7 @@ struct UmmaArgs {
     const int32_t *cols;      // plan columns: pair p >= 0, shared token -(t + 1)
     int T, K, act;
     ExpertSrc src;
-    const __half *x16;        // gate/up B rows: [T][H] fp16
+    const __half *x16;        // gate/up B rows: x in plan-column order, [P + T][H] fp16
     __half *h16;              // [P + T][h16_ld] fp16, row = plan column
     int h16_ld;
     float *yp;                // [P + T][H] fp32: row p for pair p, P + t for the shared expert
@@ -40,7 +45,14 @@ bool umma_supported(const QLayout &L);
 // The router GEMM runs for bf16 x and Wr with H a multiple of 64.
 bool umma_router_supported(int H);
 int launch_umma(const UmmaArgs &a, int n_ctas, cudaStream_t s);
-int launch_to_f16(const void *x, int xf32, size_t n, __half *out, cudaStream_t s);
+// out[i] = fp16(x[token of plan column i]) for the n_cols (device count) columns
+int launch_gather_f16(const int32_t *cols, const int32_t *n_cols, const void *x, int xf32, int K, int H, int max_rows,
+                      __half *out, cudaStream_t s);
+// 2-D row-major tensor (rows x cols of 16-bit elements, row stride in bytes) as a
+// tensor map with boxes of 64 elements x box_rows rows (<= 0: the B box) and the
+// 128-byte swizzle; bf16 or fp16.
+int make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, unsigned long long rows, unsigned long long cols,
+                 unsigned long long row_stride_bytes, int box_rows = 0);
 int init_umma_attributes(int max_smem);
 size_t umma_smem_bytes();
 
