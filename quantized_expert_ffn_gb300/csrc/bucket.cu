@@ -121,40 +121,70 @@ __global__ void __launch_bounds__(kBucketThreads) k_plan(PlanArgs a) {
     int *cstart = lc + E;  // [E]
     int *scr = cstart + E; // [64]
     bool absent = false, oob = false;
-    int running = 0;
     for (int p = tid; p < P; p += blockDim.x) a.live[p] = 0;
+    if (tid < E) lc[tid] = 0;
     __syncthreads();
     const int nb = a.offsets[E];  // pairs with an id in range (the rest were left out)
-    for (int c0 = 0; c0 < nb; c0 += blockDim.x) {
-        const int i = c0 + tid;
-        int live = 0, p = -1;
-        if (i < nb) {
-            p = a.perm[i];
-            const int e = a.ids[p];
+    // thread `tid` owns bucket positions [i0, i1): one pass counts its live pairs (and
+    // each expert's, flushed per run of equal experts), one scan places them
+    const int per = (nb + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int i0 = min(nb, tid * per), i1 = min(nb, i0 + per);
+    int my_live = 0, run_e = -1, run_n = 0;
+    // batches of 8 positions: each level of the lookups (pair, expert, slot and
+    // weight) is issued for the whole batch before the next
+    constexpr int kB = 8;
+    for (int ib = i0; ib < i1; ib += kB) {
+        int pp[kB], ee[kB], sl[kB];
+        float ww[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) pp[j] = ib + j < i1 ? a.perm[ib + j] : -1;
+#pragma unroll
+        for (int j = 0; j < kB; ++j) ee[j] = pp[j] >= 0 ? a.ids[pp[j]] : -1;
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const bool in = pp[j] >= 0 && ee[j] >= 0 && ee[j] < E;
+            sl[j] = in ? a.table[(size_t)a.layer * E + ee[j]] : -1;
+            ww[j] = in ? a.w[pp[j]] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            if (pp[j] < 0) break;
+            const int p = pp[j], e = ee[j];
+            int live = 0;
             if (e >= 0 && e < E) {
-                const int slot = a.table[(size_t)a.layer * E + e];
-                if (slot < 0) absent = true;
-                else if (slot >= a.capacity) oob = true;
-                else live = a.w[p] != 0.f;
+                if (sl[j] < 0) absent = true;
+                else if (sl[j] >= a.capacity) oob = true;
+                else live = ww[j] != 0.f;
             } else {
                 oob = true;
             }
             a.live[p] = live;
+            my_live += live;
+            if (e != run_e) {
+                if (run_n && run_e >= 0 && run_e < E) atomicAdd(&lc[run_e], run_n);
+                run_e = e;
+                run_n = 0;
+            }
+            run_n += live;
         }
-        int tot;
-        const int pos = block_exclusive_scan(live, &tot, scr);
-        if (live) a.cols[running + pos] = p;
-        running += tot;
     }
-    const int nlive = running;
+    if (run_n && run_e >= 0 && run_e < E) atomicAdd(&lc[run_e], run_n);
+    int nlive;
+    int pos = block_exclusive_scan(my_live, &nlive, scr);
+    for (int ib = i0; ib < i1; ib += kB) {
+        int pp[kB], lv[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) pp[j] = ib + j < i1 ? a.perm[ib + j] : -1;
+#pragma unroll
+        for (int j = 0; j < kB; ++j) lv[j] = pp[j] >= 0 ? a.live[pp[j]] : 0;
+#pragma unroll
+        for (int j = 0; j < kB; ++j)
+            if (lv[j]) a.cols[pos++] = pp[j];
+    }
     if (__syncthreads_or(absent) && tid == 0) set_status(a.status, MOE_STATUS_EXPERT_ABSENT);
     if (__syncthreads_or(oob) && tid == 0) set_status(a.status, MOE_STATUS_BOUNDS);
     // live count per expert (its pairs are offsets[e]..offsets[e+1] of perm)
-    int my_lc = 0;
-    if (tid < E) {
-        for (int i = a.offsets[tid]; i < a.offsets[tid + 1]; ++i) my_lc += a.live[a.perm[i]];
-        lc[tid] = my_lc;
-    }
+    const int my_lc = tid < E ? lc[tid] : 0;
     int dummy;
     const int my_cs = block_exclusive_scan(tid < E ? my_lc : 0, &dummy, scr);
     if (tid < E) cstart[tid] = my_cs;

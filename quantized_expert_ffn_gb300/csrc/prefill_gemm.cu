@@ -117,6 +117,15 @@ __device__ __forceinline__ void tma_box(void *dst, const CUtensorMap *map, int c
         "l"(map), "r"(c0), "r"(c1), "r"(su32(m))
         : "memory");
 }
+// One box of a 3-D tensor map at (c0, c1, c2).
+__device__ __forceinline__ void tma_box3(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *m) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(su32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(su32(m))
+        : "memory");
+}
+
 // Four 8x8 matrices of 16-bit elements, one register of each per lane in the
 // mma fragment layout; lane l gives the address of row l % 8 of matrix l / 8.
 __device__ __forceinline__ void stmatrix4(void *row_addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
@@ -226,23 +235,6 @@ __device__ __forceinline__ bool tile_info(const UmmaArgs &a, int n_routed, int t
     return true;
 }
 
-// The packed image of 128-k chunk c of tile ti (slot layout): gate/up: 4 row tiles
-// x their whole chunk [gate codes 1024 | up codes 1024 | gate scales 128 | up scales
-// 128] at 2,304-byte strides; down: 8 row tiles x [codes 1024 | scales 128] at
-// 1,152-byte strides (a last half chunk [codes 512 | scales 64]). Piece j: source
-// and bytes.
-__device__ __forceinline__ const uint8_t *chunk_piece(const UmmaArgs &a, const TileInfo &ti, const uint8_t *wbase,
-                                                      int c, int j, int &bytes) {
-    const QLayout &L = ti.shared ? a.src.LS : a.src.L;
-    if (a.mode == 0) {
-        bytes = L.gu_chunk_bytes;
-        return wbase + (long long)(4 * ti.mt + j) * L.gu_tile_bytes + (long long)c * L.gu_chunk_bytes;
-    }
-    const bool half = L.d_half && c == L.d_chunks - 1;
-    bytes = half ? L.d_chunk_bytes / 2 : L.d_chunk_bytes;
-    return wbase + L.d_offset + (long long)(8 * ti.mt + j) * L.d_tile_bytes + (long long)c * L.d_chunk_bytes;
-}
-
 __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ UmmaArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t fullA[kAStages], emptyA[kAStages], fullB[kBStages], emptyB[kBStages];
@@ -320,9 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         return true;
     };
 
-    auto wbase_of = [&](const TileInfo &ti) -> const uint8_t * {
-        return ti.shared ? a.src.shared : a.src.arena_base + (long long)ti.grp.slot * a.src.slot_stride;
-    };
     if (warp == kTmaWarp || warp == kTmaBWarp) {
         // ---------------------------------------------------------------- TMA warps
         // warp kTmaWarp: the packed chunk of stages s, s + 1 of each tile (HBM, up to
@@ -339,7 +328,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
             for (int t = blockIdx.x; t < n_tiles && good; t += G) {
                 TileInfo ti;
                 if (!get_tile(t, ti)) break;
-                const uint8_t *wb = a.mode == 2 ? nullptr : wbase_of(ti);
                 for (int s2 = 0; s2 < ti.nk && good; ++s2, ++it) {
                     if (packed) {
                         if (s2 & 1) continue;
@@ -348,19 +336,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                             good = false;
                             break;
                         }
-                        int bytes = 0, tot = 0;
-                        const int npieces = a.mode == 0 ? 4 : 8;
-                        const uint8_t *src[8];
-                        int nb[8];
-                        for (int j = 0; j < npieces; ++j) {
-                            src[j] = chunk_piece(a, ti, wb, s2 >> 1, j, bytes);
-                            nb[j] = bytes;
-                            tot += bytes;
-                        }
-                        mbar_expect_tx(&pfull_bar[ps], (unsigned)tot);
+                        // one chunk of the 128-row M-tile: gate/up codes + scales boxes, or
+                        // one down box (a half box for a last half chunk)
+                        const QLayout &L = ti.shared ? a.src.LS : a.src.L;
+                        const CUtensorMap *pk = ti.shared ? &a.pk[2] : &a.pk[0];
+                        const int slot = ti.shared ? 0 : ti.grp.slot;
+                        const int c = s2 >> 1;
                         uint8_t *dst = sm + kSmemP + (size_t)ps * kPacked;
-                        const int stride = a.mode == 0 ? 2304 : 1152;
-                        for (int j = 0; j < npieces; ++j) bulk_g2s(dst + j * stride, src[j], (unsigned)nb[j], &pfull_bar[ps]);
+                        if (a.mode == 0) {
+                            mbar_expect_tx(&pfull_bar[ps], 4u * 2304u);
+                            tma_box3(dst, &pk[0], c * 288, 4 * ti.mt, slot, &pfull_bar[ps]);
+                            tma_box3(dst + 8192, &pk[1], c * 288 + 256, 4 * ti.mt, slot, &pfull_bar[ps]);
+                        } else {
+                            const bool half = L.d_half && c == L.d_chunks - 1;
+                            mbar_expect_tx(&pfull_bar[ps], half ? 8u * 576u : 8u * 1152u);
+                            tma_box3(dst, &pk[half ? 1 : 0], c * 144, 8 * ti.mt, slot, &pfull_bar[ps]);
+                        }
                         ++ch;
                     } else {
                         const int bb = it % kBStages;
@@ -425,15 +416,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                     const int h = s2 & 1;
                     int row0, off_codes, off_scales;
                     if (a.mode == 0) {
+                        // slot: 4 x [gate codes 1024 | up codes 1024], then 4 x [gate scales
+                        // 128 | up scales 128]
                         const int j = lw >> 1, jm = lw & 1;
                         row0 = 32 * j + 16 * jm;
-                        off_codes = j * 2304 + jm * 1024 + h * 512;
-                        off_scales = j * 2304 + 2048 + jm * 128 + h * 64;
+                        off_codes = j * 2048 + jm * 1024 + h * 512;
+                        off_scales = 8192 + j * 256 + jm * 128 + h * 64;
                     } else {
+                        // slot: 8 x [codes 1024 | scales 128] (a half chunk: 8 x [512 | 64])
                         const bool half = L.d_half && (s2 >> 1) == L.d_chunks - 1;
                         row0 = 16 * lw;
-                        off_codes = lw * 1152 + h * 512;
-                        off_scales = lw * 1152 + (half ? 512 : 1024) + h * 64;
+                        off_codes = lw * (half ? 576 : 1152) + h * 512;
+                        off_scales = lw * (half ? 576 : 1152) + (half ? 512 : 1024) + h * 64;
                     }
                     const uint4 wv = *reinterpret_cast<const uint4 *>(pk + off_codes + 16 * lane);
                     const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -687,6 +681,44 @@ int make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, unsigned long lo
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return MOE_OK;
+}
+
+int make_packed_maps(CUtensorMap maps[2], int mode, const QLayout &L, const uint8_t *base, long long slot_stride,
+                     int n_slots) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    const uint8_t *b0 = mode == 0 ? base : base + L.d_offset;
+    const long long tile_bytes = mode == 0 ? L.gu_tile_bytes : L.d_tile_bytes;
+    const int tiles = mode == 0 ? L.gu_tiles : L.d_tiles;
+    if ((uintptr_t)b0 % 16 || tile_bytes % 16 || slot_stride % 16)
+        return set_error(MOE_ERR_ARG, "packed weights not 16-byte aligned");
+    const cuuint64_t dims[3] = {(cuuint64_t)(tile_bytes / 8), (cuuint64_t)tiles, (cuuint64_t)(n_slots > 0 ? n_slots : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)tile_bytes, (cuuint64_t)(slot_stride > 0 ? slot_stride : tile_bytes * tiles)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    for (int m = 0; m < 2; ++m) {
+        cuuint32_t box[3];
+        if (mode == 0) {
+            box[0] = m == 0 ? 256 : 32;  // 2,048 bytes of codes, 256 bytes of scales
+            box[1] = 4;
+        } else {
+            box[0] = m == 0 ? 144 : 72;  // a whole chunk, a half chunk
+            box[1] = 8;
+        }
+        box[2] = 1;
+        const CUresult r = encode(&maps[m], CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t *>(b0), dims,
+                                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (packed) failed (%d)", (int)r);
+    }
     return MOE_OK;
 }
 

@@ -19,6 +19,11 @@ struct UmmaArgs {
     // order, fp16; mode 1: h; mode 2: x, bf16) and, for mode 2, the router rows
     alignas(64) CUtensorMap tmap_b;
     alignas(64) CUtensorMap tmap_a;
+    // packed weights as 3-D byte tensors [slot][row tile][bytes] (8-byte elements):
+    // pk[0] / pk[1] routed experts, pk[2] / pk[3] the shared expert. Gate/up: [0|2]
+    // boxes of the codes of a chunk (2,048 bytes x 4 row tiles), [1|3] its scales
+    // (256 x 4); down: [0|2] a whole chunk (1,152 x 8), [1|3] a last half chunk (576 x 8).
+    alignas(64) CUtensorMap pk[4];
     int mode;
     // mode 2
     const __nv_bfloat16 *wr;  // [E][H]
@@ -53,6 +58,9 @@ int launch_gather_f16(const int32_t *cols, const int32_t *n_cols, const void *x,
 // 128-byte swizzle; bf16 or fp16.
 int make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, unsigned long long rows, unsigned long long cols,
                  unsigned long long row_stride_bytes, int box_rows = 0);
+// The packed-weight maps of one layout (routed arena or shared expert) for `mode`.
+int make_packed_maps(CUtensorMap maps[2], int mode, const QLayout &L, const uint8_t *base, long long slot_stride,
+                     int n_slots);
 int init_umma_attributes(int max_smem);
 size_t umma_smem_bytes();
 
