@@ -352,9 +352,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
     // chunks per piece: two pieces of each kind fit in the ring at once
-    const int pcg = a.geom.ring_bytes / (2 * L.gu_chunk_bytes) < 2 ? 1 : 2;
+    // chunks per piece: two pieces of each kind fit in the ring at once; larger pieces
+    // mean fewer bulk copies (the copy engine takes them one at a time)
+    const int pcg_fit = a.geom.ring_bytes / (2 * L.gu_chunk_bytes);
+    const int pcg = pcg_fit < 1 ? 1 : (pcg_fit > 8 ? 8 : pcg_fit);
     const int pcd_fit = a.geom.ring_bytes / (2 * L.d_chunk_bytes);
-    const int pcd = pcd_fit < 1 ? 1 : (pcd_fit > 4 ? 4 : pcd_fit);
+    const int pcd = pcd_fit < 1 ? 1 : (pcd_fit > 8 ? 8 : pcd_fit);
 
     prefetch_router(a, 0, wr_s, tab_s, s.bias[0]);
     for (int l = 0; l < a.n_layers; ++l) {
@@ -438,12 +441,11 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                 a.logits[(size_t)t * E + e] = v;
                 if (a.trace_logits) a.trace_logits[((size_t)l * T + t) * E + e] = v;
             }
-            // the router rows are free: request the next layer's (HBM is idle until
-            // the expert weights are known)
-            if (l + 1 < a.n_layers)
-                prefetch_router(a, l + 1, wr_s, tab_s + ((l + 1) & 1) * tab_ld, s.bias[(l + 1) & 1]);
         }
         if (!grid_sync(a.bar, target, a.status, s_flag)) break;
+        // the router rows are free: request the next layer's while top-K runs (HBM is
+        // idle until the expert weights are known)
+        if (l + 1 < a.n_layers) prefetch_router(a, l + 1, wr_s, tab_s + ((l + 1) & 1) * tab_ld, s.bias[(l + 1) & 1]);
         // ------------------------------------------------ T: top-K and the plan (every CTA)
         {
             uint32_t *segmax = reinterpret_cast<uint32_t *>(u_region);  // [kMaxTok][kMaxSeg]
@@ -855,11 +857,14 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                 }
                 const Unpack &un = shared ? a.un_s : a.un;
                 // B tiles: columns nb*4 + (g & 3); lanes g < 4 read hi limbs, g >= 4 lo limbs
-                auto make_bt = [&](int nb) {
+                // staged: B rows in shared memory (the pointer provably shared, so the
+                // loads are shared-memory loads); otherwise h limbs in global memory
+                auto make_bt = [&](int nb, auto staged_tag) {
+                    constexpr bool STAGED = decltype(staged_tag)::value;
                     const int jc = nb * 4 + (g & 3);
-                    BTile b{a.h_hi, false};
+                    BTile b{STAGED ? hst : a.h_hi, false};
                     if (jc < ncols) {
-                        if (staged) {
+                        if constexpr (STAGED) {
                             b.row = shared ? hss + (g < 4 ? 0 : lo_off_s) + jc * ldhs + 2 * c
                                            : hst + (g < 4 ? 0 : lo_off) + (col0 + jc - c_lo) * ldh + 2 * c;
                         } else {
@@ -886,11 +891,11 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                     }
                 };
                 const int nchk = LL.d_chunks;
-                auto run = [&](auto nb_tag) {
+                auto run = [&](auto nb_tag, auto staged_tag) {
                     constexpr int NB = decltype(nb_tag)::value;
                     BTile bt[NB];
 #pragma unroll
-                    for (int nb = 0; nb < NB; ++nb) bt[nb] = make_bt(nb);
+                    for (int nb = 0; nb < NB; ++nb) bt[nb] = make_bt(nb, staged_tag);
                     float acc[1][NB][4] = {};
                     const uint8_t *pbase = nullptr;
                     int pnc = 0, pbytes = 0;
@@ -915,20 +920,31 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
 #pragma unroll
                     for (int nb = 0; nb < NB; ++nb) emit(nb, acc[0][nb]);
                 };
-                if (ncols > 4)
-                    run(std::integral_constant<int, 2>{});
-                else
-                    run(std::integral_constant<int, 1>{});
-                // the last unit of row tile r to arrive combines the experts in k order
+                if (staged) {
+                    if (ncols > 4)
+                        run(std::integral_constant<int, 2>{}, std::true_type{});
+                    else
+                        run(std::integral_constant<int, 1>{}, std::true_type{});
+                } else {
+                    if (ncols > 4)
+                        run(std::integral_constant<int, 2>{}, std::false_type{});
+                    else
+                        run(std::integral_constant<int, 1>{}, std::false_type{});
+                }
+                // the last unit of row tile r to arrive combines the experts in k order; the
+                // warp's y_pair stores are ordered before lane 0's release, and the combining
+                // warp reads the others' after lane 0's acquire
                 __syncwarp();
                 int ticket = 0;
                 if (lane == 0) {
-                    __threadfence();
-                    ticket = atomicAdd(&a.d_cnt[r], 1);
+                    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                                 : "=r"(ticket)
+                                 : "l"(a.d_cnt + r)
+                                 : "memory");
                 }
                 ticket = __shfl_sync(0xffffffffu, ticket, 0);
                 if (ticket == n_tasks - 1) {
-                    __threadfence();
+                    __syncwarp();
                     for (int o = lane; o < T * 16; o += 32) {
                         const int t = o >> 4, rr = o & 15;
                         const size_t col = (size_t)r * 16 + rr, oo = (size_t)t * H + col;
