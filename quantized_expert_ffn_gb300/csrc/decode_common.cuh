@@ -340,6 +340,18 @@ __device__ __forceinline__ float topk_weight(float sel_v, int K, int lane) {
     return ex / s;
 }
 
+// topk_weight with the same arithmetic (m = the first chosen logit, the sum in k
+// order), the exponentials exchanged through this warp's 32-float shared-memory
+// scratch instead of warp shuffles
+__device__ __forceinline__ float topk_weight_smem(float sel_v, float m, int K, int lane, float *scratch) {
+    const float ex = lane < K ? expf(sel_v - m) : 0.f;
+    scratch[lane] = ex;
+    __syncwarp();
+    float s = 0.f;
+    for (int k = 0; k < K; ++k) s += scratch[k];
+    return ex / s;
+}
+
 // ---------------------------------------------------------------- rmsnorm
 
 // RMSNorm with the canonical 512-lane order: thread i (0..511) accumulates x_h^2

@@ -63,7 +63,9 @@ struct alignas(16) Plan {
     float rpart[16][kMaxTok][4];          // router partial sums [row][token][warp]
     float wsum[kMaxTok][kNormWarps];      // RMSNorm warp sums
     unsigned long long sel[kMaxTok][32];  // chosen keys per token, rank order
+    float wex[kMaxTok][32];               // softmax exponentials per token
     uint64_t ring_bar[kPersistThreads / 32][8];  // weight-ring mbarriers per warp
+    uint64_t rbar;                               // router-row copies
 };
 
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned *p) {
@@ -264,27 +266,32 @@ __device__ __forceinline__ void load_chunk_s(const uint8_t *cp, const uint8_t *s
 }
 
 // Request the router rows this CTA owns for layer l, their bias and the layer's
-// slot-table row into shared memory (one commit group).
-__device__ void prefetch_router(const PersistArgs &a, int l, uint8_t *wr_s, int32_t *tab_s, float *bias_s) {
-    const int G = gridDim.x, c = blockIdx.x;
+// slot-table row into shared memory; called by one warp. The rows (H * wsz bytes
+// each, contiguous in global memory) and the table row go by bulk copies that
+// complete on `m` (one phase per call), the few bias words by cp.async (one
+// commit group per lane).
+__device__ void prefetch_router(const PersistArgs &a, int l, uint8_t *wr_s, int32_t *tab_s, float *bias_s,
+                                uint64_t *m) {
+    const int G = gridDim.x, c = blockIdx.x, lane = threadIdx.x & 31;
     const int wsz = a.wr_bf16 ? 2 : 4;
     const int row_bytes = a.H * wsz;
     const uint8_t *Wr = reinterpret_cast<const uint8_t *>(a.layers[l].Wr);
     const int nr = (a.E - c + G - 1) / G;
-    const int per_row = row_bytes / 16;
-    for (int i = threadIdx.x; i < nr * per_row; i += blockDim.x) {
-        const int r = i / per_row, o = (i % per_row) * 16;
-        const int e = c + r * G;
-        cp_async16(wr_s + (size_t)r * row_bytes + o, Wr + (size_t)e * row_bytes + o);
-    }
-    if (a.layers[l].bias)
-        for (int r = threadIdx.x; r < nr; r += blockDim.x) cp_async4(bias_s + r, a.layers[l].bias + c + r * G);
     const int32_t *tab = a.layers[l].table + (size_t)a.layers[l].layer * a.E;
-    if (((uintptr_t)tab & 15) == 0 && (a.E & 3) == 0) {
-        for (int i = threadIdx.x; i < a.E / 4; i += blockDim.x) cp_async16(tab_s + 4 * i, tab + 4 * i);
-    } else {
-        for (int i = threadIdx.x; i < a.E; i += blockDim.x) cp_async4(tab_s + i, tab + i);
+    const bool tab_bulk = ((uintptr_t)tab & 15) == 0 && (a.E & 3) == 0;
+    if (lane == 0) {
+        // the CTA's earlier reads of these bytes (ordered before by a CTA barrier)
+        // come before the copies' writes
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(m, (unsigned)(nr * row_bytes + (tab_bulk ? a.E * 4 : 0)));
+        for (int r = 0; r < nr; ++r)
+            bulk_g2s(wr_s + (size_t)r * row_bytes, Wr + (size_t)(c + r * G) * row_bytes, (unsigned)row_bytes, m);
+        if (tab_bulk) bulk_g2s(tab_s, tab, (unsigned)(a.E * 4), m);
     }
+    if (!tab_bulk)
+        for (int i = lane; i < a.E; i += 32) cp_async4(tab_s + i, tab + i);
+    if (a.layers[l].bias)
+        for (int r = lane; r < nr; r += 32) cp_async4(bias_s + r, a.layers[l].bias + c + r * G);
     cp_async_commit();
 }
 
@@ -349,9 +356,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
     ring.R = a.geom.ring_bytes;
     ring.head = ring.tail = ring.issued = ring.consumed = ring.front = 0;
     if (lane < kRingBars) mbar_init(&s.ring_bar[warp][lane], 1);
+    if (tid == 0) mbar_init(&s.rbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
-    // chunks per piece: two pieces of each kind fit in the ring at once
     // chunks per piece: two pieces of each kind fit in the ring at once; larger pieces
     // mean fewer bulk copies (the copy engine takes them one at a time)
     const int pcg_fit = a.geom.ring_bytes / (2 * L.gu_chunk_bytes);
@@ -359,14 +366,15 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
     const int pcd_fit = a.geom.ring_bytes / (2 * L.d_chunk_bytes);
     const int pcd = pcd_fit < 1 ? 1 : (pcd_fit > 8 ? 8 : pcd_fit);
 
-    prefetch_router(a, 0, wr_s, tab_s, s.bias[0]);
+    if (warp == 0) prefetch_router(a, 0, wr_s, tab_s, s.bias[0], &s.rbar);
+    int r_issued = 1, r_done = 0;  // router prefetches issued / waited for
     for (int l = 0; l < a.n_layers; ++l) {
         const PersistLayer &Ly = a.layers[l];
         const int32_t *const tab = tab_s + (l & 1) * tab_ld;
         if (tid < kMaxTok) {
             s.misc[4 + tid] = 0;
             s.ncand[tid] = 0;
-            s.theta[tid] = 0;
+            s.theta[tid] = 0xFFFFFFFFu;
         }
         // ------------------------------------------------ N: layer input
         if (a.stack) {
@@ -408,7 +416,13 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                 *reinterpret_cast<uint4 *>(xs + (size_t)t * ldx + h8) = x[idx];
             }
         }
-        cp_async_wait_all();  // this layer's router rows, bias and table row
+        // this layer's router rows, bias and table row
+        cp_async_wait_all();
+        if (!mbar_wait(&s.rbar, (unsigned)l & 1u) && tid == 0) {
+            set_status(a.status, MOE_STATUS_TIMEOUT);
+            atomicExch(a.bar + 1, 1u);
+        }
+        r_done = l + 1;
         __syncthreads();
         // ------------------------------------------------ R: router logits of my experts
         {
@@ -443,120 +457,119 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
             }
         }
         if (!grid_sync(a.bar, target, a.status, s_flag)) break;
-        // the router rows are free: request the next layer's while top-K runs (HBM is
-        // idle until the expert weights are known)
-        if (l + 1 < a.n_layers) prefetch_router(a, l + 1, wr_s, tab_s + ((l + 1) & 1) * tab_ld, s.bias[(l + 1) & 1]);
         // ------------------------------------------------ T: top-K and the plan (every CTA)
         {
-            uint32_t *segmax = reinterpret_cast<uint32_t *>(u_region);  // [kMaxTok][kMaxSeg]
-            unsigned long long *cand =
-                reinterpret_cast<unsigned long long *>(u_region + kMaxTok * kMaxSeg * sizeof(uint32_t));
-            // expert e sits in thread e (and e - 512); segments of `seg` threads
-            const int nact = E < kPersistThreads ? E : kPersistThreads;
-            int seg = 1;
-            while (seg < 32 && (nact + 2 * seg - 1) / (2 * seg) >= 2 * K) seg *= 2;
-            while (seg < 32 && (nact + seg - 1) / seg > kMaxSeg) seg *= 2;
-            const int nseg = (nact + seg - 1) / seg;
+            // ord keys of the logits; token rows are padded to Ep (a multiple of 32)
+            // with "no candidate" entries, so a warp's 32 entries and every segment
+            // belong to one token
+            const int Ep = (E + 31) & ~31, TE = T * Ep;
+            uint32_t *const ords = reinterpret_cast<uint32_t *>(u_region);  // [T][Ep]
+            uint32_t *const segmax = ords + TE;                              // [kMaxTok][kMaxSeg]
+            unsigned long long *const cand =
+                reinterpret_cast<unsigned long long *>(segmax + kMaxTok * kMaxSeg);  // [kMaxTok][kCandCap]
+            // segments of `seg` entries, at least 2K of them per token where kMaxSeg allows
+            int lseg = 5;
+            while (lseg > 0 && (Ep >> lseg) < 2 * K && (Ep >> (lseg - 1)) <= kMaxSeg) --lseg;
+            const int seg = 1 << lseg, nseg = Ep >> lseg;
             const bool all_cand = E <= kCandCap;  // no threshold: every expert is a candidate
-            const bool in1 = tid < E, in2 = tid + kPersistThreads < E;
-            float v1[kMaxTok], v2[kMaxTok];
-#pragma unroll
-            for (int t = 0; t < kMaxTok; ++t) {
-                v1[t] = (t < T && in1) ? __ldcg(a.logits + (size_t)t * E + tid) : 0.f;
-                v2[t] = (t < T && in2) ? __ldcg(a.logits + (size_t)t * E + tid + kPersistThreads) : 0.f;
-            }
-            uint32_t o1[kMaxTok], o2[kMaxTok];
-#pragma unroll
-            for (int t = 0; t < kMaxTok; ++t) {
-                o1[t] = in1 ? topk_ord(v1[t]) : 0u;
-                o2[t] = in2 ? topk_ord(v2[t]) : 0u;
-                if (t < T) {
-                    const bool bad = (in1 && !isfinite(v1[t])) || (in2 && !isfinite(v2[t]));
-                    if (__any_sync(0xffffffffu, bad) && lane == 0) s.misc[4 + t] = 1;
-                    if (!all_cand) {
-                        uint32_t m = o1[t] > o2[t] ? o1[t] : o2[t];
-                        for (int d = 1; d < seg; d <<= 1) {
-                            const uint32_t o = __shfl_xor_sync(0xffffffffu, m, d);
-                            m = o > m ? o : m;
-                        }
-                        if ((tid & (seg - 1)) == 0 && tid < nact) segmax[t * kMaxSeg + tid / seg] = m;
-                    }
-                }
-            }
-            __syncthreads();
-            // threshold: the K-th largest segment maximum (at least K experts reach
-            // it, so every top-K expert does); left at 0 if there are fewer than K
-            if (!all_cand) {
-                const int t = tid / kMaxSeg, j = tid % kMaxSeg;
-                if (t < T && j < nseg) {
-                    const uint32_t *sm = segmax + t * kMaxSeg;
-                    const uint32_t mv = sm[j];
-                    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-#pragma unroll 4
-                    for (int j4 = 0; j4 < nseg; j4 += 4) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(sm + j4);
-                        r0 += (j4 < nseg) & ((v.x > mv) | ((v.x == mv) & (j4 < j)));
-                        r1 += (j4 + 1 < nseg) & ((v.y > mv) | ((v.y == mv) & (j4 + 1 < j)));
-                        r2 += (j4 + 2 < nseg) & ((v.z > mv) | ((v.z == mv) & (j4 + 2 < j)));
-                        r3 += (j4 + 3 < nseg) & ((v.w > mv) | ((v.w == mv) & (j4 + 3 < j)));
-                    }
-                    if ((r0 + r1) + (r2 + r3) == K - 1) s.theta[t] = mv;
-                }
-            }
-            __syncthreads();
             const unsigned lt = (1u << lane) - 1u;
+            // (1) keys and segment maxima (the loop bound is uniform in each warp)
+            const float inv_ep = __frcp_rn((float)Ep);  // token of flat index i: (int)((i + 0.5) / Ep), exact here
+            auto tok = [&](int i) { return (int)(((float)i + 0.5f) * inv_ep); };
+            for (int b0 = 0; b0 < TE; b0 += 4 * kPersistThreads) {
+                float v[4];
 #pragma unroll
-            for (int t = 0; t < kMaxTok; ++t) {
-                if (t < T) {
-                    const uint32_t th = s.theta[t];
-                    const bool c1 = in1 && o1[t] >= th, c2 = in2 && o2[t] >= th;
-                    const unsigned b1 = __ballot_sync(0xffffffffu, c1), b2 = __ballot_sync(0xffffffffu, c2);
-                    const int n = __popc(b1) + __popc(b2);
-                    int base = 0;
-                    if (lane == 0 && n) base = atomicAdd(&s.ncand[t], n);
-                    base = __shfl_sync(0xffffffffu, base, 0);
-                    if (c1) {
-                        const int pos = base + __popc(b1 & lt);
-                        if (pos < kCandCap) cand[t * kCandCap + pos] = topk_key_of(o1[t], tid);
-                    }
-                    if (c2) {
-                        const int pos = base + __popc(b1) + __popc(b2 & lt);
-                        if (pos < kCandCap) cand[t * kCandCap + pos] = topk_key_of(o2[t], tid + kPersistThreads);
+                for (int u = 0; u < 4; ++u) {
+                    const int idx = b0 + u * kPersistThreads + tid, t = tok(idx), e = idx - t * Ep;
+                    v[u] = (idx < TE && e < E) ? __ldcg(a.logits + (size_t)t * E + e) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int idx = b0 + u * kPersistThreads + tid, t = tok(idx), e = idx - t * Ep;
+                    if (idx - lane < TE) {
+                        const bool valid = e < E;
+                        const uint32_t o = valid ? topk_ord(v[u]) : 0u;
+                        if (valid && !isfinite(v[u])) s.misc[4 + t] = 1;
+                        ords[idx] = o;
+                        if (!all_cand) {
+                            uint32_t m;
+                            if (seg == 32) {
+                                m = __reduce_max_sync(0xffffffffu, o);
+                            } else {
+                                m = o;
+                                for (int d = 1; d < seg; d <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, d));
+                            }
+                            if ((lane & (seg - 1)) == 0) segmax[t * kMaxSeg + (e >> lseg)] = m;
+                        }
                     }
                 }
             }
             __syncthreads();
-            bool overflow = false;
-            for (int t = 0; t < T; ++t) overflow |= s.ncand[t] > kCandCap;
-            if (!overflow) {
-                // rank of each candidate among its token's candidates = its place in the top-K
-                for (int idx = tid; idx < T * kCandCap; idx += kPersistThreads) {
-                    const int t = idx / kCandCap, ci = idx % kCandCap;
+            // (2) threshold of each token: the K-th largest segment maximum, counted
+            // with multiplicity = the smallest maximum that fewer than K maxima
+            // exceed. Each maximum is a distinct entry, so at least K entries reach
+            // it and every top-K entry does. A warp ranks one maximum against all
+            // (shared-memory broadcasts and a ballot: warp shuffles are slow here).
+            if (!all_cand) {
+                for (int t = 0; t < T; ++t) {
+                    const uint32_t *sm = segmax + t * kMaxSeg;
+                    for (int i = warp; i < nseg; i += kPWarps) {
+                        const uint32_t mi = sm[i];
+                        int rank = 0;
+                        for (int j = lane; j - lane < nseg; j += 32)
+                            rank += __popc(__ballot_sync(0xffffffffu, j < nseg && sm[j] > mi));
+                        if (lane == 0 && rank < K) atomicMin(&s.theta[t], mi);
+                    }
+                }
+            }
+            __syncthreads();
+            // (3) candidates: the entries at or above the threshold
+            for (int b0 = 0; b0 < TE; b0 += kPersistThreads) {
+                if (b0 + warp * 32 >= TE) break;
+                const int idx = b0 + tid, t = tok(idx), e = idx - t * Ep;
+                const uint32_t o = ords[idx];
+                const bool c = e < E && o >= (all_cand ? 0u : s.theta[t]);
+                const unsigned bal = __ballot_sync(0xffffffffu, c);
+                int base = 0;
+                if (lane == 0 && bal) base = atomicAdd(&s.ncand[t], __popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                if (c) {
+                    const int pos = base + __popc(bal & lt);
+                    if (pos < kCandCap) cand[t * kCandCap + pos] = topk_key_of(o, e);
+                }
+            }
+            __syncthreads();
+            // (4) rank of each candidate among its token's candidates = its place in
+            // the top-K (keys are distinct); s.sel[t][k] = the k-th key. A warp ranks
+            // one candidate against all (broadcast + ballot).
+            int maxn = 0;
+            for (int t = 0; t < T; ++t) maxn = max(maxn, s.ncand[t]);
+            if (maxn <= kCandCap) {
+                for (int t = 0; t < T; ++t) {
                     const int n = s.ncand[t];
-                    if (ci < n) {
-                        const unsigned long long *ct = cand + t * kCandCap;
-                        const unsigned long long key = ct[ci];
-                        int r0 = 0, r1 = 0;
-#pragma unroll 4
-                        for (int i2 = 0; i2 < n; i2 += 2) {
-                            const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(ct + i2);
-                            r0 += v.x > key;
-                            r1 += (i2 + 1 < n) & (v.y > key);
-                        }
-                        if (r0 + r1 < K) s.sel[t][r0 + r1] = key;
+                    const unsigned long long *ct = cand + t * kCandCap;
+                    for (int i = warp; i < n; i += kPWarps) {
+                        const unsigned long long ki = ct[i];
+                        int rank = 0;
+                        for (int j = lane; j - lane < n; j += 32)
+                            rank += __popc(__ballot_sync(0xffffffffu, j < n && ct[j] > ki));
+                        if (lane == 0 && rank < K) s.sel[t][rank] = ki;
                     }
                 }
             } else {
+                // too many candidates (e.g. many equal logits)
                 topk_sort_merge(a.logits, T, E, reinterpret_cast<unsigned long long *>(u_region), s.sel);
             }
             __syncthreads();
+            // (5) weights of token t (warp t)
             if (warp < T) {
                 const int t = warp;
                 const unsigned long long key = s.sel[t][lane];
                 const int si = topk_key_index(key);
                 const float sv = topk_key_value(key);
                 const bool bad = s.misc[4 + t] != 0;
-                const float wk = bad ? __int_as_float(0x7fc00000) : topk_weight(sv, K, lane);
+                const float m = topk_key_value(s.sel[t][0]);
+                const float wk = bad ? __int_as_float(0x7fc00000) : topk_weight_smem(sv, m, K, lane, s.wex[t]);
                 if (lane < K) {
                     s.ids[t * K + lane] = si;
                     s.w[t * K + lane] = wk;
@@ -564,22 +577,37 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                 }
                 if (bad && lane == 0 && cta == 0) set_status(a.status, MOE_STATUS_NONFINITE);
             }
-            __syncthreads();
-            // stable order of pairs by expert: rank = #{q : (id_q, q) < (id_p, p)}
-            if (tid < P) {
-                const int ep = s.ids[tid];
-                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-#pragma unroll 2
-                for (int q4 = 0; q4 < P; q4 += 4) {
-                    const int4 v = *reinterpret_cast<const int4 *>(s.ids + q4);
-                    r0 += (q4 < P) & ((v.x < ep) | ((v.x == ep) & (q4 < tid)));
-                    r1 += (q4 + 1 < P) & ((v.y < ep) | ((v.y == ep) & (q4 + 1 < tid)));
-                    r2 += (q4 + 2 < P) & ((v.z < ep) | ((v.z == ep) & (q4 + 2 < tid)));
-                    r3 += (q4 + 3 < P) & ((v.w < ep) | ((v.w == ep) & (q4 + 3 < tid)));
+            // (6) stable order of pairs by expert: rank = #{q : (id_q, q) < (id_p, p)}
+            if (T == 1 && P <= 32) {
+                // one token: its pairs are warp 0's lanes
+                if (warp == 0) {
+                    __syncwarp();
+                    const int ep = lane < P ? s.ids[lane] : 0x7FFFFFFF;
+                    int r = 0;
+                    for (int q = 0; q < P; ++q) {
+                        const int eq = s.ids[q];
+                        r += (eq < ep) | ((eq == ep) & (q < lane));
+                    }
+                    if (lane < P) s.sorted[r] = lane;
+                    __syncwarp();
                 }
-                s.sorted[(r0 + r1) + (r2 + r3)] = tid;
+            } else {
+                __syncthreads();
+                if (tid < P) {
+                    const int ep = s.ids[tid];
+                    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+#pragma unroll 2
+                    for (int q4 = 0; q4 < P; q4 += 4) {
+                        const int4 v4 = *reinterpret_cast<const int4 *>(s.ids + q4);
+                        r0 += (q4 < P) & ((v4.x < ep) | ((v4.x == ep) & (q4 < tid)));
+                        r1 += (q4 + 1 < P) & ((v4.y < ep) | ((v4.y == ep) & (q4 + 1 < tid)));
+                        r2 += (q4 + 2 < P) & ((v4.z < ep) | ((v4.z == ep) & (q4 + 2 < tid)));
+                        r3 += (q4 + 3 < P) & ((v4.w < ep) | ((v4.w == ep) & (q4 + 3 < tid)));
+                    }
+                    s.sorted[(r0 + r1) + (r2 + r3)] = tid;
+                }
+                __syncthreads();
             }
-            __syncthreads();
             if (warp == 0) {
                 int running = 0;
                 bool absent = false, oob = false;
@@ -632,22 +660,25 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                     // down units (expert-major: unit j = expert j / dt, row tile j % dt)
                     // split over the CTAs by down bytes: CTA c takes the units whose
                     // byte midpoint falls in [c D / G, (c + 1) D / G)
+                    // (single-precision arithmetic: CTA c and CTA c + 1 evaluate the same
+                    // boundary with the same operations, so the ranges tile [0, n_units))
                     const bool sh = Ly.shared != nullptr;
-                    const long long nr_units = (long long)nu * dt;
-                    const int n_units = (int)nr_units + (sh ? dt : 0);
-                    const long long dr = L.d_tile_bytes, dsb = sh ? a.LS.d_tile_bytes : 0;
-                    const long long Dr = nr_units * dr, Dtot = Dr + (long long)dt * dsb;
-                    auto first_unit = [&](long long b) -> int {
-                        if (b <= 0) return 0;
-                        const long long x = b - dr / 2;  // routed: j*dr + dr/2 >= b
-                        const long long j = x <= 0 ? 0 : (x + dr - 1) / dr;
-                        if (j < nr_units || dsb == 0) return (int)(j < nr_units ? j : nr_units);
-                        const long long y = b - Dr - dsb / 2;  // shared: Dr + k*dsb + dsb/2 >= b
-                        const long long jj = nr_units + (y <= 0 ? 0 : (y + dsb - 1) / dsb);
-                        return (int)(jj < n_units ? jj : n_units);
+                    const int nr_units = nu * dt;
+                    const int n_units = nr_units + (sh ? dt : 0);
+                    const float dr = (float)L.d_tile_bytes, dsb = sh ? (float)a.LS.d_tile_bytes : 0.f;
+                    const float Dr = (float)nr_units * dr, Dtot = Dr + (float)dt * dsb;
+                    auto first_unit = [&](int c) -> int {
+                        if (c <= 0) return 0;
+                        const float b = __fdividef(Dtot * (float)c, (float)G);
+                        const float x = b - 0.5f * dr;  // routed: j*dr + dr/2 >= b
+                        const int j = x <= 0.f ? 0 : (int)ceilf(__fdividef(x, dr));
+                        if (j < nr_units || !sh) return j < nr_units ? j : nr_units;
+                        const float y = b - Dr - 0.5f * dsb;  // shared: Dr + k*dsb + dsb/2 >= b
+                        const int jj = nr_units + (y <= 0.f ? 0 : (int)ceilf(__fdividef(y, dsb)));
+                        return jj < n_units ? jj : n_units;
                     };
-                    s.misc[12] = first_unit(Dtot * cta / G);
-                    s.misc[13] = cta == G - 1 ? n_units : first_unit(Dtot * (cta + 1) / G);
+                    s.misc[12] = first_unit(cta);
+                    s.misc[13] = cta == G - 1 ? n_units : first_unit(cta + 1);
                 }
             }
             __syncthreads();
@@ -842,6 +873,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                 }
             }
             __syncthreads();
+            // the next layer's router rows (their buffer is free since barrier 1); warp 0
+            // gets the last down units, so it has the most slack here
+            if (warp == 0 && l + 1 < a.n_layers) {
+                prefetch_router(a, l + 1, wr_s, tab_s + ((l + 1) & 1) * tab_ld, s.bias[(l + 1) & 1], &s.rbar);
+                r_issued = l + 2;
+            }
             for (int di = 0;; ++di) {
                 const int j = j0 + dw + kPWarps * di;
                 if (j >= j1) break;
@@ -974,6 +1011,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
         }
     }
     ring_drain(ring);
+    // a router prefetch still in flight (the loop stopped early)
+    if (r_issued > r_done) mbar_wait(&s.rbar, (unsigned)(r_issued - 1) & 1u);
     cp_async_wait_all();
 }
 
@@ -999,7 +1038,8 @@ PersistGeom persist_geom(int kind, int T, int H, int E, int K, int F, int F_shar
     g.hst_bytes = al(xs_bytes) + kRedBytes;  // h staging reuses xs + red
     g.off_ring = g.off_xs + g.hst_bytes;
     g.off_u = g.off_ring;
-    const size_t topk_fast = (size_t)kMaxTok * kMaxSeg * 4 + (size_t)T * kCandCap * 8;
+    const size_t topk_fast =
+        (size_t)T * ((E + 31) & ~31) * 4 + (size_t)kMaxTok * kMaxSeg * 4 + (size_t)T * kCandCap * 8;
     const size_t topk_sort = (size_t)T * ((E + 31) / 32) * 32 * 8;
     const size_t norm = (size_t)T * H * 4;
     size_t u = topk_fast > topk_sort ? topk_fast : topk_sort;
