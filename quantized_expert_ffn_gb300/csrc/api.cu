@@ -88,7 +88,7 @@ int check_dims(int H, int F) {
 // Workspace carving for one layer call of up to T tokens.
 struct WsLayout {
     size_t logits, ids, w, counts, offsets, perm, active, n_active, live, cols, groups_gu, groups_d, n_groups, h, yp,
-        u, x16, bar, total;
+        u, x16, bar, wide, total;
     int sync_words;  // persistent path: barrier words + down tile counters
     int max_routed_gu, max_routed_d, max_shared, h_ld;
 };
@@ -124,6 +124,7 @@ WsLayout ws_layout(const moe_layer_desc *d, int T, int nc_gu) {
     W.x16 = take((P + T) * (size_t)d->H * 2);  // x in plan-column order (tensor-core path)
     W.sync_words = 4 + d->H / 16;
     W.bar = take((size_t)W.sync_words * 4);
+    W.wide = take(use_wide(T, d->K) ? wide_scratch_bytes(T, d->K, d->E) : 0);  // multi-CTA sort and plan
     W.total = o;
     return W;
 }
@@ -222,7 +223,7 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
     pa.groups_d = (Group *)(ws + W.groups_d);
     pa.n_groups = (int32_t *)(ws + W.n_groups);
     pa.status = ctx->d_status;
-    int rc = launch_plan(pa, s);
+    int rc = use_wide(T, d->K) ? launch_plan_wide(pa, (int32_t *)(ws + W.wide), s) : launch_plan(pa, s);
     if (rc) return rc;
 
     ExpertArgs ea;
@@ -421,9 +422,14 @@ int layer_core(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype x
     if (rc) return rc;
     rc = launch_topk(logits, T, d->E, d->K, ids, w, ctx->d_status, s);
     if (rc) return rc;
-    rc = launch_bucket(ids, T, d->K, d->E, (int32_t *)(ws + W.counts), (int32_t *)(ws + W.offsets),
-                       (int32_t *)(ws + W.perm), (int32_t *)(ws + W.active), (int32_t *)(ws + W.n_active),
-                       ctx->d_status, s);
+    if (use_wide(T, d->K))
+        rc = launch_bucket_wide(ids, T, d->K, d->E, (int32_t *)(ws + W.counts), (int32_t *)(ws + W.offsets),
+                                (int32_t *)(ws + W.perm), (int32_t *)(ws + W.active), (int32_t *)(ws + W.n_active),
+                                (int32_t *)(ws + W.wide), ctx->d_status, s);
+    else
+        rc = launch_bucket(ids, T, d->K, d->E, (int32_t *)(ws + W.counts), (int32_t *)(ws + W.offsets),
+                           (int32_t *)(ws + W.perm), (int32_t *)(ws + W.active), (int32_t *)(ws + W.n_active),
+                           ctx->d_status, s);
     if (rc) return rc;
     return run_experts(ctx, d, x, xt, T, ids, w, (int32_t *)(ws + W.offsets), (int32_t *)(ws + W.perm), y,
                        accumulate, ws, W, s);

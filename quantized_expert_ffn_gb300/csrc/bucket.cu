@@ -217,6 +217,184 @@ __global__ void __launch_bounds__(kBucketThreads) k_plan(PlanArgs a) {
     }
 }
 
+// ---------------------------------------------------------------- wide windows
+// The same stable counting sort and plan spread over one CTA per 1,024 pairs (or
+// bucket positions): a single CTA is bound by its own share of the L2 bandwidth
+// once the window holds tens of thousands of pairs. Outputs are identical to
+// k_bucket / k_plan.
+
+// Per-chunk expert histogram: cc[c][e] = pairs of chunk c with id e.
+__global__ void __launch_bounds__(kBucketThreads) k_bucket_count(const int32_t *__restrict__ ids, int P, int E,
+                                                                 int32_t *cc, uint32_t *status) {
+    extern __shared__ int sm[];
+    const int tid = threadIdx.x, c = blockIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) sm[e] = 0;
+    __syncthreads();
+    const int p = c * kBucketThreads + tid;
+    bool oob = false;
+    if (p < P) {
+        const int e = ids[p];
+        if (e >= 0 && e < E) atomicAdd(&sm[e], 1);
+        else oob = true;
+    }
+    if (__syncthreads_or(oob) && tid == 0) set_status(status, MOE_STATUS_BOUNDS);
+    for (int e = tid; e < E; e += blockDim.x) cc[(size_t)c * E + e] = sm[e];
+}
+
+// Totals, offsets and active experts; cc[c][e] becomes the number of expert-e
+// pairs in chunks before c.
+__global__ void __launch_bounds__(kBucketThreads) k_bucket_scan(int C, int E, int32_t *cc, int32_t *counts,
+                                                                int32_t *offsets, int32_t *active,
+                                                                int32_t *n_active) {
+    __shared__ int scr[64];
+    const int tid = threadIdx.x;
+    int run = 0;
+    if (tid < E) {
+        // batches of 8 chunks: the loads of a batch are in flight together
+        for (int c0 = 0; c0 < C; c0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = c0 + j < C ? cc[(size_t)(c0 + j) * E + tid] : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (c0 + j < C) cc[(size_t)(c0 + j) * E + tid] = run;
+                run += v[j];
+            }
+        }
+    }
+    int total;
+    const int pre = block_exclusive_scan(tid < E ? run : 0, &total, scr);
+    if (tid < E) {
+        counts[tid] = run;
+        offsets[tid] = pre;
+    }
+    if (tid == 0) offsets[E] = total;
+    const int act = (tid < E && run > 0) ? 1 : 0;
+    int nact;
+    const int apos = block_exclusive_scan(act, &nact, scr);
+    if (act) active[apos] = tid;
+    if (tid == 0) *n_active = nact;
+}
+
+// Stable placement of chunk c (the in-chunk rank as in k_bucket).
+__global__ void __launch_bounds__(kBucketThreads) k_bucket_place(const int32_t *__restrict__ ids, int P, int E,
+                                                                 const int32_t *cc, const int32_t *offsets,
+                                                                 int32_t *perm) {
+    extern __shared__ int sm[];
+    int *base = sm;       // [E]
+    int *wt = base + E;   // [32][E]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, c = blockIdx.x;
+    for (int e = tid; e < E; e += blockDim.x) base[e] = offsets[e] + cc[(size_t)c * E + e];
+    for (int i = tid; i < 32 * E; i += blockDim.x) wt[i] = 0;
+    __syncthreads();
+    const int p = c * kBucketThreads + tid;
+    int e = p < P ? ids[p] : -1;
+    if (e >= E) e = -1;
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & ((1u << lane) - 1));
+    if (e >= 0 && rank == 0) wt[warp * E + e] = __popc(same);
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += blockDim.x) {
+        int run = base[ee];
+        for (int w = 0; w < 32; ++w) {
+            const int n = wt[w * E + ee];
+            wt[w * E + ee] = run;
+            run += n;
+        }
+    }
+    __syncthreads();
+    if (e >= 0) perm[wt[warp * E + e] + rank] = p;
+}
+
+// Plan, pass 1 (one CTA per 1,024 bucket positions): liveness of the pair at
+// each position, live pairs per expert (lc) and per CTA (blk); pairs whose id is
+// out of range (not in the buckets) are marked dead by their own index.
+__global__ void __launch_bounds__(kBucketThreads) k_plan_live(PlanArgs a, int32_t *lc, int32_t *blk) {
+    const int tid = threadIdx.x, i = blockIdx.x * kBucketThreads + tid;
+    const int P = a.T * a.K, E = a.E;
+    const int nb = a.offsets[E];
+    bool absent = false, oob = false;
+    int live = 0, e = -1;
+    if (i < nb) {
+        const int p = a.perm[i];
+        e = a.ids[p];
+        const int slot = a.table[(size_t)a.layer * E + e];
+        if (slot < 0) absent = true;
+        else if (slot >= a.capacity) oob = true;
+        else live = a.w[p] != 0.f;
+        a.live[p] = live;
+    }
+    if (i < P) {
+        const int ei = a.ids[i];
+        if (ei < 0 || ei >= E) {
+            a.live[i] = 0;
+            oob = true;
+        }
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, live ? e : -1);
+    if (live && (same & ((1u << (tid & 31)) - 1)) == 0) atomicAdd(&lc[e], __popc(same));
+    const int n = __syncthreads_count(live);
+    if (tid == 0) blk[blockIdx.x] = n;
+    if (__syncthreads_or(absent) && tid == 0) set_status(a.status, MOE_STATUS_EXPERT_ABSENT);
+    if (__syncthreads_or(oob) && tid == 0) set_status(a.status, MOE_STATUS_BOUNDS);
+}
+
+// Plan, pass 2 (one CTA): column bases of the position blocks and of the
+// experts, the groups, the group counts and the shared expert's columns/groups.
+__global__ void __launch_bounds__(kBucketThreads) k_plan_groups(PlanArgs a, int nblk, const int32_t *lc,
+                                                                int32_t *blk) {
+    __shared__ int scr[64];
+    const int tid = threadIdx.x, E = a.E;
+    int nlive;
+    const int bl = tid < nblk ? blk[tid] : 0;
+    const int bb = block_exclusive_scan(bl, &nlive, scr);
+    if (tid < nblk) blk[tid] = bb;
+    const int my_lc = tid < E ? lc[tid] : 0;
+    int dummy;
+    const int my_cs = block_exclusive_scan(my_lc, &dummy, scr);
+    const int ng_gu = tid < E ? (my_lc + a.nc_gu - 1) / a.nc_gu : 0;
+    const int ng_d = tid < E ? (my_lc + a.nc_d - 1) / a.nc_d : 0;
+    int tot_gu, tot_d;
+    const int gb_gu = block_exclusive_scan(ng_gu, &tot_gu, scr);
+    const int gb_d = block_exclusive_scan(ng_d, &tot_d, scr);
+    if (tid < E && my_lc > 0) {
+        const int slot = a.table[(size_t)a.layer * E + tid];
+        for (int j = 0; j < ng_gu; ++j)
+            a.groups_gu[gb_gu + j] = Group{slot, my_cs + j * a.nc_gu, min(a.nc_gu, my_lc - j * a.nc_gu), 0};
+        for (int j = 0; j < ng_d; ++j)
+            a.groups_d[gb_d + j] = Group{slot, my_cs + j * a.nc_d, min(a.nc_d, my_lc - j * a.nc_d), 0};
+    }
+    if (tid == 0) {
+        a.n_groups[0] = tot_gu;
+        a.n_groups[1] = tot_d;
+        a.n_groups[2] = nlive + (a.has_shared ? a.T : 0);
+    }
+    if (a.has_shared) {
+        for (int t = tid; t < a.T; t += blockDim.x) a.cols[nlive + t] = -(t + 1);
+        const int sg_gu = (a.T + a.nc_gu - 1) / a.nc_gu, sg_d = (a.T + a.nc_d - 1) / a.nc_d;
+        for (int j = tid; j < sg_gu; j += blockDim.x)
+            a.groups_gu[a.max_routed_gu + j] = Group{-2, nlive + j * a.nc_gu, min(a.nc_gu, a.T - j * a.nc_gu), 0};
+        for (int j = tid; j < sg_d; j += blockDim.x)
+            a.groups_d[a.max_routed_d + j] = Group{-2, nlive + j * a.nc_d, min(a.nc_d, a.T - j * a.nc_d), 0};
+    }
+}
+
+// Plan, pass 3 (one CTA per 1,024 bucket positions): the live pairs in bucket
+// order are the routed plan columns.
+__global__ void __launch_bounds__(kBucketThreads) k_plan_cols(PlanArgs a, const int32_t *blk) {
+    __shared__ int scr[64];
+    const int tid = threadIdx.x, i = blockIdx.x * kBucketThreads + tid;
+    const int nb = a.offsets[a.E];
+    int p = -1, live = 0;
+    if (i < nb) {
+        p = a.perm[i];
+        live = a.live[p];
+    }
+    int dummy;
+    const int pre = block_exclusive_scan(live, &dummy, scr);
+    if (live) a.cols[blk[blockIdx.x] + pre] = p;
+}
+
 }  // namespace
 
 int launch_bucket(const int32_t *ids, int T, int K, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
@@ -230,7 +408,44 @@ int launch_bucket(const int32_t *ids, int T, int K, int E, int32_t *counts, int3
 int init_bucket_attributes(int max_smem) {
     int rc = set_max_dynamic_smem((const void *)k_bucket, max_smem);
     if (!rc) rc = set_max_dynamic_smem((const void *)k_plan, max_smem);
+    if (!rc) rc = set_max_dynamic_smem((const void *)k_bucket_place, max_smem);
     return rc;
+}
+
+size_t wide_scratch_bytes(int T, int K, int E) {
+    const size_t C = ((size_t)T * K + kBucketThreads - 1) / kBucketThreads;
+    const size_t a = C * (size_t)E, b = (size_t)E + 2 * C;
+    return (a > b ? a : b) * sizeof(int32_t);
+}
+
+bool use_wide(int T, int K) {
+    const long long P = (long long)T * K;
+    return P > 2 * kBucketThreads && P <= (long long)kBucketThreads * kBucketThreads;
+}
+
+int launch_bucket_wide(const int32_t *ids, int T, int K, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
+                       int32_t *active, int32_t *n_active, int32_t *scratch, uint32_t *status, cudaStream_t s) {
+    const int P = T * K, C = (P + kBucketThreads - 1) / kBucketThreads;
+    k_bucket_count<<<C, kBucketThreads, (size_t)E * sizeof(int), s>>>(ids, P, E, scratch, status);
+    MOE_CUDA_TRY(cudaGetLastError());
+    k_bucket_scan<<<1, kBucketThreads, 0, s>>>(C, E, scratch, counts, offsets, active, n_active);
+    MOE_CUDA_TRY(cudaGetLastError());
+    k_bucket_place<<<C, kBucketThreads, (size_t)33 * E * sizeof(int), s>>>(ids, P, E, scratch, offsets, perm);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int launch_plan_wide(const PlanArgs &a, int32_t *scratch, cudaStream_t s) {
+    const int P = a.T * a.K, C = (P + kBucketThreads - 1) / kBucketThreads;
+    int32_t *lc = scratch, *blk = scratch + a.E;
+    MOE_CUDA_TRY(cudaMemsetAsync(lc, 0, (size_t)a.E * sizeof(int32_t), s));
+    k_plan_live<<<C, kBucketThreads, 0, s>>>(a, lc, blk);
+    MOE_CUDA_TRY(cudaGetLastError());
+    k_plan_groups<<<1, kBucketThreads, 0, s>>>(a, C, lc, blk);
+    MOE_CUDA_TRY(cudaGetLastError());
+    k_plan_cols<<<C, kBucketThreads, 0, s>>>(a, blk);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
 }
 
 int launch_plan(const PlanArgs &a, cudaStream_t s) {

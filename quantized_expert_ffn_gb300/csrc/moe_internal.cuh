@@ -283,6 +283,13 @@ int launch_topk(const float *logits, int T, int E, int K, int32_t *ids, float *w
 int launch_bucket(const int32_t *ids, int T, int K, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
                   int32_t *active, int32_t *n_active, uint32_t *status, cudaStream_t s);
 int launch_plan(const PlanArgs &a, cudaStream_t s);
+// Windows of more than 2,048 pairs (up to 1,024 x 1,024): the same sort and plan
+// over one CTA per 1,024 pairs; `scratch` holds wide_scratch_bytes(T, K, E).
+bool use_wide(int T, int K);
+size_t wide_scratch_bytes(int T, int K, int E);
+int launch_bucket_wide(const int32_t *ids, int T, int K, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
+                       int32_t *active, int32_t *n_active, int32_t *scratch, uint32_t *status, cudaStream_t s);
+int launch_plan_wide(const PlanArgs &a, int32_t *scratch, cudaStream_t s);
 int launch_gateup(const ExpertArgs &a, moe_dtype xt, cudaStream_t s);
 int launch_down(const ExpertArgs &a, cudaStream_t s);
 int launch_combine(const float *yp, const float *w, const int32_t *live, int T, int K, int H, int has_shared,

@@ -200,6 +200,22 @@ def test_t_invariance_bitwise(q2, gemma):
             assert torch_equal(i1[0], i4[t])
 
 
+@pytest.mark.parametrize("name,T,W", [("q2", 256, 64), ("gemma", 512, 64)])
+def test_wide_window_sort_and_plan_bitwise(q2, gemma, name, T, W):
+    # windows of more than 2,048 pairs are sorted and planned by the multi-CTA
+    # kernels, windows of W tokens by the single-CTA ones; both windows take the
+    # same router and expert kernels (T, W >= 64), so every token's ids and
+    # output must be the same bits
+    import torch
+    g = q2 if name == "q2" else gemma
+    assert T * g.cfg.K > 2048 >= W * g.cfg.K
+    x = to_dev(_x(g.cfg, T, step=31))
+    y, _, ids = g.forward(x)
+    parts = [g.forward(x[s:s + W].contiguous()) for s in range(0, T, W)]
+    assert torch.equal(torch.cat([p[2] for p in parts]), ids)
+    assert torch.equal(torch.cat([p[0] for p in parts]), y)
+
+
 def torch_equal(a, b):
     import torch
     return bool(torch.equal(a, b))
