@@ -607,33 +607,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
     }
 }
 
-// x (bf16 or fp32) -> fp16 rows in plan-column order: one thread per 8 elements
-__global__ void k_gather_f16(const int32_t *__restrict__ cols, const int32_t *__restrict__ n_cols,
-                             const void *__restrict__ x, int xf32, int K, int H, int max_rows, __half *__restrict__ out) {
-    const int per_row = H / 8;
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const int row = (int)(i / per_row), v = (int)(i % per_row);
-    if (row >= max_rows || row >= *n_cols) return;
+// x (bf16 or fp32) -> fp16 rows in plan-column order: one CTA per row, 8
+// elements per thread and step
+__global__ void __launch_bounds__(128) k_gather_f16(const int32_t *__restrict__ cols, const int32_t *__restrict__ n_cols,
+                                                    const void *__restrict__ x, int xf32, int K, int H,
+                                                    __half *__restrict__ out) {
+    const int row = blockIdx.x;
+    if (row >= *n_cols) return;
     const int cv = cols[row];
     const int t = cv >= 0 ? cv / K : -cv - 1;
-    float f[8];
-    if (xf32) {
-        const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + (size_t)t * H + 8 * v);
-        const float4 a0 = p[0], a1 = p[1];
-        f[0] = a0.x; f[1] = a0.y; f[2] = a0.z; f[3] = a0.w; f[4] = a1.x; f[5] = a1.y; f[6] = a1.z; f[7] = a1.w;
-    } else {
-        const uint4 w = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H + 8 * v);
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    for (int v = threadIdx.x; v < H / 8; v += blockDim.x) {
+        float f[8];
+        if (xf32) {
+            const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + (size_t)t * H + 8 * v);
+            const float4 a0 = p[0], a1 = p[1];
+            f[0] = a0.x; f[1] = a0.y; f[2] = a0.z; f[3] = a0.w; f[4] = a1.x; f[5] = a1.y; f[6] = a1.z; f[7] = a1.w;
+        } else {
+            const uint4 w = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H + 8 * v);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f[2 * j] = __uint_as_float(ww[j] << 16);
-            f[2 * j + 1] = __uint_as_float(ww[j] & 0xFFFF0000u);
+            for (int j = 0; j < 4; ++j) {
+                f[2 * j] = __uint_as_float(ww[j] << 16);
+                f[2 * j + 1] = __uint_as_float(ww[j] & 0xFFFF0000u);
+            }
         }
-    }
-    __align__(16) __half o[8];
+        __align__(16) __half o[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) o[j] = __float2half_rn(f[j]);
-    *reinterpret_cast<uint4 *>(out + (size_t)row * H + 8 * v) = *reinterpret_cast<const uint4 *>(o);
+        for (int j = 0; j < 8; ++j) o[j] = __float2half_rn(f[j]);
+        __stcs(reinterpret_cast<uint4 *>(out + (size_t)row * H + 8 * v), *reinterpret_cast<const uint4 *>(o));
+    }
 }
 
 }  // namespace
@@ -650,9 +652,8 @@ int launch_umma(const UmmaArgs &a, int n_ctas, cudaStream_t s) {
 
 int launch_gather_f16(const int32_t *cols, const int32_t *n_cols, const void *x, int xf32, int K, int H, int max_rows,
                       __half *out, cudaStream_t s) {
-    const long long n = (long long)max_rows * (H / 8);
-    if (n == 0) return MOE_OK;
-    k_gather_f16<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(cols, n_cols, x, xf32, K, H, max_rows, out);
+    if (max_rows == 0) return MOE_OK;
+    k_gather_f16<<<(unsigned)max_rows, 128, 0, s>>>(cols, n_cols, x, xf32, K, H, out);
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }
