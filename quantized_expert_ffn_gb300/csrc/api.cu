@@ -279,6 +279,9 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
         ua.status = ctx->d_status;
         rc = make_tmap_2d(&ua.tmap_b, x16, false, (unsigned long long)maxc, (unsigned long long)d->H,
                           (unsigned long long)d->H * 2);
+        for (int i = 0; i < 4 && !rc; ++i)
+            rc = make_tmap_2d(&ua.tmap_bn[i], x16, false, (unsigned long long)maxc, (unsigned long long)d->H,
+                              (unsigned long long)d->H * 2, 16 << i);
         if (!rc) rc = make_packed_maps(&ua.pk[0], 0, sl->layout, sl->base, (long long)sl->stride, sl->capacity);
         if (!rc && d->shared) rc = make_packed_maps(&ua.pk[2], 0, d->shared->layout, ea.src.shared, 0, 1);
         if (rc) return rc;
@@ -286,6 +289,9 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
         if (rc) return rc;
         rc = make_tmap_2d(&ua.tmap_b, ua.h16, false, (unsigned long long)maxc, (unsigned long long)W.h_ld,
                           (unsigned long long)W.h_ld * 2);
+        for (int i = 0; i < 4 && !rc; ++i)
+            rc = make_tmap_2d(&ua.tmap_bn[i], ua.h16, false, (unsigned long long)maxc, (unsigned long long)W.h_ld,
+                              (unsigned long long)W.h_ld * 2, 16 << i);
         if (!rc) rc = make_packed_maps(&ua.pk[0], 1, sl->layout, sl->base, (long long)sl->stride, sl->capacity);
         if (!rc && d->shared) rc = make_packed_maps(&ua.pk[2], 1, d->shared->layout, ea.src.shared, 0, 1);
         if (rc) return rc;

@@ -322,6 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
             if (!packed) {
                 asm volatile("prefetch.tensormap [%0];" ::"l"(&a.tmap_b) : "memory");
                 if (a.mode == 2) asm volatile("prefetch.tensormap [%0];" ::"l"(&a.tmap_a) : "memory");
+                else
+                    for (int i = 0; i < 4; ++i) asm volatile("prefetch.tensormap [%0];" ::"l"(&a.tmap_bn[i]) : "memory");
             }
             int it = 0, ch = 0;
             bool good = !(packed && a.mode == 2);
@@ -359,8 +361,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                             good = false;
                             break;
                         }
-                        mbar_expect_tx(&fullB[bb], (unsigned)(kBoxRows * kBK * 2));
-                        tma_box(sm + kSmemB + (size_t)bb * kBTile, &a.tmap_b, s2 * kBK, ti.grp.col0, &fullB[bb]);
+                        // the smallest box holding the group's columns (rows past them
+                        // belong to the next group or read as zeros; the MMA's N stops
+                        // at round-up(ncols, 16))
+                        int bi = 4;
+                        if (a.mode != 2) {
+                            const int nr = (ti.grp.ncols + 15) & ~15;
+                            bi = nr <= 16 ? 0 : nr <= 32 ? 1 : nr <= 64 ? 2 : nr <= 128 ? 3 : 4;
+                        }
+                        const CUtensorMap *mb = bi < 4 ? &a.tmap_bn[bi] : &a.tmap_b;
+                        const int box_rows = bi < 4 ? 16 << bi : kBoxRows;
+                        mbar_expect_tx(&fullB[bb], (unsigned)(box_rows * kBK * 2));
+                        tma_box(sm + kSmemB + (size_t)bb * kBTile, mb, s2 * kBK, ti.grp.col0, &fullB[bb]);
                         if (a.mode == 2) {
                             const int ba = it % kAStages;
                             if (it >= kAStages && !wait(&emptyA[ba], ((it / kAStages) - 1) & 1)) {

@@ -19,6 +19,9 @@ struct UmmaArgs {
     // order, fp16; mode 1: h; mode 2: x, bf16) and, for mode 2, the router rows
     alignas(64) CUtensorMap tmap_b;
     alignas(64) CUtensorMap tmap_a;
+    // modes 0 and 1: the B tensor again with boxes of 16, 32, 64 and 128 rows, so a
+    // group of n columns moves the smallest box that holds round-up(n, 16) rows
+    alignas(64) CUtensorMap tmap_bn[4];
     // packed weights as 3-D byte tensors [slot][row tile][bytes] (8-byte elements):
     // pk[0] / pk[1] routed experts, pk[2] / pk[3] the shared expert. Gate/up: [0|2]
     // boxes of the codes of a chunk (2,048 bytes x 4 row tiles), [1|3] its scales
