@@ -97,6 +97,16 @@ typedef struct {
 
 typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_GEGLU_TANH = 1 } moe_act;
 
+/* Route weights of the K chosen experts (the choice is the same for every kind:
+ * the K largest logits, equal logits to the lower id; sigmoid is monotone, so
+ * ranking sigmoid scores is ranking logits). Krasis white paper sec. 5.3 names
+ * sigmoid top-k routers (Nemotron Nano) beside softmax ones.
+ *   MOE_ROUTER_SOFTMAX       w_k = softmax over the K chosen logits (default)
+ *   MOE_ROUTER_SIGMOID       w_k = 1 / (1 + exp(-logit_k))
+ *   MOE_ROUTER_SIGMOID_NORM  the sigmoid scores divided by their sum over the K
+ * All in fp32 (expf, IEEE division; sums in rank order). */
+typedef enum { MOE_ROUTER_SOFTMAX = 0, MOE_ROUTER_SIGMOID = 1, MOE_ROUTER_SIGMOID_NORM = 2 } moe_router_kind;
+
 /* ------------------------------------------------------------ context */
 
 /* Create a context on CUDA device `device` (made current for the call). The
@@ -219,6 +229,35 @@ typedef struct {
     const moe_slots *shared; /* shared expert (layer `layer`, expert 0) or NULL */
     int F_shared;            /* its FFN width */
     int act;                 /* moe_act */
+    /* --- optional (zero / NULL = off) ---
+     * router_scale [H] f32: per-input-dimension scale of the router input,
+     *   logits = Wr (x * router_scale) (+ bias); the product x_h * s_h is rounded
+     *   to fp32 and the dot product accumulates in fp32 (kairos README, "The MoE
+     *   forward": the router scale is per input dimension).
+     * down_scale [E] f32: per-expert scale of the down projection, folded into
+     *   the route weight: the combine adds fp32(w_k * s_e) * y_k (kairos README:
+     *   the down scale is per expert). A pair whose scaled weight is 0 does no
+     *   expert work.
+     * router_kind: moe_router_kind.
+     * drop_eligible [E] u8, drop_protect_pct P, drop_mass_pct M: route-drop
+     *   policy P/M (Krasis white paper sec. 7.2). Per token: the first
+     *   ceil(K * P / 100) ranks are kept; among the later ranks whose expert is
+     *   eligible (nonzero byte) and whose weight is positive, taken from the
+     *   smallest weight up (equal weights: later rank first), routes are dropped
+     *   while the dropped weight c (fp32, summed in that order) keeps
+     *   c * 100 <= M * S, S = the sum of the K route weights in rank order
+     *   (fp32); the first route that does not fit ends the scan. A dropped route
+     *   keeps its place with weight 0 (no expert work, nothing added) and the
+     *   survivors are not renormalised (sec. 7.3). The decision uses the route
+     *   weights before down_scale. drop_eligible NULL = off.
+     * omitted_out [T] f32 (device, NULL = not reported): the dropped share c / S
+     *   of each token (0 when nothing is dropped). */
+    const float *router_scale;
+    const float *down_scale;
+    int router_kind;
+    const uint8_t *drop_eligible;
+    int drop_protect_pct, drop_mass_pct;
+    float *omitted_out;
 } moe_layer_desc;
 
 MOE_API int moe_layer_workspace(const moe_layer_desc *desc, int T_max, size_t *bytes);
@@ -226,9 +265,12 @@ MOE_API int moe_layer_workspace(const moe_layer_desc *desc, int T_max, size_t *b
 /* Expert part of the layer (steps 4-6): with the routing (ids, w) and buckets
  * (offsets, perm from moe_bucket over the same ids) given, computes
  *   y[t] = sum_k w[t][k] * expert_{ids[t][k]}(x[t]) (+ shared(x[t]))
- * with the layer description's slots (desc->Wr and bias are not read). Pairs
- * with w == 0 do no expert work and add nothing. ws: device workspace of at
- * least moe_layer_workspace(desc, T) bytes, 256-byte aligned. */
+ * with the layer description's slots (desc->Wr, bias, router_scale and the
+ * routing options are not read; desc->down_scale is: w becomes fp32(w *
+ * down_scale[e])). Pairs with w == 0 do no expert work and add nothing. ws:
+ * device workspace of at least moe_layer_workspace(desc, T) bytes, 256-byte
+ * aligned. A router input other than the experts' input (a separately normed
+ * tensor) is served by moe_router_topk on that input followed by this call. */
 MOE_API int moe_expert_ffn(moe_ctx *ctx, const moe_layer_desc *desc, const void *x, moe_dtype xt, int T,
                    const int32_t *ids, const float *w, const int32_t *offsets,
                    const int32_t *perm, float *y, void *ws, size_t ws_bytes,

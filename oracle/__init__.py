@@ -84,6 +84,15 @@ def _load():
     lib.orc_layer_forward.argtypes = [i, i, i, i, i, i, i, p, p, p, p, i, p, i, p, p, p, p, p]
     lib.orc_rmsnorm.restype = None
     lib.orc_rmsnorm.argtypes = [p, i, i, d, p]
+    lib.orc_router_logits_scaled.restype = None
+    lib.orc_router_logits_scaled.argtypes = [p, i, i, p, i, p, p, p]
+    lib.orc_route_weights.restype = None
+    lib.orc_route_weights.argtypes = [i, p, i, p]
+    lib.orc_route_drop.restype = i
+    lib.orc_route_drop.argtypes = [p, p, i, i, i, p, p, p]
+    lib.orc_layer_forward_routed.restype = i
+    lib.orc_layer_forward_routed.argtypes = [i, i, i, i, i, i, i, p, p, p, i, p, p, i, i, p, p, p, i, p, i, p,
+                                             p, p, p, p, p]
     _lib = lib
     return lib
 
@@ -194,6 +203,79 @@ def layer_forward(kind: int, zero_point: int, H: int, E: int, K: int, F: int, Wr
                                        _ptr(x), T, _ptr(li), _ptr(y), _ptr(ids), _ptr(w),
                                        _ptr(logits))
     return dict(y=y, ids=ids, w=w, logits=logits, status=int(status))
+
+
+ROUTER_SOFTMAX, ROUTER_SIGMOID, ROUTER_SIGMOID_NORM = 0, 1, 2
+
+
+def router_logits_scaled(x, Wr, scale, bias=None) -> np.ndarray:
+    """logits = Wr (x * scale) (+ bias), the router input scaled per input dimension."""
+    x = _f64(x)
+    Wr = _f64(Wr)
+    T, H = x.shape
+    E = Wr.shape[0]
+    sc = _f64(scale)
+    assert Wr.shape == (E, H) and sc.shape == (H,)
+    b = None if bias is None else _f64(bias)
+    out = np.empty((T, E), dtype=np.float64)
+    _load().orc_router_logits_scaled(_ptr(x), T, H, _ptr(Wr), E, _ptr(b), _ptr(sc), _ptr(out))
+    return out
+
+
+def route_weights(kind: int, sel_logits) -> np.ndarray:
+    """Route weights of the K chosen logits (rank order) for a router kind."""
+    l = _f64(sel_logits)
+    w = np.empty_like(l)
+    _load().orc_route_weights(kind, _ptr(l), l.size, _ptr(w))
+    return w
+
+
+def route_drop(w32, eligible, P: int, M: int):
+    """The P/M drop rule on one token's fp32 route weights; returns (weights after the
+    drop (f32), dropped count, dropped share (f32), decision margin)."""
+    w = np.ascontiguousarray(w32, dtype=np.float32)
+    el = _u8(eligible)
+    K = w.size
+    assert el.size == K and K <= 64
+    out = np.empty_like(w)
+    share = np.zeros(1, dtype=np.float32)
+    margin = np.zeros(1, dtype=np.float64)
+    n = _load().orc_route_drop(_ptr(w), _ptr(el), K, P, M, _ptr(out), _ptr(share), _ptr(margin))
+    return out, int(n), float(share[0]), float(margin[0])
+
+
+def layer_forward_routed(kind: int, zero_point: int, H: int, E: int, K: int, F: int, Wr, bias, experts, x,
+                         shared=None, F_shared: int = 0, logits_in=None, act: int = ACT_SWIGLU,
+                         router_scale=None, router_kind: int = ROUTER_SOFTMAX, down_scale=None,
+                         drop_eligible=None, drop_protect_pct: int = 0, drop_mass_pct: int = 0, drop_w32=None):
+    """layer_forward with a scaled router input, a router kind, the drop rule and a
+    per-expert down scale. Returns dict(y, ids, w, omitted, margin, status)."""
+    x = _f64(x)
+    T = x.shape[0]
+    assert x.shape == (T, H) and len(experts) == E
+    Wr_ = None if Wr is None else _f64(Wr)
+    b = None if bias is None else _f64(bias)
+    rs = None if router_scale is None else _f64(router_scale)
+    ds = None if down_scale is None else _f64(down_scale)
+    de = None if drop_eligible is None else _u8(drop_eligible)
+    dw = None if drop_w32 is None else np.ascontiguousarray(drop_w32, dtype=np.float32)
+    blobs = [None if e is None else _u8(e) for e in experts]
+    table = (ctypes.c_void_p * E)(*[None if e is None else e.ctypes.data for e in blobs])
+    sh = None if shared is None else _u8(shared)
+    li = None if logits_in is None else _f64(logits_in)
+    if li is None:
+        assert Wr_ is not None and Wr_.shape == (E, H)
+    y = np.empty((T, H), dtype=np.float64)
+    ids = np.empty((T, K), dtype=np.int32)
+    w = np.empty((T, K), dtype=np.float64)
+    omitted = np.zeros(T, dtype=np.float32)
+    margin = np.ones(T, dtype=np.float64)
+    status = _load().orc_layer_forward_routed(kind, zero_point, act, H, E, K, F, _ptr(Wr_), _ptr(b), _ptr(rs),
+                                              router_kind, _ptr(ds), _ptr(de), drop_protect_pct, drop_mass_pct,
+                                              _ptr(dw), ctypes.cast(table, ctypes.c_void_p), _ptr(sh), F_shared,
+                                              _ptr(x), T, _ptr(li), _ptr(y), _ptr(ids), _ptr(w), _ptr(omitted),
+                                              _ptr(margin))
+    return dict(y=y, ids=ids, w=w, omitted=omitted, margin=margin, status=int(status))
 
 
 def rmsnorm(x, eps: float = 1e-6) -> np.ndarray:

@@ -28,6 +28,17 @@
  *     NaN ranks below every number; weights are the softmax over all experts,
  *     renormalised over the K selected;
  *   - the shared expert has weight 1 and is added after the routed sum.
+ *
+ * Further routing forms, from the same pages:
+ *   [R] "The MoE forward": the router scale is per input dimension, the down
+ *       scale per expert (logits = Wr (x * s_r); expert e's output is scaled by s_e);
+ *   [K] sec. 5.3: sigmoid top-k routers (scores 1 / (1 + e^-l), optionally
+ *       normalised over the K chosen); the selection of the K largest logits is
+ *       the selection of the K largest sigmoid scores, as the sigmoid is monotone;
+ *   [K] sec. 7.2-7.3: the P/M route-drop rule (below, orc_route_drop), no
+ *       renormalisation of the surviving weights.
+ * The route-drop rule decides integers (which routes go) from floating-point sums;
+ * it is written in fp32, the precision the GPU decides in, and fed fp32 weights.
  */
 #include <math.h>
 #include <stdint.h>
@@ -39,6 +50,10 @@
 
 #define ORC_ACT_SWIGLU 0
 #define ORC_ACT_GEGLU_TANH 1
+
+#define ORC_ROUTER_SOFTMAX 0
+#define ORC_ROUTER_SIGMOID 1
+#define ORC_ROUTER_SIGMOID_NORM 2
 
 /* status bits returned by orc_layer_forward */
 #define ORC_ABSENT 1
@@ -126,6 +141,103 @@ void orc_router_logits(const double *x, int T, int H, const double *Wr, int E,
                 s += bias[e];
             logits[(int64_t)t * E + e] = s;
         }
+}
+
+/* logits[t][e] = sum_h Wr[e][h] * (x[t][h] * s[h]) (+ bias[e]): the router input
+ * scaled per input dimension ([R]). */
+void orc_router_logits_scaled(const double *x, int T, int H, const double *Wr, int E,
+                              const double *bias, const double *s, double *logits)
+{
+    for (int t = 0; t < T; t++)
+        for (int e = 0; e < E; e++) {
+            double acc = 0.0;
+            for (int h = 0; h < H; h++)
+                acc += Wr[(int64_t)e * H + h] * (x[(int64_t)t * H + h] * s[h]);
+            if (bias)
+                acc += bias[e];
+            logits[(int64_t)t * E + e] = acc;
+        }
+}
+
+/* Route weights of the K chosen logits l[0..K) (rank order) for a router kind:
+ * softmax over the K (= the full softmax renormalised over them), the sigmoid
+ * 1 / (1 + e^-l), or the sigmoid divided by its sum over the K. */
+void orc_route_weights(int kind, const double *l, int K, double *w)
+{
+    if (kind == ORC_ROUTER_SOFTMAX) {
+        double sum = 0.0;
+        for (int k = 0; k < K; k++)
+            sum += exp(l[k] - l[0]);
+        for (int k = 0; k < K; k++)
+            w[k] = exp(l[k] - l[0]) / sum;
+        return;
+    }
+    double sum = 0.0;
+    for (int k = 0; k < K; k++) {
+        w[k] = 1.0 / (1.0 + exp(-l[k]));
+        sum += w[k];
+    }
+    if (kind == ORC_ROUTER_SIGMOID_NORM)
+        for (int k = 0; k < K; k++)
+            w[k] /= sum;
+}
+
+/* The P/M route-drop rule ([K] sec. 7.2) on one token's K route weights w[0..K)
+ * (rank order, fp32) with eligible[k] (the expert of rank k may be dropped):
+ *   1. the first ceil(K P / 100) ranks are kept;
+ *   2. candidates: later ranks that are eligible and have a positive weight;
+ *   3. taken from the smallest weight up (equal weights: the later rank first);
+ *   4. a candidate is dropped while the dropped total c (fp32, in that order)
+ *      stays at or below M percent of S, the sum of the K weights in rank order
+ *      (fp32): c * 100 <= M * S; the first that does not fit ends the scan.
+ * Dropped routes get weight 0; the others keep theirs ([K] sec. 7.3). Returns the
+ * number dropped; *share = c / S (0 if S is 0); *margin = the smallest
+ * |c' * 100 - M * S| / (M * S) over the comparisons made (how far each decision
+ * was from flipping; 1 if none or M * S is 0). */
+int orc_route_drop(const float *w, const uint8_t *eligible, int K, int P, int M, float *w_out,
+                   float *share, double *margin)
+{
+    int protect = (K * P + 99) / 100;
+    float S = 0.0f;
+    for (int k = 0; k < K; k++)
+        S += w[k];
+    int order[64], n = 0;
+    for (int k = protect; k < K; k++)
+        if (eligible[k] && w[k] > 0.0f)
+            order[n++] = k;
+    /* insertion sort: ascending weight, equal weights later rank first */
+    for (int i = 1; i < n; i++) {
+        int v = order[i], j = i - 1;
+        while (j >= 0 && (w[order[j]] > w[v] || (w[order[j]] == w[v] && order[j] < v))) {
+            order[j + 1] = order[j];
+            j--;
+        }
+        order[j + 1] = v;
+    }
+    for (int k = 0; k < K; k++)
+        w_out[k] = w[k];
+    float c = 0.0f, lim = (float)M * S;
+    double mg = 1.0;
+    int nd = 0;
+    for (int i = 0; i < n; i++) {
+        float c2 = c + w[order[i]];
+        float lhs = c2 * 100.0f;
+        if (lim > 0.0f) {
+            double r = fabs((double)lhs - (double)lim) / (double)lim;
+            if (r < mg)
+                mg = r;
+        }
+        if (lhs <= lim) {
+            c = c2;
+            w_out[order[i]] = 0.0f;
+            nd++;
+        } else {
+            break;
+        }
+    }
+    *share = S > 0.0f ? c / S : 0.0f;
+    *margin = mg;
+    return nd;
 }
 
 /* 1 if expert a ranks before expert b: larger logit first, equal logits to the
@@ -276,6 +388,91 @@ void orc_expert_ffn(int kind, int zero_point, int act, const uint8_t *blob, int 
  * experts[e] == NULL means expert e is absent: it contributes nothing and the
  * ORC_ABSENT bit is returned. A pair with weight exactly 0 contributes nothing.
  * Returns status bits (ORC_ABSENT, ORC_NONFINITE). */
+/* The layer with the routing forms above: logits from the scaled router input
+ * (router_scale may be NULL) unless logits_in is given; top-K selection as
+ * orc_topk; route weights of router_kind (fp64); if drop_eligible is not NULL,
+ * the drop rule on the fp32 rounding of those weights (drop_w32 may give the fp32
+ * weights to decide on instead), dropped routes then count 0; then each weight is
+ * multiplied by down_scale[e] (may be NULL); the combine as orc_layer_forward.
+ * omitted [T] (may be NULL) gets each token's dropped share, margin [T] the
+ * decision margin of orc_route_drop. Returns the status bits. */
+int orc_layer_forward_routed(int kind, int zero_point, int act, int H, int E, int K, int F,
+                             const double *Wr, const double *bias, const double *router_scale,
+                             int router_kind, const double *down_scale, const uint8_t *drop_eligible,
+                             int P, int M, const float *drop_w32, const uint8_t *const *experts,
+                             const uint8_t *shared, int F_shared, const double *x, int T,
+                             const double *logits_in, double *y, int *ids, double *w, float *omitted,
+                             double *margin)
+{
+    int status = 0;
+    double *logits = (double *)malloc(sizeof(double) * (size_t)T * E);
+    double *ye = (double *)malloc(sizeof(double) * (size_t)H);
+    if (logits_in)
+        memcpy(logits, logits_in, sizeof(double) * (size_t)T * E);
+    else if (router_scale)
+        orc_router_logits_scaled(x, T, H, Wr, E, bias, router_scale, logits);
+    else
+        orc_router_logits(x, T, H, Wr, E, bias, logits);
+    if (orc_topk(logits, T, E, K, ids, w))
+        status |= ORC_NONFINITE;
+    for (int t = 0; t < T; t++) {
+        double lsel[32];
+        float w32[32], wd[32], share = 0.0f;
+        uint8_t el[32];
+        double mg = 1.0;
+        int bad = 0;
+        for (int k = 0; k < K; k++) {
+            lsel[k] = logits[(int64_t)t * E + ids[t * K + k]];
+            if (!isfinite(lsel[k]))
+                bad = 1;
+        }
+        if (!bad)
+            orc_route_weights(router_kind, lsel, K, w + t * K);
+        if (!bad && drop_eligible) {
+            for (int k = 0; k < K; k++) {
+                w32[k] = drop_w32 ? drop_w32[t * K + k] : (float)w[t * K + k];
+                el[k] = drop_eligible[ids[t * K + k]] != 0;
+            }
+            orc_route_drop(w32, el, K, P, M, wd, &share, &mg);
+            for (int k = 0; k < K; k++)
+                if (wd[k] == 0.0f && w32[k] != 0.0f)
+                    w[t * K + k] = 0.0;
+        }
+        if (omitted)
+            omitted[t] = share;
+        if (margin)
+            margin[t] = mg;
+        if (!bad && down_scale)
+            for (int k = 0; k < K; k++)
+                w[t * K + k] *= down_scale[ids[t * K + k]];
+        double *yt = y + (int64_t)t * H;
+        const double *xt = x + (int64_t)t * H;
+        for (int j = 0; j < H; j++)
+            yt[j] = 0.0;
+        for (int k = 0; k < K; k++) {
+            int e = ids[t * K + k];
+            double wk = w[t * K + k];
+            if (!experts[e]) {
+                status |= ORC_ABSENT;
+                continue;
+            }
+            if (wk == 0.0)
+                continue;
+            orc_expert_ffn(kind, zero_point, act, experts[e], H, F, xt, 1, ye);
+            for (int j = 0; j < H; j++)
+                yt[j] += wk * ye[j];
+        }
+        if (shared) {
+            orc_expert_ffn(kind, zero_point, act, shared, H, F_shared, xt, 1, ye);
+            for (int j = 0; j < H; j++)
+                yt[j] += ye[j];
+        }
+    }
+    free(logits);
+    free(ye);
+    return status;
+}
+
 int orc_layer_forward(int kind, int zero_point, int act, int H, int E, int K, int F,
                       const double *Wr, const double *bias, const uint8_t *const *experts,
                       const uint8_t *shared, int F_shared, const double *x, int T,

@@ -20,6 +20,7 @@ STATUS_EXPERT_ABSENT, STATUS_NONFINITE, STATUS_TIMEOUT, STATUS_BOUNDS = 1, 2, 4,
 F32, BF16 = 0, 1
 Q4_32, Q2_64 = 0, 1
 ACT_SWIGLU, ACT_GEGLU_TANH = 0, 1
+ROUTER_SOFTMAX, ROUTER_SIGMOID, ROUTER_SIGMOID_NORM = 0, 1, 2
 
 
 class MoeError(RuntimeError):
@@ -36,7 +37,10 @@ class LayerDesc(ctypes.Structure):
     _fields_ = [("slots", ctypes.c_void_p), ("layer", ctypes.c_int), ("H", ctypes.c_int),
                 ("E", ctypes.c_int), ("K", ctypes.c_int), ("F", ctypes.c_int),
                 ("Wr", ctypes.c_void_p), ("wr_dtype", ctypes.c_int), ("bias", ctypes.c_void_p),
-                ("shared", ctypes.c_void_p), ("F_shared", ctypes.c_int), ("act", ctypes.c_int)]
+                ("shared", ctypes.c_void_p), ("F_shared", ctypes.c_int), ("act", ctypes.c_int),
+                ("router_scale", ctypes.c_void_p), ("down_scale", ctypes.c_void_p), ("router_kind", ctypes.c_int),
+                ("drop_eligible", ctypes.c_void_p), ("drop_protect_pct", ctypes.c_int),
+                ("drop_mass_pct", ctypes.c_int), ("omitted_out", ctypes.c_void_p)]
 
 
 _lib = None
@@ -220,9 +224,13 @@ def moe_bucket(ctx: int, ids, E: int, counts, offsets, perm, active, n_active, s
 
 
 def layer_desc(slots: int, layer: int, H: int, E: int, K: int, F: int, Wr=None, bias=None,
-               shared: int | None = None, F_shared: int = 0, act: int = ACT_SWIGLU) -> LayerDesc:
+               shared: int | None = None, F_shared: int = 0, act: int = ACT_SWIGLU, router_scale=None,
+               down_scale=None, router_kind: int = ROUTER_SOFTMAX, drop_eligible=None, drop_protect_pct: int = 0,
+               drop_mass_pct: int = 0, omitted_out=None) -> LayerDesc:
     wr_dtype = dtype_code(Wr) if Wr is not None else BF16
-    return LayerDesc(slots, layer, H, E, K, F, _ptr(Wr), wr_dtype, _ptr(bias), shared, F_shared, act)
+    return LayerDesc(slots, layer, H, E, K, F, _ptr(Wr), wr_dtype, _ptr(bias), shared, F_shared, act,
+                     _ptr(router_scale), _ptr(down_scale), router_kind, _ptr(drop_eligible), drop_protect_pct,
+                     drop_mass_pct, _ptr(omitted_out))
 
 
 def moe_layer_workspace(desc: LayerDesc, T_max: int) -> int:

@@ -139,6 +139,13 @@ int check_desc(const moe_layer_desc *d) {
     if (d->E < 1 || d->E > 1024) return set_error(MOE_ERR_SHAPE, "E=%d not in 1..1024", d->E);
     if (d->K < 1 || d->K > 32 || d->K > d->E) return set_error(MOE_ERR_SHAPE, "K=%d not in 1..min(E, 32)", d->K);
     if (d->act != MOE_ACT_SWIGLU && d->act != MOE_ACT_GEGLU_TANH) return set_error(MOE_ERR_ARG, "unknown activation %d", d->act);
+    if (d->router_kind < MOE_ROUTER_SOFTMAX || d->router_kind > MOE_ROUTER_SIGMOID_NORM)
+        return set_error(MOE_ERR_ARG, "unknown router kind %d", d->router_kind);
+    if (d->drop_eligible && (d->drop_protect_pct < 0 || d->drop_protect_pct > 100 || d->drop_mass_pct < 0 ||
+                             d->drop_mass_pct > 100))
+        return set_error(MOE_ERR_ARG, "drop policy %d/%d not in 0..100", d->drop_protect_pct, d->drop_mass_pct);
+    if (d->router_scale && (uintptr_t)d->router_scale % 16)
+        return set_error(MOE_ERR_ARG, "router_scale not 16-byte aligned");
     if (d->shared) {
         const moe_slots *sh = d->shared;
         if (sh->H != d->H || sh->F != d->F_shared || sh->fmt.kind != s->fmt.kind)
@@ -160,10 +167,11 @@ int check_ws(void *ws, size_t ws_bytes, size_t need) {
 
 // Router logits: windows of at least MOE_OPT_PREFILL_MIN_T tokens with bf16 x and
 // Wr run the GEMM on the tensor cores (fp32 accumulation in tensor memory); other
-// windows use the CUDA-core kernel with the canonical per-row order.
+// windows use the CUDA-core kernel with the canonical per-row order, as does a
+// router with a per-input-dimension scale (its input x * s is fp32).
 int router_logits(moe_ctx *ctx, const void *x, moe_dtype xt, int T, int H, const void *Wr, moe_dtype wt,
-                  const float *bias, int E, float *logits, cudaStream_t s) {
-    if (T >= ctx->prefill_min && xt == MOE_BF16 && wt == MOE_BF16 && umma_router_supported(H) &&
+                  const float *bias, const float *router_scale, int E, float *logits, cudaStream_t s) {
+    if (!router_scale && T >= ctx->prefill_min && xt == MOE_BF16 && wt == MOE_BF16 && umma_router_supported(H) &&
         (size_t)ctx->max_smem >= umma_smem_bytes() && (uintptr_t)x % 16 == 0 && (uintptr_t)Wr % 16 == 0) {
         int sms = 0;
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device));
@@ -187,7 +195,18 @@ int router_logits(moe_ctx *ctx, const void *x, moe_dtype xt, int T, int H, const
         const int tiles = ua.n_mt * ((T + 255) / 256);
         return launch_umma(ua, tiles < sms ? tiles : sms, s);
     }
-    return launch_router_logits(x, xt, T, H, Wr, wt, bias, E, logits, s);
+    return launch_router_logits(x, xt, T, H, Wr, wt, bias, router_scale, E, logits, s);
+}
+
+RouteOpts route_opts(const moe_layer_desc *d, int T) {
+    RouteOpts o;
+    o.kind = d->router_kind;
+    o.down_scale = d->down_scale;
+    o.drop_eligible = d->drop_eligible;
+    o.drop_protect = d->drop_protect_pct;
+    o.drop_mass = d->drop_mass_pct;
+    o.omitted = T > 0 ? d->omitted_out : nullptr;
+    return o;
 }
 
 // Steps 4-6 (plan, experts, combine) given ids, w, offsets, perm.
@@ -409,6 +428,8 @@ int try_persistent(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers, boo
             P.arena = d.slots->base;
             P.stride = (long long)d.slots->stride;
             P.shared = d.shared ? d.shared->base + (size_t)d.shared->h_table[0] * d.shared->stride : nullptr;
+            P.router_scale = d.router_scale;
+            P.route = route_opts(&d, T);
         }
         rc = launch_decode_persistent(a, G, s);
         if (rc) return rc;
@@ -424,9 +445,9 @@ int layer_core(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype x
     float *logits = logits_out ? logits_out : (float *)(ws + W.logits);
     int32_t *ids = ids_out ? ids_out : (int32_t *)(ws + W.ids);
     float *w = (float *)(ws + W.w);
-    int rc = router_logits(ctx, x, xt, T, d->H, d->Wr, d->wr_dtype, d->bias, d->E, logits, s);
+    int rc = router_logits(ctx, x, xt, T, d->H, d->Wr, d->wr_dtype, d->bias, d->router_scale, d->E, logits, s);
     if (rc) return rc;
-    rc = launch_topk(logits, T, d->E, d->K, ids, w, ctx->d_status, s);
+    rc = launch_topk(logits, T, d->E, d->K, ids, w, route_opts(d, T), ctx->d_status, s);
     if (rc) return rc;
     if (use_wide(T, d->K))
         rc = launch_bucket_wide(ids, T, d->K, d->E, (int32_t *)(ws + W.counts), (int32_t *)(ws + W.offsets),
@@ -746,9 +767,9 @@ int moe_router_topk(moe_ctx *ctx, const void *x, moe_dtype xt, int T, int H, con
     const cudaStream_t s = (cudaStream_t)stream;
     float *logits = logits_out;
     if (!logits) return set_error(MOE_ERR_ARG, "logits_out is required by this implementation (pass a [T][E] buffer)");
-    int rc = router_logits(ctx, x, xt, T, H, Wr, wt, bias, E, logits, s);
+    int rc = router_logits(ctx, x, xt, T, H, Wr, wt, bias, nullptr, E, logits, s);
     if (rc) return rc;
-    return launch_topk(logits, T, E, K, ids, w, ctx->d_status, s);
+    return launch_topk(logits, T, E, K, ids, w, RouteOpts{}, ctx->d_status, s);
 }
 
 int moe_bucket(moe_ctx *ctx, const int32_t *ids, int T, int K, int E, int32_t *counts, int32_t *offsets,
@@ -783,6 +804,13 @@ int moe_expert_ffn(moe_ctx *ctx, const moe_layer_desc *desc, const void *x, moe_
     rc = check_ws(ws, ws_bytes, ws_layout(desc, T, 4).total);
     if (rc) return rc;
     MOE_GUARD(ctx);
+    if (desc->down_scale) {
+        // the given route weights with each expert's down scale folded in
+        float *ws_w = (float *)((uint8_t *)ws + W.w);
+        rc = launch_scale_weights(ids, w, desc->down_scale, T * desc->K, desc->E, ws_w, (cudaStream_t)stream);
+        if (rc) return rc;
+        w = ws_w;
+    }
     return run_experts(ctx, desc, x, xt, T, ids, w, offsets, perm, y, 0, (uint8_t *)ws, W, (cudaStream_t)stream);
 }
 

@@ -352,6 +352,86 @@ __device__ __forceinline__ float topk_weight_smem(float sel_v, float m, int K, i
     return ex / s;
 }
 
+// Route-drop policy P/M (Krasis white paper sec. 7.2) on the K route weights of
+// one token (lane k < K holds choice k: weight w, expert si): the first
+// ceil(K P / 100) ranks are kept; the later ranks with an eligible expert and a
+// positive weight are taken from the smallest weight up (equal weights: later rank
+// first) while the dropped sum c (fp32, in that order) keeps c * 100 <= M * S, S the
+// fp32 sum of the K weights in rank order; the first that does not fit ends it.
+// Dropped routes get weight 0 (sec. 7.3: no renormalisation). Scratch: this warp's
+// 32 floats and 64 ints of shared memory. *share = c / S (0 if S = 0).
+__device__ __forceinline__ float route_drop(const RouteOpts &o, float w, int si, int K, int lane, float *fs, int *is,
+                                            float *share) {
+    __syncwarp();
+    const int protect = (K * o.drop_protect + 99) / 100;
+    const bool cand = lane < K && lane >= protect && w > 0.f && o.drop_eligible[si] != 0;
+    fs[lane] = lane < K ? w : 0.f;
+    is[lane] = cand ? 1 : 0;
+    __syncwarp();
+    float S = 0.f;
+    for (int k = 0; k < K; ++k) S += fs[k];
+    int r = 0;
+    if (cand)
+        for (int j = protect; j < K; ++j) {
+            const float wj = fs[j];
+            r += is[j] && (wj < w || (wj == w && j > lane));
+        }
+    const int nc = __popc(__ballot_sync(0xffffffffu, cand));
+    if (cand) is[32 + r] = lane;
+    __syncwarp();
+    // every lane walks the same list in the same order
+    float c = 0.f;
+    int nd = 0;
+    const float lim = (float)o.drop_mass * S;
+    for (int i = 0; i < nc; ++i) {
+        const float c2 = c + fs[is[32 + i]];
+        if (c2 * 100.f <= lim) {
+            c = c2;
+            ++nd;
+        } else {
+            break;
+        }
+    }
+    *share = S > 0.f ? c / S : 0.f;
+    __syncwarp();
+    return (cand && r < nd) ? 0.f : w;
+}
+
+// Route weight of choice `lane` (< K) of one token: logit sv, expert si, m = the
+// largest chosen logit. The kind's weight (softmax: topk_weight_smem's arithmetic;
+// sigmoid: 1 / (1 + expf(-sv)); sigmoid_norm: that over the sum of the K in rank
+// order), then the drop policy, then the expert's down scale. Lane 0 writes the
+// dropped share to omitted[t] when omitted is not null. Every lane of the warp calls
+// it; fs / is: this warp's 32 floats and 64 ints of shared memory.
+__device__ __forceinline__ float route_weight(const RouteOpts &o, float sv, float m, int si, int K, int lane,
+                                              float *fs, int *is, float *omitted, int t) {
+    float w;
+    if (o.kind == MOE_ROUTER_SOFTMAX) {
+        w = topk_weight_smem(sv, m, K, lane, fs);
+    } else {
+        const float sg = lane < K ? 1.f / (1.f + expf(-sv)) : 0.f;
+        if (o.kind == MOE_ROUTER_SIGMOID_NORM) {
+            __syncwarp();
+            fs[lane] = sg;
+            __syncwarp();
+            float sum = 0.f;
+            for (int k = 0; k < K; ++k) sum += fs[k];
+            w = sg / sum;
+        } else {
+            w = sg;
+        }
+    }
+    if (o.drop_eligible) {
+        float share;
+        w = route_drop(o, w, si, K, lane, fs, is, &share);
+        if (omitted && lane == 0) omitted[t] = share;
+    } else if (omitted && lane == 0) {
+        omitted[t] = 0.f;
+    }
+    if (o.down_scale && lane < K) w *= o.down_scale[si];
+    return w;
+}
+
 // ---------------------------------------------------------------- rmsnorm
 
 // RMSNorm with the canonical 512-lane order: thread i (0..511) accumulates x_h^2

@@ -63,7 +63,8 @@ struct alignas(16) Plan {
     float rpart[16][kMaxTok][4];          // router partial sums [row][token][warp]
     float wsum[kMaxTok][kNormWarps];      // RMSNorm warp sums
     unsigned long long sel[kMaxTok][32];  // chosen keys per token, rank order
-    float wex[kMaxTok][32];               // softmax exponentials per token
+    float wex[kMaxTok][32];               // route-weight scratch per token
+    int wix[kMaxTok][64];
     uint64_t ring_bar[kPersistThreads / 32][8];  // weight-ring mbarriers per warp
     uint64_t rbar;                               // router-row copies
 };
@@ -429,11 +430,19 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
             const int wsz = a.wr_bf16 ? 2 : 4;
             const int q = warp & 3;
             const int nr = (E - cta + G - 1) / G;  // experts cta, cta + G, ...
+            const float *const rscale = Ly.router_scale;
             auto xf = [&](int t, int h, float v[8]) {
                 if (XF32 && !a.stack)
                     load_w8<float>(reinterpret_cast<const float *>(a.x) + (size_t)t * H + h, v);
                 else
                     bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xs + (size_t)t * ldx + h), v);
+                if (rscale) {
+                    // the scaled router input x_h * s_h, rounded to fp32
+                    float sc[8];
+                    load_w8<float>(rscale + h, sc);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] *= sc[j];
+                }
             };
             for (int r = warp >> 2; r < nr; r += kPWarps / 4) {
                 float acc[kMaxTok];
@@ -569,7 +578,14 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                 const float sv = topk_key_value(key);
                 const bool bad = s.misc[4 + t] != 0;
                 const float m = topk_key_value(s.sel[t][0]);
-                const float wk = bad ? __int_as_float(0x7fc00000) : topk_weight_smem(sv, m, K, lane, s.wex[t]);
+                float wk;
+                if (bad) {
+                    wk = __int_as_float(0x7fc00000);
+                    if (lane == 0 && cta == 0 && Ly.route.omitted) Ly.route.omitted[t] = 0.f;
+                } else {
+                    wk = route_weight(Ly.route, sv, m, si, K, lane, s.wex[t], s.wix[t],
+                                      cta == 0 ? Ly.route.omitted : nullptr, t);
+                }
                 if (lane < K) {
                     s.ids[t * K + lane] = si;
                     s.w[t * K + lane] = wk;

@@ -7,7 +7,7 @@ namespace moe {
 
 constexpr int kPersistThreads = 512;
 constexpr int kMaxTok = 8;             // tokens per window on this path
-constexpr int kMaxPersistLayers = 48;  // layers per launch (longer stacks: several launches)
+constexpr int kMaxPersistLayers = 32;  // layers per launch (longer stacks: several launches)
 constexpr size_t kRedBytes = (kPersistThreads / 32) * 32 * 8 * sizeof(float);
 constexpr int kMaxRingBytes = 16384;   // weight ring per warp (bytes)
 constexpr int kCandCap = 128;          // top-K candidates per token kept by the threshold pass
@@ -36,6 +36,8 @@ struct PersistLayer {
     const uint8_t *arena;   // slot 0 of the pool
     long long stride;       // bytes per slot
     const uint8_t *shared;  // shared expert (device layout) or null
+    const float *router_scale;  // [H] or null
+    RouteOpts route;            // route-weight kind, drop policy, down scale
 };
 
 struct PersistArgs {

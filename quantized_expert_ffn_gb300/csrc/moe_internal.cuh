@@ -251,6 +251,15 @@ struct PlanArgs {
     uint32_t *status;
 };
 
+// Route-weight options of one layer (moe_layer_desc's optional fields).
+struct RouteOpts {
+    int kind = MOE_ROUTER_SOFTMAX;            // moe_router_kind
+    const float *down_scale = nullptr;        // [E] or null
+    const uint8_t *drop_eligible = nullptr;   // [E] or null: no drops
+    int drop_protect = 0, drop_mass = 0;      // P, M (percent)
+    float *omitted = nullptr;                 // [T] or null
+};
+
 struct ExpertArgs {
     ExpertSrc src;
     const Group *groups;
@@ -277,9 +286,13 @@ int init_expert_attributes(int max_smem);
 int init_repack_attributes(int max_smem);
 int repack_expert(const QLayout &L, const uint8_t *blob, uint8_t *dst, cudaStream_t stream);
 int launch_router_logits(const void *x, moe_dtype xt, int T, int H, const void *Wr, moe_dtype wt,
-                         const float *bias, int E, float *logits, cudaStream_t s);
-int launch_topk(const float *logits, int T, int E, int K, int32_t *ids, float *w, uint32_t *status,
-                cudaStream_t s);
+                         const float *bias, const float *router_scale, int E, float *logits, cudaStream_t s);
+int launch_topk(const float *logits, int T, int E, int K, int32_t *ids, float *w, const RouteOpts &ro,
+                uint32_t *status, cudaStream_t s);
+// w_out[p] = fp32(w[p] * down_scale[ids[p]]) (the route weight of pair p with its
+// expert's down scale folded in; ids out of range give 0)
+int launch_scale_weights(const int32_t *ids, const float *w, const float *down_scale, int P, int E, float *w_out,
+                         cudaStream_t s);
 int launch_bucket(const int32_t *ids, int T, int K, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
                   int32_t *active, int32_t *n_active, uint32_t *status, cudaStream_t s);
 int launch_plan(const PlanArgs &a, cudaStream_t s);

@@ -19,7 +19,8 @@ constexpr int kRouterExp = 16;  // experts per CTA (one warp each)
 // x rows staged in shared memory serve 16 experts.
 template <typename XT, typename WT>
 __global__ void __launch_bounds__(32 * kRouterExp) k_router_logits(const XT *__restrict__ x, const WT *__restrict__ Wr,
-                                                                   const float *__restrict__ bias, int T, int H, int E,
+                                                                   const float *__restrict__ bias,
+                                                                   const float *__restrict__ rscale, int T, int H, int E,
                                                                    float *__restrict__ logits) {
     extern __shared__ __align__(16) float xs[];  // [8][H]
     const int t0 = blockIdx.y * kRouterTok;
@@ -28,6 +29,13 @@ __global__ void __launch_bounds__(32 * kRouterExp) k_router_logits(const XT *__r
         const int t = i / (H / 8), h = (i % (H / 8)) * 8;
         float v[8];
         load_w8<XT>(x + (size_t)(t0 + t) * H + h, v);
+        if (rscale) {
+            // the scaled router input x_h * s_h, rounded to fp32
+            float sc[8];
+            load_w8<float>(rscale + h, sc);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] *= sc[j];
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) xs[t * H + h + j] = v[j];
     }
@@ -64,8 +72,10 @@ constexpr int kTopkWarps = 8;
 // agrees with any other correct selection. Weights: softmax of the K chosen
 // logits (= the full softmax renormalised over them).
 __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int T, int E, int K,
-                                              int32_t *__restrict__ ids, float *__restrict__ w,
+                                              int32_t *__restrict__ ids, float *__restrict__ w, const RouteOpts ro,
                                               uint32_t *status) {
+    __shared__ float fs[kTopkWarps][32];
+    __shared__ int is[kTopkWarps][64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * kTopkWarps + warp;
     if (t >= T) return;
@@ -84,25 +94,38 @@ __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, 
     const float sv = topk_key_value(best);
     if (lane < K) ids[(size_t)t * K + lane] = si;
     if (bad) {
-        if (lane == 0) set_status(status, MOE_STATUS_NONFINITE);
+        if (lane == 0) {
+            set_status(status, MOE_STATUS_NONFINITE);
+            if (ro.omitted) ro.omitted[t] = 0.f;
+        }
         if (lane < K) w[(size_t)t * K + lane] = __int_as_float(0x7fc00000);
         return;
     }
-    const float wk = topk_weight(sv, K, lane);
+    const float m = __shfl_sync(0xffffffffu, sv, 0);
+    const float wk = route_weight(ro, sv, m, si, K, lane, fs[warp], is[warp], ro.omitted, t);
     if (lane < K) w[(size_t)t * K + lane] = wk;
+}
+
+// w_out[p] = fp32(w[p] * down_scale[ids[p]]), as route_weight folds the scale
+__global__ void k_scale_weights(const int32_t *__restrict__ ids, const float *__restrict__ w,
+                                const float *__restrict__ down_scale, int P, int E, float *__restrict__ w_out) {
+    const int p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= P) return;
+    const int e = ids[p];
+    w_out[p] = (e >= 0 && e < E) ? w[p] * down_scale[e] : 0.f;
 }
 
 }  // namespace
 
 int launch_router_logits(const void *x, moe_dtype xt, int T, int H, const void *Wr, moe_dtype wt,
-                         const float *bias, int E, float *logits, cudaStream_t s) {
+                         const float *bias, const float *router_scale, int E, float *logits, cudaStream_t s) {
     if (T == 0) return MOE_OK;
     const dim3 grid((E + kRouterExp - 1) / kRouterExp, (T + kRouterTok - 1) / kRouterTok);
     const size_t smem = (size_t)kRouterTok * H * sizeof(float);
     if (smem > 200 * 1024) return set_error(MOE_ERR_SHAPE, "router: H=%d too large", H);
 #define MOE_ROUTER_CASE(XT, WT)                                                                     \
     {                                                                                               \
-        k_router_logits<XT, WT><<<grid, 32 * kRouterExp, smem, s>>>((const XT *)x, (const WT *)Wr, bias, T, H, E, logits); \
+        k_router_logits<XT, WT><<<grid, 32 * kRouterExp, smem, s>>>((const XT *)x, (const WT *)Wr, bias, router_scale, T, H, E, logits); \
     }
     if (xt == MOE_F32 && wt == MOE_F32) MOE_ROUTER_CASE(float, float)
     else if (xt == MOE_F32 && wt == MOE_BF16) MOE_ROUTER_CASE(float, __nv_bfloat16)
@@ -113,10 +136,18 @@ int launch_router_logits(const void *x, moe_dtype xt, int T, int H, const void *
     return MOE_OK;
 }
 
-int launch_topk(const float *logits, int T, int E, int K, int32_t *ids, float *w, uint32_t *status,
-                cudaStream_t s) {
+int launch_topk(const float *logits, int T, int E, int K, int32_t *ids, float *w, const RouteOpts &ro,
+                uint32_t *status, cudaStream_t s) {
     if (T == 0) return MOE_OK;
-    k_topk<<<(T + kTopkWarps - 1) / kTopkWarps, 32 * kTopkWarps, 0, s>>>(logits, T, E, K, ids, w, status);
+    k_topk<<<(T + kTopkWarps - 1) / kTopkWarps, 32 * kTopkWarps, 0, s>>>(logits, T, E, K, ids, w, ro, status);
+    MOE_CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int launch_scale_weights(const int32_t *ids, const float *w, const float *down_scale, int P, int E, float *w_out,
+                         cudaStream_t s) {
+    if (P == 0) return MOE_OK;
+    k_scale_weights<<<(P + 255) / 256, 256, 0, s>>>(ids, w, down_scale, P, E, w_out);
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }

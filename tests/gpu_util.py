@@ -77,10 +77,13 @@ class GpuLayers:
             T.cuda.synchronize()
             del staging
 
+    # optional layer_desc fields (act, router_scale, down_scale, router_kind, drop policy)
+    opts: dict = {}
+
     def desc(self, l: int = 0):
         cfg = self.cfg
         return L.layer_desc(self.slots, l, cfg.H, cfg.E, cfg.K, cfg.F, self.Wr[l], self.bias[l],
-                            self.shared[l] if self.shared else None, cfg.F_shared)
+                            self.shared[l] if self.shared else None, cfg.F_shared, **self.opts)
 
     def workspace(self, T_tokens: int, extra: int = 0):
         T = torch()

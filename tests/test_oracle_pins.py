@@ -409,3 +409,148 @@ def test_rmsnorm_closed_forms():
     y = oracle.rmsnorm(x, 0.0)
     np.testing.assert_allclose((y * y).mean(1), 1.0, rtol=1e-14)
     np.testing.assert_allclose(oracle.rmsnorm(7.5 * x, 0.0), y, rtol=1e-14)
+
+
+# ------------------------------------------------------------------ routing forms
+# (kairos README "The MoE forward": per-input-dim router scale, per-expert down scale;
+#  Krasis white paper sec. 5.3: sigmoid top-k; sec. 7.2-7.3: the P/M drop rule)
+
+def _w32(*v):
+    return np.array(v, dtype=np.float32)
+
+
+def test_drop_rule_protects_leading_ranks_and_takes_smallest_first():
+    # top-10, 75/8: ceil(10 * 75 / 100) = 8 ranks kept (the white paper's "protects
+    # ranks 1-8"); ranks 9 and 10 hold 0.03 each of a total mass of 1.0
+    w = _w32(0.3, 0.2, 0.1, 0.1, 0.1, 0.05, 0.05, 0.04, 0.03, 0.03)
+    out, n, share, _ = oracle.route_drop(w, np.ones(10), 75, 8)
+    assert n == 2 and np.array_equal(out[:8], w[:8]) and out[8] == 0 and out[9] == 0
+    assert abs(share - 0.06) < 1e-6
+    # 75/5: 0.03 fits, 0.06 does not; equal weights go later rank first
+    out, n, share, _ = oracle.route_drop(w, np.ones(10), 75, 5)
+    assert n == 1 and out[9] == 0 and out[8] == w[8] and abs(share - 0.03) < 1e-6
+    # rank 10 not eligible: only rank 9 is a candidate
+    el = np.ones(10)
+    el[9] = 0
+    out, n, _, _ = oracle.route_drop(w, el, 75, 8)
+    assert n == 1 and out[8] == 0 and out[9] == w[9]
+
+
+def test_drop_rule_order_is_by_weight_not_rank():
+    # ranks 3 and 4 are candidates (K=4, P=50 keeps 2); rank 4 is heavier than rank 3
+    w = _w32(0.5, 0.3, 0.05, 0.15)
+    out, n, share, _ = oracle.route_drop(w, np.ones(4), 50, 10)
+    # smallest first: 0.05 (rank 3) fits under 10%, then 0.20 > 10% stops the scan
+    assert n == 1 and out[2] == 0 and out[3] == w[3] and abs(share - 0.05) < 1e-6
+    # M = 100: every candidate goes (their sum never exceeds the total)
+    out, n, _, _ = oracle.route_drop(w, np.ones(4), 50, 100)
+    assert n == 2 and out[2] == 0 and out[3] == 0 and np.array_equal(out[:2], w[:2])
+
+
+def test_drop_rule_off_cases():
+    w = _w32(0.4, 0.3, 0.2, 0.1, 0.0)
+    for P, M, el in [(100, 50, np.ones(5)), (0, 0, np.ones(5)), (0, 50, np.zeros(5))]:
+        out, n, share, _ = oracle.route_drop(w, el, P, M)
+        assert n == 0 and np.array_equal(out, w) and share == 0.0
+    # a zero weight is never a candidate; P = 0 leaves every positive rank eligible
+    out, n, _, _ = oracle.route_drop(w, np.ones(5), 0, 10)
+    assert n == 1 and out[3] == 0 and out[4] == 0 and np.array_equal(out[:3], w[:3])
+
+
+def test_drop_rule_stops_at_the_first_route_that_does_not_fit():
+    # candidates ascending: 0.02, 0.05, 0.06; 10% of 1.0 admits 0.02 and 0.05 (0.07)
+    # but not 0.06 (0.13); the scan stops there even though nothing smaller is left
+    w = _w32(0.6, 0.27, 0.05, 0.06, 0.02)
+    out, n, share, _ = oracle.route_drop(w, np.ones(5), 20, 10)
+    assert n == 2 and out[4] == 0 and out[2] == 0 and out[3] == w[3] and abs(share - 0.07) < 1e-6
+
+
+def test_route_weight_kinds_closed_forms():
+    assert oracle.route_weights(oracle.ROUTER_SIGMOID, [0.0])[0] == 0.5
+    a = 1.7
+    w = oracle.route_weights(oracle.ROUTER_SIGMOID, [a, -a])
+    assert abs(w[0] - 1 / (1 + math.exp(-a))) < 1e-15 and abs(w[0] + w[1] - 1.0) < 1e-15
+    # sigmoid(a) + sigmoid(-a) = 1, so the normalised pair equals the plain sigmoid
+    wn = oracle.route_weights(oracle.ROUTER_SIGMOID_NORM, [a, -a])
+    assert np.allclose(wn, w, rtol=0, atol=1e-15)
+    assert oracle.route_weights(oracle.ROUTER_SIGMOID_NORM, [0.3])[0] == 1.0
+    # softmax over the K chosen = the full softmax renormalised over them (orc_topk)
+    rng = np.random.default_rng(20)
+    l = rng.standard_normal((1, 12))
+    ids, wt, _ = oracle.topk(l, 4)
+    ws = oracle.route_weights(oracle.ROUTER_SOFTMAX, l[0, ids[0]])
+    np.testing.assert_allclose(ws, wt[0], rtol=1e-14, atol=1e-15)
+
+
+def test_scaled_router_input():
+    rng = np.random.default_rng(21)
+    T, H, E = 3, 32, 5
+    x = rng.standard_normal((T, H))
+    Wr = rng.standard_normal((E, H))
+    b = rng.standard_normal(E)
+    base = oracle.router_logits(x, Wr, b)
+    assert np.array_equal(oracle.router_logits_scaled(x, Wr, np.ones(H), b), base)
+    two = oracle.router_logits_scaled(x, Wr, np.full(H, 2.0), b)
+    np.testing.assert_allclose(two - b, 2.0 * (base - b), rtol=1e-14, atol=1e-13)
+    j = 7
+    onehot = np.zeros(H)
+    onehot[j] = 1.0
+    np.testing.assert_allclose(oracle.router_logits_scaled(x, Wr, onehot), np.outer(x[:, j], Wr[:, j]),
+                               rtol=1e-15, atol=1e-15)
+
+
+def test_layer_down_scale_and_router_kinds():
+    rng = np.random.default_rng(22)
+    kind, zp, H, E, K, F = Q4, 8, 64, 6, 3, 32
+    experts, params = _selector_layer(kind, zp, H, E, F, rng)
+    sh_idx = rng.permutation(H)[:F]
+    shared = selector_expert(kind, zp, H, F, sh_idx, sh_idx, sh_idx, 9, 9, 10)
+    Wr = rng.standard_normal((E, H)) * 0.3
+    x = rng.standard_normal((4, H))
+    s_e = np.array([0.5, 2.0, 0.0, 1.5, 3.0, 1.0])
+    for rk in (oracle.ROUTER_SOFTMAX, oracle.ROUTER_SIGMOID, oracle.ROUTER_SIGMOID_NORM):
+        r = oracle.layer_forward_routed(kind, zp, H, E, K, F, Wr, None, experts, x, shared=shared, F_shared=F,
+                                        router_kind=rk, down_scale=s_e)
+        assert r["status"] == 0
+        logits = x @ Wr.T
+        for t in range(4):
+            order = sorted(range(E), key=lambda e: (-logits[t, e], e))[:K]
+            assert list(r["ids"][t]) == order
+            l = logits[t, order]
+            if rk == oracle.ROUTER_SOFTMAX:
+                w = scipy.special.softmax(l)
+            else:
+                w = 1 / (1 + np.exp(-l))
+                if rk == oracle.ROUTER_SIGMOID_NORM:
+                    w = w / w.sum()
+            want = _selector_out(x[t], (sh_idx, sh_idx, sh_idx, 2))
+            for k, e in enumerate(order):
+                want = want + w[k] * s_e[e] * _selector_out(x[t], params[e])
+            np.testing.assert_allclose(r["y"][t], want, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(r["w"][t], w * s_e[order], rtol=1e-14, atol=1e-15)
+
+
+def test_layer_drop_removes_exactly_the_dropped_routes():
+    rng = np.random.default_rng(23)
+    kind, zp, H, E, K, F = Q4, 8, 64, 8, 4, 32
+    experts, params = _selector_layer(kind, zp, H, E, F, rng)
+    Wr = rng.standard_normal((E, H)) * 0.3
+    x = rng.standard_normal((6, H))
+    el = np.array([1, 0, 1, 1, 0, 1, 1, 1], dtype=np.uint8)
+    r = oracle.layer_forward_routed(kind, zp, H, E, K, F, Wr, None, experts, x, drop_eligible=el,
+                                    drop_protect_pct=50, drop_mass_pct=30)
+    base = oracle.layer_forward(kind, zp, H, E, K, F, Wr, None, experts, x)
+    for t in range(6):
+        w32 = base["w"][t].astype(np.float32)
+        want_w, n, share, _ = oracle.route_drop(w32, el[base["ids"][t]], 50, 30)
+        assert r["omitted"][t] == share
+        want = np.zeros(H)
+        for k, e in enumerate(base["ids"][t]):
+            if want_w[k] != 0:
+                want += base["w"][t, k] * _selector_out(x[t], params[e])
+        np.testing.assert_allclose(r["y"][t], want, rtol=1e-12, atol=1e-12)
+    # the kept weights are not renormalised (softmax over the K chosen and the
+    # renormalised full softmax agree to rounding)
+    kept = r["w"] != 0
+    assert kept.sum() < kept.size
+    np.testing.assert_allclose(r["w"][kept], base["w"][kept], rtol=1e-14, atol=0)
