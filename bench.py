@@ -411,8 +411,8 @@ def main():
     # kernels of ours per step: the persistent path runs the whole 48-layer chain as
     # one cooperative kernel (plus a memset of its barrier words); the multi-kernel
     # path runs rmsnorm, router, top-k, bucket, plan, gate/up, down, combine per layer
-    # the persistent kernel runs up to 32 layers per cooperative launch
-    launches_per_step = -(-args.layers // 32) if r["path"] == "persistent" else 8 * args.layers
+    # the persistent kernel runs up to 48 layers per cooperative launch
+    launches_per_step = -(-args.layers // 48) if r["path"] == "persistent" else 8 * args.layers
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": n_gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms"] / args.steps, "higher_is_better": True,

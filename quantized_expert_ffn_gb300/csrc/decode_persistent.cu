@@ -64,7 +64,6 @@ struct alignas(16) Plan {
     float wsum[kMaxTok][kNormWarps];      // RMSNorm warp sums
     unsigned long long sel[kMaxTok][32];  // chosen keys per token, rank order
     float wex[kMaxTok][32];               // route-weight scratch per token
-    int wix[kMaxTok][64];
     uint64_t ring_bar[kPersistThreads / 32][8];  // weight-ring mbarriers per warp
     uint64_t rbar;                               // router-row copies
 };
@@ -327,7 +326,10 @@ __device__ void topk_sort_merge(const float *logits, int T, int E, unsigned long
     if (tid < T * 32) sel[tid >> 5][tid & 31] = lists[(size_t)(tid >> 5) * nch * 32 + (tid & 31)];
 }
 
-template <int KIND, bool XF32>
+// OPTS: some layer of the launch has a router scale or non-default route options;
+// without them the kernel carries none of that code (it costs the serial steps
+// measurable time even when skipped)
+template <int KIND, bool XF32, bool OPTS>
 __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_constant__ PersistArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ Plan s;
@@ -436,7 +438,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                     load_w8<float>(reinterpret_cast<const float *>(a.x) + (size_t)t * H + h, v);
                 else
                     bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xs + (size_t)t * ldx + h), v);
-                if (rscale) {
+                if (OPTS && rscale) {
                     // the scaled router input x_h * s_h, rounded to fp32
                     float sc[8];
                     load_w8<float>(rscale + h, sc);
@@ -581,10 +583,13 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                 float wk;
                 if (bad) {
                     wk = __int_as_float(0x7fc00000);
-                    if (lane == 0 && cta == 0 && Ly.route.omitted) Ly.route.omitted[t] = 0.f;
-                } else {
-                    wk = route_weight(Ly.route, sv, m, si, K, lane, s.wex[t], s.wix[t],
+                    if (OPTS && lane == 0 && cta == 0 && Ly.route.omitted) Ly.route.omitted[t] = 0.f;
+                } else if constexpr (OPTS) {
+                    wk = route_weight(Ly.route, sv, m, si, K, lane, s.wex[t],
+                                      reinterpret_cast<int *>(u_region) + t * 64,
                                       cta == 0 ? Ly.route.omitted : nullptr, t);
+                } else {
+                    wk = topk_weight_smem(sv, m, K, lane, s.wex[t]);
                 }
                 if (lane < K) {
                     s.ids[t * K + lane] = si;
@@ -1083,11 +1088,19 @@ PersistGeom persist_geom(int kind, int T, int H, int E, int K, int F, int F_shar
 }
 
 int launch_decode_persistent(const PersistArgs &a, int G, cudaStream_t s) {
+    bool opts = false;
+    for (int l = 0; l < a.n_layers; ++l) {
+        const PersistLayer &L = a.layers[l];
+        opts |= L.router_scale != nullptr || L.route.kind != MOE_ROUTER_SOFTMAX || L.route.down_scale != nullptr ||
+                L.route.drop_eligible != nullptr || L.route.omitted != nullptr;
+    }
     const void *kern;
+#define MOE_PICK(KD, XF) (opts ? (const void *)k_decode<KD, XF, true> : (const void *)k_decode<KD, XF, false>)
     if (a.L.kind == MOE_Q2_64)
-        kern = a.x_f32 ? (const void *)k_decode<MOE_Q2_64, true> : (const void *)k_decode<MOE_Q2_64, false>;
+        kern = a.x_f32 ? MOE_PICK(MOE_Q2_64, true) : MOE_PICK(MOE_Q2_64, false);
     else
-        kern = a.x_f32 ? (const void *)k_decode<MOE_Q4_32, true> : (const void *)k_decode<MOE_Q4_32, false>;
+        kern = a.x_f32 ? MOE_PICK(MOE_Q4_32, true) : MOE_PICK(MOE_Q4_32, false);
+#undef MOE_PICK
     MOE_CUDA_TRY(cudaMemsetAsync(a.bar, 0, (size_t)a.sync_words * sizeof(unsigned), s));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
@@ -1116,17 +1129,19 @@ int persist_max_ctas(int smem_bytes, int *G) {
     int per_sm = 0, per_sm2 = 0;
     const int dyn = smem_bytes - (int)sizeof(Plan);
     MOE_CUDA_TRY(
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode<MOE_Q2_64, false>, kPersistThreads, dyn));
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode<MOE_Q2_64, false, true>, kPersistThreads, dyn));
     MOE_CUDA_TRY(
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm2, k_decode<MOE_Q4_32, false>, kPersistThreads, dyn));
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm2, k_decode<MOE_Q4_32, false, true>, kPersistThreads, dyn));
     if (per_sm2 < per_sm) per_sm = per_sm2;
     *G = per_sm >= 1 ? sms : 0;
     return MOE_OK;
 }
 
 int init_persist_attributes(int max_smem) {
-    const void *ks[] = {(const void *)k_decode<MOE_Q2_64, true>, (const void *)k_decode<MOE_Q2_64, false>,
-                        (const void *)k_decode<MOE_Q4_32, true>, (const void *)k_decode<MOE_Q4_32, false>};
+    const void *ks[] = {(const void *)k_decode<MOE_Q2_64, true, false>, (const void *)k_decode<MOE_Q2_64, false, false>,
+                        (const void *)k_decode<MOE_Q4_32, true, false>, (const void *)k_decode<MOE_Q4_32, false, false>,
+                        (const void *)k_decode<MOE_Q2_64, true, true>,  (const void *)k_decode<MOE_Q2_64, false, true>,
+                        (const void *)k_decode<MOE_Q4_32, true, true>,  (const void *)k_decode<MOE_Q4_32, false, true>};
     for (const void *k : ks) {
         int rc = set_max_dynamic_smem(k, max_smem);
         if (rc) return rc;

@@ -7,7 +7,7 @@ namespace moe {
 
 constexpr int kPersistThreads = 512;
 constexpr int kMaxTok = 8;             // tokens per window on this path
-constexpr int kMaxPersistLayers = 32;  // layers per launch (longer stacks: several launches)
+constexpr int kMaxPersistLayers = 48;  // layers per launch (longer stacks: several launches)
 constexpr size_t kRedBytes = (kPersistThreads / 32) * 32 * 8 * sizeof(float);
 constexpr int kMaxRingBytes = 16384;   // weight ring per warp (bytes)
 constexpr int kCandCap = 128;          // top-K candidates per token kept by the threshold pass
@@ -62,7 +62,7 @@ struct PersistArgs {
     uint32_t *status;
     PersistLayer layers[kMaxPersistLayers];
 };
-static_assert(sizeof(PersistArgs) <= 4096, "kernel parameters must fit in 4 KB");
+static_assert(sizeof(PersistArgs) <= 32764, "kernel parameters must fit in 32,764 bytes");
 
 PersistGeom persist_geom(int kind, int T, int H, int E, int K, int F, int F_shared, int wr_bytes, int x_f32, int G,
                          size_t max_smem);
