@@ -347,6 +347,99 @@ MOE_API int moe_layer_forward_static(moe_ctx *ctx, const moe_layer_desc *desc, c
 MOE_API int moe_rmsnorm_bf16(moe_ctx *ctx, const float *x, int T, int H, float eps, void *out,
                      moe_stream_t stream);
 
+/* ------------------------------------------------------------ residency policies
+ *
+ * Host-side replacement policies that decide which (layer, expert) pairs stay
+ * resident in a pool of `capacity` slots, fed with the routed ids of each layer
+ * and token, and a driver that applies their decisions to a moe_slots pool
+ * through moe_slot_load / moe_slot_evict (publish after the copy lands). Pure
+ * host code: no GPU work except in moe_policy_apply.
+ *
+ *   MOE_POLICY_LRU (kairos README, "Decode, 2026-09-28/29"): on a routing event
+ *     (the ids one token routes to in one layer) every resident id of the event
+ *     becomes most recently used, in event order; then each missing id, in event
+ *     order, is loaded, evicting the least recently used entry that is not in
+ *     the event when the pool is full.
+ *   MOE_POLICY_DECAYED_FREQ (kairos README, "2026-09-29: which experts to
+ *     keep"): every entry has a score that halves every `half_life` tokens and
+ *     gains 1 per access; misses load as for LRU, and the victim is the entry
+ *     of lowest decayed score among those not in the event and not accessed in
+ *     the last `recency_guard` tokens (all guarded: among those not in the
+ *     event); equal scores go to the least recently used, then the lower
+ *     (layer, expert).
+ *   MOE_POLICY_LFU_SWAP (Strata article, "The cache's replacement rule"): misses
+ *     do not load; every access adds 1 to a float counter of its pair; at the
+ *     end of every `swap_every`-th token, per layer, the hottest missing experts
+ *     (counter >= min_count) pair with the coldest resident ones (hottest first,
+ *     coldest first; equal counters to the lower expert) and swap while the
+ *     newcomer's counter is at least the resident's + margin; across layers only
+ *     the max_swaps largest gains (newcomer - resident; equal gains to the lower
+ *     layer, then the earlier pair) are kept. After every token every counter is
+ *     multiplied by `decay`. Swapped-in experts count as resident from the next
+ *     token (their copy lands first).
+ *
+ * The experts of the event being served are never evicted. Capacity counts
+ * entries over all layers (one pool, like moe_slots). */
+typedef enum { MOE_POLICY_LRU = 0, MOE_POLICY_DECAYED_FREQ = 1, MOE_POLICY_LFU_SWAP = 2 } moe_policy_kind;
+
+typedef struct {
+    int kind;           /* moe_policy_kind */
+    int capacity;       /* resident entries, >= 1 */
+    double half_life;   /* DECAYED_FREQ: tokens (32 in the README) */
+    int recency_guard;  /* DECAYED_FREQ: tokens (2) */
+    float decay;        /* LFU_SWAP: counter factor per token (0.7) */
+    float margin;       /* LFU_SWAP: hysteresis (1.5) */
+    float min_count;    /* LFU_SWAP: newcomer threshold (2.0) */
+    int swap_every;     /* LFU_SWAP: tokens between swap rounds (4) */
+    int max_swaps;      /* LFU_SWAP: swaps per round over all layers (96) */
+} moe_policy_params;
+
+typedef struct moe_policy moe_policy;
+
+/* A policy over n_layers x n_experts pairs with an empty pool. */
+MOE_API int moe_policy_create(const moe_policy_params *params, int n_layers, int n_experts,
+                              moe_policy **out);
+MOE_API int moe_policy_destroy(moe_policy *p);
+
+/* Make the listed pairs resident without counting accesses (a shipped profile),
+ * in list order, until the pool is full; returns how many were placed in *n_placed. */
+MOE_API int moe_policy_seed(moe_policy *p, const int32_t *layers, const int32_t *experts, int n,
+                            int *n_placed);
+
+/* One routing event: `ids` [n] (host) routed by the current token in `layer`.
+ * hit [n] (host, may be NULL) gets 1 for ids resident before the event. Loads
+ * decided now (LRU, DECAYED_FREQ) are appended to the plan: load_expert [n]
+ * (experts of `layer` to load, event order) with the evicted pairs
+ * evict_layer / evict_expert [n] (-1 where no eviction was needed); *n_loads
+ * their number. Duplicate ids in one event count once. */
+MOE_API int moe_policy_route(moe_policy *p, int layer, const int32_t *ids, int n, uint8_t *hit,
+                             int32_t *load_expert, int32_t *evict_layer, int32_t *evict_expert,
+                             int *n_loads);
+
+/* End of the current token. LFU_SWAP makes its swap round's decisions and, with
+ * plan buffers, returns them (at most cap swaps are made then): load_layer /
+ * load_expert with evict_layer / evict_expert, *n_swaps (NULL buffers: a replay
+ * that only updates residency). The other policies advance their clock and
+ * return no swaps. */
+MOE_API int moe_policy_end_token(moe_policy *p, int32_t *load_layer, int32_t *load_expert,
+                                 int32_t *evict_layer, int32_t *evict_expert, int cap, int *n_swaps);
+
+/* Residency of one pair (1 / 0) and the pool's occupancy. */
+MOE_API int moe_policy_resident(const moe_policy *p, int layer, int expert, int *resident);
+MOE_API int moe_policy_count(const moe_policy *p, int *n_resident);
+
+/* Apply decisions to a slot pool on `stream`: for i in 0..n-1, evict
+ * (evict_layer[i], evict_expert[i]) when evict_layer[i] >= 0, then load
+ * (load_layer[i], load_expert[i]) from blobs[load_layer[i] * n_experts +
+ * load_expert[i]] (host pointers to canonical blobs of nbytes; pinned memory
+ * keeps the copies asynchronous). Each table entry is published only after its
+ * copy lands (moe_slot_load); work enqueued earlier on `stream` still sees an
+ * evicted expert, so a layer's own experts are never taken from under it. */
+MOE_API int moe_policy_apply(moe_slots *slots, int n_experts, const void *const *blobs, size_t nbytes,
+                             const int32_t *load_layer, const int32_t *load_expert,
+                             const int32_t *evict_layer, const int32_t *evict_expert, int n,
+                             moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

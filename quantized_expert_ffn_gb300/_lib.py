@@ -43,6 +43,14 @@ class LayerDesc(ctypes.Structure):
                 ("drop_mass_pct", ctypes.c_int), ("omitted_out", ctypes.c_void_p)]
 
 
+class PolicyParams(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("capacity", ctypes.c_int), ("half_life", ctypes.c_double),
+                ("recency_guard", ctypes.c_int), ("decay", ctypes.c_float), ("margin", ctypes.c_float),
+                ("min_count", ctypes.c_float), ("swap_every", ctypes.c_int), ("max_swaps", ctypes.c_int)]
+
+
+POLICY_LRU, POLICY_DECAYED_FREQ, POLICY_LFU_SWAP = 0, 1, 2
+
 _lib = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -73,6 +81,14 @@ _SIGS = {
                           _P],
     "moe_stack_forward_host": [_P, ctypes.POINTER(LayerDesc), _I, _P, _I, ctypes.c_float, _P, _SZ, _P],
     "moe_rmsnorm_bf16": [_P, _P, _I, _I, ctypes.c_float, _P, _P],
+    "moe_policy_create": [ctypes.POINTER(PolicyParams), _I, _I, ctypes.POINTER(_P)],
+    "moe_policy_destroy": [_P],
+    "moe_policy_seed": [_P, _P, _P, _I, ctypes.POINTER(_I)],
+    "moe_policy_route": [_P, _I, _P, _I, _P, _P, _P, _P, ctypes.POINTER(_I)],
+    "moe_policy_end_token": [_P, _P, _P, _P, _P, _I, ctypes.POINTER(_I)],
+    "moe_policy_resident": [_P, _I, _I, ctypes.POINTER(_I)],
+    "moe_policy_count": [_P, ctypes.POINTER(_I)],
+    "moe_policy_apply": [_P, _I, _P, _SZ, _P, _P, _P, _P, _I, _P],
 }
 
 
@@ -283,3 +299,86 @@ def moe_stack_forward_host(ctx: int, descs, resid_host, eps: float, ws, stream=N
 def moe_rmsnorm_bf16(ctx: int, x, eps: float, out, stream=None):
     T, H = x.shape
     _check(load().moe_rmsnorm_bf16(ctx, _ptr(x), T, H, eps, _ptr(out), _stream(stream)))
+
+
+# ------------------------------------------------------------ residency policies
+# (host arrays: numpy; marshalling only)
+
+def policy_params(kind: int, capacity: int, half_life: float = 32.0, recency_guard: int = 2, decay: float = 0.7,
+                  margin: float = 1.5, min_count: float = 2.0, swap_every: int = 4,
+                  max_swaps: int = 96) -> PolicyParams:
+    return PolicyParams(kind, capacity, half_life, recency_guard, decay, margin, min_count, swap_every, max_swaps)
+
+
+def _np_ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+class Policy:
+    """A moe_policy handle over n_layers x n_experts pairs."""
+
+    def __init__(self, params: PolicyParams, n_layers: int, n_experts: int):
+        import numpy as np
+        self._np = np
+        h = _P()
+        _check(load().moe_policy_create(ctypes.byref(params), n_layers, n_experts, ctypes.byref(h)))
+        self.h = h.value
+        self.n_layers, self.n_experts = n_layers, n_experts
+        self.cap = max(params.max_swaps, 1)
+
+    def seed(self, layers, experts) -> int:
+        np = self._np
+        l = np.ascontiguousarray(layers, dtype=np.int32)
+        e = np.ascontiguousarray(experts, dtype=np.int32)
+        out = _I()
+        _check(load().moe_policy_seed(self.h, _np_ptr(l), _np_ptr(e), l.size, ctypes.byref(out)))
+        return out.value
+
+    def route(self, layer: int, ids):
+        """Returns (hit [n] uint8, loads [m] int32, evict_layer [m], evict_expert [m])."""
+        np = self._np
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        n = ids.size
+        hit = np.zeros(n, dtype=np.uint8)
+        le = np.zeros(max(n, 1), dtype=np.int32)
+        el = np.zeros(max(n, 1), dtype=np.int32)
+        ee = np.zeros(max(n, 1), dtype=np.int32)
+        m = _I()
+        _check(load().moe_policy_route(self.h, layer, _np_ptr(ids), n, _np_ptr(hit), _np_ptr(le), _np_ptr(el),
+                                       _np_ptr(ee), ctypes.byref(m)))
+        k = m.value
+        return hit, le[:k].copy(), el[:k].copy(), ee[:k].copy()
+
+    def end_token(self, plan: bool = True):
+        """Returns (load_layer, load_expert, evict_layer, evict_expert) of the swaps made."""
+        np = self._np
+        bufs = [np.zeros(self.cap, dtype=np.int32) for _ in range(4)] if plan else [None] * 4
+        m = _I()
+        _check(load().moe_policy_end_token(self.h, *[_np_ptr(b) for b in bufs], self.cap, ctypes.byref(m)))
+        if not plan:
+            return None
+        return tuple(b[:m.value].copy() for b in bufs)
+
+    def resident(self, layer: int, expert: int) -> bool:
+        out = _I()
+        _check(load().moe_policy_resident(self.h, layer, expert, ctypes.byref(out)))
+        return bool(out.value)
+
+    def count(self) -> int:
+        out = _I()
+        _check(load().moe_policy_count(self.h, ctypes.byref(out)))
+        return out.value
+
+    def close(self):
+        if self.h:
+            load().moe_policy_destroy(self.h)
+            self.h = None
+
+
+def moe_policy_apply(slots: int, n_experts: int, blob_ptrs, nbytes: int, load_layer, load_expert, evict_layer,
+                     evict_expert, stream=None):
+    import numpy as np
+    bp = np.ascontiguousarray(blob_ptrs, dtype=np.uint64)
+    arrs = [np.ascontiguousarray(a, dtype=np.int32) for a in (load_layer, load_expert, evict_layer, evict_expert)]
+    _check(load().moe_policy_apply(slots, n_experts, _np_ptr(bp), nbytes, *[_np_ptr(a) for a in arrs],
+                                   arrs[0].size, _stream(stream)))

@@ -1,0 +1,311 @@
+// residency.cu -- host-side replacement policies for the expert slot pool and the
+// driver that applies their decisions (moe_policy_* in moe.h). Host code only: no
+// kernel lives here; moe_policy_apply enqueues through moe_slot_evict / moe_slot_load.
+//
+// kairos-engine README, "Decode, 2026-09-28/29" (an LRU cache of experts; resolving
+// a layer stamps its slots most recently used so the layer cannot evict its own
+// experts) and "2026-09-29: which experts to keep" (decayed frequency with a
+// 32-token half-life and a 2-token recency guard); Strata article, "The cache's
+// replacement rule" (per-layer float counters, swaps of the hottest missing against
+// the coldest resident experts with a 1.5 hysteresis and a threshold of 2, at most
+// 96 swaps per round, counters x 0.7 per round).
+#include <algorithm>
+#include <cmath>
+#include <vector>
+
+#include "moe_internal.cuh"
+
+struct moe_policy {
+    moe_policy_params pr;
+    int L = 0, E = 0, n = 0;      // layers, experts, pairs
+    std::vector<uint8_t> res;     // resident flag per pair
+    std::vector<uint8_t> mark;    // pair is in the event being served
+    int n_res = 0;
+    // LRU order: doubly linked list of resident pairs, head = most recent
+    std::vector<int> prev, next;
+    int head = -1, tail = -1;
+    // decayed frequency
+    std::vector<double> score;
+    std::vector<long long> tau, last;  // token of the score's last update / last access (-1: never)
+    std::vector<unsigned long long> stamp;  // access order (0: never)
+    unsigned long long clock = 0;
+    double f = 1.0;  // score factor per token, 2^(-1 / half_life)
+    // LFU with swaps
+    std::vector<float> cnt;
+    long long token = 0;
+};
+
+namespace {
+
+using moe::set_error;
+
+void lru_unlink(moe_policy *p, int k) {
+    if (p->prev[k] >= 0) p->next[p->prev[k]] = p->next[k];
+    else p->head = p->next[k];
+    if (p->next[k] >= 0) p->prev[p->next[k]] = p->prev[k];
+    else p->tail = p->prev[k];
+    p->prev[k] = p->next[k] = -1;
+}
+
+void lru_push_front(moe_policy *p, int k) {
+    p->prev[k] = -1;
+    p->next[k] = p->head;
+    if (p->head >= 0) p->prev[p->head] = k;
+    p->head = k;
+    if (p->tail < 0) p->tail = k;
+}
+
+void lru_push_back(moe_policy *p, int k) {
+    p->next[k] = -1;
+    p->prev[k] = p->tail;
+    if (p->tail >= 0) p->next[p->tail] = k;
+    p->tail = k;
+    if (p->head < 0) p->head = k;
+}
+
+void make_resident(moe_policy *p, int k) {
+    p->res[k] = 1;
+    ++p->n_res;
+    if (p->pr.kind == MOE_POLICY_LRU) lru_push_front(p, k);
+}
+
+void make_absent(moe_policy *p, int k) {
+    p->res[k] = 0;
+    --p->n_res;
+    if (p->pr.kind == MOE_POLICY_LRU) lru_unlink(p, k);
+}
+
+double decayed(const moe_policy *p, int k) { return p->score[k] * std::pow(p->f, (double)(p->token - p->tau[k])); }
+
+// Victim for a load, or -1: never a pair of the event being served.
+int pick_victim(const moe_policy *p) {
+    if (p->pr.kind == MOE_POLICY_LRU) {
+        for (int k = p->tail; k >= 0; k = p->prev[k])
+            if (!p->mark[k]) return k;
+        return -1;
+    }
+    // decayed frequency: lowest decayed score; equal scores to the least recently
+    // used, then the lower pair; first among entries outside the recency guard
+    for (int guarded = 1; guarded >= 0; --guarded) {
+        int best = -1;
+        double bs = 0.0;
+        for (int k = 0; k < p->n; ++k) {
+            if (!p->res[k] || p->mark[k]) continue;
+            if (guarded && p->last[k] >= 0 && p->token - p->last[k] < p->pr.recency_guard) continue;
+            const double s = decayed(p, k);
+            if (best < 0 || s < bs || (s == bs && p->stamp[k] < p->stamp[best])) {
+                best = k;
+                bs = s;
+            }
+        }
+        if (best >= 0) return best;
+    }
+    return -1;
+}
+
+}  // namespace
+
+extern "C" {
+
+MOE_API int moe_policy_create(const moe_policy_params *params, int n_layers, int n_experts, moe_policy **out) {
+    if (!params || !out) return set_error(MOE_ERR_ARG, "null argument");
+    const moe_policy_params &q = *params;
+    if (q.kind < MOE_POLICY_LRU || q.kind > MOE_POLICY_LFU_SWAP) return set_error(MOE_ERR_ARG, "unknown policy %d", q.kind);
+    if (n_layers < 1 || n_experts < 1 || (long long)n_layers * n_experts > (1LL << 26))
+        return set_error(MOE_ERR_SHAPE, "n_layers=%d n_experts=%d", n_layers, n_experts);
+    if (q.capacity < 1) return set_error(MOE_ERR_ARG, "capacity %d < 1", q.capacity);
+    if (q.kind == MOE_POLICY_DECAYED_FREQ && !(q.half_life > 0.0))
+        return set_error(MOE_ERR_ARG, "half_life must be positive");
+    if (q.kind == MOE_POLICY_DECAYED_FREQ && q.recency_guard < 0) return set_error(MOE_ERR_ARG, "recency_guard < 0");
+    if (q.kind == MOE_POLICY_LFU_SWAP && (q.swap_every < 1 || q.max_swaps < 0))
+        return set_error(MOE_ERR_ARG, "swap_every %d / max_swaps %d", q.swap_every, q.max_swaps);
+    moe_policy *p = new moe_policy;
+    p->pr = q;
+    p->L = n_layers;
+    p->E = n_experts;
+    p->n = n_layers * n_experts;
+    p->res.assign(p->n, 0);
+    p->mark.assign(p->n, 0);
+    p->prev.assign(p->n, -1);
+    p->next.assign(p->n, -1);
+    p->score.assign(p->n, 0.0);
+    p->tau.assign(p->n, 0);
+    p->last.assign(p->n, -1);
+    p->stamp.assign(p->n, 0);
+    p->cnt.assign(p->n, 0.f);
+    if (q.kind == MOE_POLICY_DECAYED_FREQ) p->f = std::pow(2.0, -1.0 / q.half_life);
+    *out = p;
+    return MOE_OK;
+}
+
+MOE_API int moe_policy_destroy(moe_policy *p) {
+    delete p;
+    return MOE_OK;
+}
+
+MOE_API int moe_policy_seed(moe_policy *p, const int32_t *layers, const int32_t *experts, int n, int *n_placed) {
+    if (!p || (n > 0 && (!layers || !experts))) return set_error(MOE_ERR_ARG, "null argument");
+    int placed = 0;
+    for (int i = 0; i < n && p->n_res < p->pr.capacity; ++i) {
+        if (layers[i] < 0 || layers[i] >= p->L || experts[i] < 0 || experts[i] >= p->E)
+            return set_error(MOE_ERR_ARG, "pair (%d, %d) out of range", layers[i], experts[i]);
+        const int k = layers[i] * p->E + experts[i];
+        if (p->res[k]) continue;
+        // a profile lists the hottest first: seeded entries are older than any access,
+        // the first listed the most recent of them
+        p->res[k] = 1;
+        ++p->n_res;
+        if (p->pr.kind == MOE_POLICY_LRU) lru_push_back(p, k);
+        ++placed;
+    }
+    if (n_placed) *n_placed = placed;
+    return MOE_OK;
+}
+
+MOE_API int moe_policy_route(moe_policy *p, int layer, const int32_t *ids, int n, uint8_t *hit, int32_t *load_expert,
+                             int32_t *evict_layer, int32_t *evict_expert, int *n_loads) {
+    if (!p || (n > 0 && !ids)) return set_error(MOE_ERR_ARG, "null argument");
+    if (layer < 0 || layer >= p->L) return set_error(MOE_ERR_ARG, "layer %d out of range", layer);
+    for (int i = 0; i < n; ++i)
+        if (ids[i] < 0 || ids[i] >= p->E) return set_error(MOE_ERR_ARG, "expert %d out of range", ids[i]);
+    const bool demand = p->pr.kind != MOE_POLICY_LFU_SWAP;
+    if (demand && (!load_expert || !evict_layer || !evict_expert || !n_loads))
+        return set_error(MOE_ERR_ARG, "null plan buffers");
+    // the event's distinct pairs, in event order
+    std::vector<int> ev;
+    ev.reserve(n);
+    for (int i = 0; i < n; ++i) {
+        const int k = layer * p->E + ids[i];
+        if (hit) hit[i] = p->res[k];
+        if (p->mark[k]) continue;
+        p->mark[k] = 1;
+        ev.push_back(k);
+    }
+    int nl = 0;
+    if (p->pr.kind == MOE_POLICY_LFU_SWAP) {
+        for (int k : ev) p->cnt[k] += 1.0f;
+    } else {
+        for (int k : ev) {
+            if (p->pr.kind == MOE_POLICY_LRU) {
+                if (p->res[k]) {
+                    lru_unlink(p, k);
+                    lru_push_front(p, k);
+                }
+            } else {
+                p->score[k] = p->score[k] * std::pow(p->f, (double)(p->token - p->tau[k])) + 1.0;
+                p->tau[k] = p->token;
+                p->last[k] = p->token;
+                p->stamp[k] = ++p->clock;
+            }
+        }
+        for (int k : ev) {
+            if (p->res[k]) continue;
+            int victim = -1;
+            if (p->n_res >= p->pr.capacity) {
+                victim = pick_victim(p);
+                if (victim < 0) continue;  // the pool holds only this event's experts
+                make_absent(p, victim);
+            }
+            make_resident(p, k);
+            load_expert[nl] = k % p->E;
+            evict_layer[nl] = victim < 0 ? -1 : victim / p->E;
+            evict_expert[nl] = victim < 0 ? -1 : victim % p->E;
+            ++nl;
+        }
+    }
+    for (int k : ev) p->mark[k] = 0;
+    if (n_loads) *n_loads = nl;
+    return MOE_OK;
+}
+
+MOE_API int moe_policy_end_token(moe_policy *p, int32_t *load_layer, int32_t *load_expert, int32_t *evict_layer,
+                                 int32_t *evict_expert, int cap, int *n_swaps) {
+    if (!p) return set_error(MOE_ERR_ARG, "null argument");
+    int ns = 0;
+    ++p->token;
+    if (p->pr.kind == MOE_POLICY_LFU_SWAP) {
+        if (p->token % p->pr.swap_every == 0) {
+            struct Swap {
+                float gain;
+                int layer, in, out;
+            };
+            std::vector<Swap> sw;
+            std::vector<std::pair<float, int>> cand, vict;
+            for (int l = 0; l < p->L; ++l) {
+                cand.clear();
+                vict.clear();
+                for (int e = 0; e < p->E; ++e) {
+                    const int k = l * p->E + e;
+                    if (p->res[k]) vict.emplace_back(p->cnt[k], e);
+                    else if (p->cnt[k] >= p->pr.min_count) cand.emplace_back(p->cnt[k], e);
+                }
+                std::sort(cand.begin(), cand.end(), [](const std::pair<float, int> &a, const std::pair<float, int> &b) {
+                    return a.first != b.first ? a.first > b.first : a.second < b.second;
+                });
+                std::sort(vict.begin(), vict.end(), [](const std::pair<float, int> &a, const std::pair<float, int> &b) {
+                    return a.first != b.first ? a.first < b.first : a.second < b.second;
+                });
+                const size_t m = std::min(cand.size(), vict.size());
+                for (size_t i = 0; i < m; ++i) {
+                    if (cand[i].first < vict[i].first + p->pr.margin) break;
+                    sw.push_back(Swap{cand[i].first - vict[i].first, l, cand[i].second, vict[i].second});
+                }
+            }
+            std::stable_sort(sw.begin(), sw.end(), [](const Swap &a, const Swap &b) { return a.gain > b.gain; });
+            // with plan buffers, no more swaps than they hold (every swap made is reported)
+            const bool out = load_layer && load_expert && evict_layer && evict_expert;
+            size_t take = std::min(sw.size(), (size_t)p->pr.max_swaps);
+            if (out) take = std::min(take, (size_t)(cap > 0 ? cap : 0));
+            for (size_t i = 0; i < take; ++i) {
+                const Swap &s = sw[i];
+                make_absent(p, s.layer * p->E + s.out);
+                make_resident(p, s.layer * p->E + s.in);
+                if (out) {
+                    load_layer[i] = s.layer;
+                    load_expert[i] = s.in;
+                    evict_layer[i] = s.layer;
+                    evict_expert[i] = s.out;
+                }
+            }
+            ns = (int)take;
+        }
+        for (float &c : p->cnt) c *= p->pr.decay;
+    }
+    if (n_swaps) *n_swaps = ns;
+    return MOE_OK;
+}
+
+MOE_API int moe_policy_resident(const moe_policy *p, int layer, int expert, int *resident) {
+    if (!p || !resident) return set_error(MOE_ERR_ARG, "null argument");
+    if (layer < 0 || layer >= p->L || expert < 0 || expert >= p->E) return set_error(MOE_ERR_ARG, "pair out of range");
+    *resident = p->res[layer * p->E + expert];
+    return MOE_OK;
+}
+
+MOE_API int moe_policy_count(const moe_policy *p, int *n_resident) {
+    if (!p || !n_resident) return set_error(MOE_ERR_ARG, "null argument");
+    *n_resident = p->n_res;
+    return MOE_OK;
+}
+
+MOE_API int moe_policy_apply(moe_slots *slots, int n_experts, const void *const *blobs, size_t nbytes,
+                             const int32_t *load_layer, const int32_t *load_expert, const int32_t *evict_layer,
+                             const int32_t *evict_expert, int n, moe_stream_t stream) {
+    if (!slots || (n > 0 && (!blobs || !load_layer || !load_expert || !evict_layer || !evict_expert)))
+        return set_error(MOE_ERR_ARG, "null argument");
+    for (int i = 0; i < n; ++i) {
+        if (evict_layer[i] >= 0) {
+            const int rc = moe_slot_evict(slots, evict_layer[i], evict_expert[i], stream);
+            if (rc) return rc;
+        }
+        if (load_layer[i] < 0 || load_expert[i] < 0 || load_expert[i] >= n_experts)
+            return set_error(MOE_ERR_ARG, "load pair (%d, %d) out of range", load_layer[i], load_expert[i]);
+        const void *blob = blobs[(size_t)load_layer[i] * n_experts + load_expert[i]];
+        if (!blob) return set_error(MOE_ERR_ARG, "no blob for (%d, %d)", load_layer[i], load_expert[i]);
+        const int rc = moe_slot_load(slots, load_layer[i], load_expert[i], blob, nbytes, stream);
+        if (rc) return rc;
+    }
+    return MOE_OK;
+}
+
+}  // extern "C"
