@@ -382,3 +382,49 @@ def moe_policy_apply(slots: int, n_experts: int, blob_ptrs, nbytes: int, load_la
     arrs = [np.ascontiguousarray(a, dtype=np.int32) for a in (load_layer, load_expert, evict_layer, evict_expert)]
     _check(load().moe_policy_apply(slots, n_experts, _np_ptr(bp), nbytes, *[_np_ptr(a) for a in arrs],
                                    arrs[0].size, _stream(stream)))
+
+
+# the C names, for callers that hold the handle themselves (Policy wraps these)
+def moe_policy_create(params: PolicyParams, n_layers: int, n_experts: int) -> int:
+    h = _P()
+    _check(load().moe_policy_create(ctypes.byref(params), n_layers, n_experts, ctypes.byref(h)))
+    return h.value
+
+
+def moe_policy_destroy(h: int):
+    _check(load().moe_policy_destroy(h))
+
+
+def moe_policy_seed(h: int, layers, experts) -> int:
+    import numpy as np
+    l = np.ascontiguousarray(layers, dtype=np.int32)
+    e = np.ascontiguousarray(experts, dtype=np.int32)
+    out = _I()
+    _check(load().moe_policy_seed(h, _np_ptr(l), _np_ptr(e), l.size, ctypes.byref(out)))
+    return out.value
+
+
+def moe_policy_route(h: int, layer: int, ids, hit, load_expert, evict_layer, evict_expert) -> int:
+    n = _I()
+    _check(load().moe_policy_route(h, layer, _np_ptr(ids), ids.size, _np_ptr(hit), _np_ptr(load_expert),
+                                   _np_ptr(evict_layer), _np_ptr(evict_expert), ctypes.byref(n)))
+    return n.value
+
+
+def moe_policy_end_token(h: int, load_layer, load_expert, evict_layer, evict_expert, cap: int) -> int:
+    n = _I()
+    _check(load().moe_policy_end_token(h, _np_ptr(load_layer), _np_ptr(load_expert), _np_ptr(evict_layer),
+                                       _np_ptr(evict_expert), cap, ctypes.byref(n)))
+    return n.value
+
+
+def moe_policy_resident(h: int, layer: int, expert: int) -> bool:
+    out = _I()
+    _check(load().moe_policy_resident(h, layer, expert, ctypes.byref(out)))
+    return bool(out.value)
+
+
+def moe_policy_count(h: int) -> int:
+    out = _I()
+    _check(load().moe_policy_count(h, ctypes.byref(out)))
+    return out.value
