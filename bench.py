@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill (T=4096 Gemma-shaped layer) line")
+    ap.add_argument("--no-residency", action="store_true", help="skip the residency-policy replay and load line")
     return ap.parse_args()
 
 
@@ -173,6 +174,79 @@ class Stack:
             self.descs.append(L.layer_desc(self.slots, l, cfg.H, cfg.E, cfg.K, cfg.F, self.Wr[l], self.bias[l]))
         torch.cuda.synchronize()
         del staging
+
+
+def run_residency(L, torch, ctx):
+    """Replay of the residency policies on a sticky Zipf routing trace of the
+    48-layer stack's shape (hit rates with 5, 10 and 20% of the (layer, expert)
+    pairs resident, Belady's ceiling beside them; us_per_event includes the Python
+    call), and the rate at which moe_policy_apply makes experts resident from
+    pinned host memory."""
+    import time
+    import synth.device as sdev
+    from synth import traces
+    E, Ln, K, T_prof, T_rep = 512, 48, 10, 32, 256
+    tr = traces.routing_trace(T_prof + T_rep, Ln, E, K, seed=11)
+    prof = traces.profile_ranking(tr[:T_prof])
+    rep = np.ascontiguousarray(tr[T_prof:])
+    n_ids = T_rep * Ln * K
+    rows = []
+    for frac in (0.05, 0.1, 0.2):
+        cap = int(frac * Ln * E)
+        row = {"capacity": cap, "resident_frac": round(frac, 3)}
+        for name, kind in (("lru", L.POLICY_LRU), ("decayed_freq_hl32_guard2", L.POLICY_DECAYED_FREQ),
+                           ("lfu_swap_0.7_1.5_2_every4_96", L.POLICY_LFU_SWAP)):
+            pol = L.Policy(L.policy_params(kind, cap), Ln, E)
+            pol.seed(*prof)
+            hits = 0
+            t0 = time.perf_counter()
+            for t in range(T_rep):
+                for l in range(Ln):
+                    h = pol.route(l, rep[t, l])[0]
+                    hits += int(h.sum())
+                pol.end_token()
+            dt = time.perf_counter() - t0
+            pol.close()
+            row[name] = {"hit_rate": hits / n_ids, "misses_per_token": (n_ids - hits) / T_rep,
+                         "us_per_event": dt / (T_rep * Ln) * 1e6}
+        bel = L.moe_policy_belady(rep, E, cap, *prof)
+        row["belady"] = {"hit_rate": bel / n_ids, "misses_per_token": (n_ids - bel) / T_rep}
+        rows.append(row)
+    # loads through moe_policy_apply: Q2_0 experts of the stack's shape from pinned host memory
+    cfg = C.CONFIGS["q2_layer"]
+    n = 32
+    eb = cfg.expert_bytes()
+    arena = L.moe_arena_create(ctx, n * ((eb + 255) // 256 * 256) + 4096)
+    slots = L.moe_slots_create(ctx, arena, 1, cfg.E, cfg.kind, cfg.zero_point, cfg.H, cfg.F, n)
+    staging = torch.empty(n * eb, dtype=torch.uint8, device="cuda")
+    sdev.expert_blobs_into(staging, cfg.seed, cfg.tag_expert(0, 0), n, 3 * cfg.matrix_blocks(), cfg.d_lo, cfg.d_hi)
+    host = staging.cpu().pin_memory()
+    ptrs = np.zeros(cfg.E, dtype=np.uint64)
+    ptrs[:n] = host.data_ptr() + np.arange(n, dtype=np.uint64) * np.uint64(eb)
+    zero = np.zeros(n, np.int32)
+    ex = np.arange(n, dtype=np.int32)
+    none = np.full(n, -1, np.int32)
+    stream = torch.cuda.current_stream()
+    L.moe_policy_apply(slots, cfg.E, ptrs, eb, zero, ex, none, none, stream=stream)
+    ms = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        L.moe_policy_apply(slots, cfg.E, ptrs, eb, zero, ex, zero, ex, stream=stream)  # evict + reload each
+        e1.record(stream)
+        stream.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    L.moe_slots_destroy(slots)
+    L.moe_arena_destroy(arena)
+    del staging, host
+    ms_med = float(np.median(ms))
+    return {"trace": f"sticky Zipf(1.1) routing, {Ln} layers x {E} experts, top-{K}, {T_rep} tokens replayed "
+                     f"after a {T_prof}-token profile seeds the pool; adjacent tokens share "
+                     f"{traces.sharing(rep):.0%} of a layer's experts",
+            "replay": rows,
+            "load": {"what": f"{n} Q2_0 experts ({eb:,} B each) evicted and reloaded through moe_policy_apply "
+                             "from pinned host memory (copy, repack, publish)",
+                     "ms": ms_med, "gb_s": n * eb / (ms_med / 1e3) / 1e9}}
 
 
 def run_prefill(L, torch, ctx, steps: int = 20, warmup: int = 3):
@@ -318,13 +392,14 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     pre = None if args.no_prefill else run_prefill(L, torch, ctx)
+    resid_line = None if (args.no_residency or rank != 0) else run_residency(L, torch, ctx)
 
     times = torch.tensor([ms, e2e_ms], device="cuda")
     if world > 1:
         torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
     ms, e2e_ms_max = float(times[0]), float(times[1])
     return dict(ms=ms, e2e_ms=e2e_ms_max, layer_ms=layer_ms, clocks=clocks, status=status, cfg=cfg, path=path,
-                distinct=distinct, prefill=pre)
+                distinct=distinct, prefill=pre, residency=resid_line)
 
 
 # ------------------------------------------------------------------ oracle (CPU)
@@ -451,6 +526,8 @@ def main():
             else "fallback", "frac": tf / bf16_peak,
             "path": {2: "tcgen05 grouped GEMMs", 1: "persistent", 0: "mma.sync"}.get(pre["path"], str(pre["path"])),
             "device_status": pre["status"]}
+    if r.get("residency"):
+        line["residency"] = r["residency"]
     if rank == 0 and not args.no_cpu_baseline:
         rate, done, busy = oracle_sample_rate(10.0, T)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",

@@ -428,6 +428,16 @@ MOE_API int moe_policy_end_token(moe_policy *p, int32_t *load_layer, int32_t *lo
 MOE_API int moe_policy_resident(const moe_policy *p, int layer, int expert, int *resident);
 MOE_API int moe_policy_count(const moe_policy *p, int *n_resident);
 
+/* Offline ceiling for a demand cache (Belady: evict the resident pair whose next
+ * use is farthest away, never one of the event being served) over a recorded
+ * trace: ids [T][n_layers][K] (host; token-major, then layer, events of K ids),
+ * the pool of `capacity` first seeded with the listed pairs (as moe_policy_seed).
+ * *hits gets the number of routed ids found resident (duplicates within an event
+ * count once, as in moe_policy_route). */
+MOE_API int moe_policy_belady(const int32_t *ids, int T, int n_layers, int K, int n_experts, int capacity,
+                              const int32_t *seed_layers, const int32_t *seed_experts, int n_seed,
+                              long long *hits);
+
 /* Apply decisions to a slot pool on `stream`: for i in 0..n-1, evict
  * (evict_layer[i], evict_expert[i]) when evict_layer[i] >= 0, then load
  * (load_layer[i], load_expert[i]) from blobs[load_layer[i] * n_experts +

@@ -89,6 +89,7 @@ _SIGS = {
     "moe_policy_resident": [_P, _I, _I, ctypes.POINTER(_I)],
     "moe_policy_count": [_P, ctypes.POINTER(_I)],
     "moe_policy_apply": [_P, _I, _P, _SZ, _P, _P, _P, _P, _I, _P],
+    "moe_policy_belady": [_P, _I, _I, _I, _I, _I, _P, _P, _I, ctypes.POINTER(ctypes.c_longlong)],
 }
 
 
@@ -427,4 +428,17 @@ def moe_policy_resident(h: int, layer: int, expert: int) -> bool:
 def moe_policy_count(h: int) -> int:
     out = _I()
     _check(load().moe_policy_count(h, ctypes.byref(out)))
+    return out.value
+
+
+def moe_policy_belady(trace, n_experts: int, capacity: int, seed_layers=None, seed_experts=None) -> int:
+    """trace: int32 [T][n_layers][K] (host). Belady's hits with the pool seeded."""
+    import numpy as np
+    tr = np.ascontiguousarray(trace, dtype=np.int32)
+    T, Ln, K = tr.shape
+    sl = None if seed_layers is None else np.ascontiguousarray(seed_layers, dtype=np.int32)
+    se = None if seed_experts is None else np.ascontiguousarray(seed_experts, dtype=np.int32)
+    out = ctypes.c_longlong()
+    _check(load().moe_policy_belady(_np_ptr(tr), T, Ln, K, n_experts, capacity, _np_ptr(sl), _np_ptr(se),
+                                    0 if sl is None else sl.size, ctypes.byref(out)))
     return out.value

@@ -11,6 +11,8 @@
 // 96 swaps per round, counters x 0.7 per round).
 #include <algorithm>
 #include <cmath>
+#include <limits>
+#include <queue>
 #include <vector>
 
 #include "moe_internal.cuh"
@@ -21,6 +23,7 @@ struct moe_policy {
     std::vector<uint8_t> res;     // resident flag per pair
     std::vector<uint8_t> mark;    // pair is in the event being served
     int n_res = 0;
+    std::vector<int> rlist, rpos;  // resident pairs (any order) and each pair's index in it
     // LRU order: doubly linked list of resident pairs, head = most recent
     std::vector<int> prev, next;
     int head = -1, tail = -1;
@@ -30,6 +33,7 @@ struct moe_policy {
     std::vector<unsigned long long> stamp;  // access order (0: never)
     unsigned long long clock = 0;
     double f = 1.0;  // score factor per token, 2^(-1 / half_life)
+    std::vector<double> fpow;  // fpow[d] = pow(f, d), the factor after d tokens
     // LFU with swaps
     std::vector<float> cnt;
     long long token = 0;
@@ -63,22 +67,43 @@ void lru_push_back(moe_policy *p, int k) {
     if (p->head < 0) p->head = k;
 }
 
+void list_add(moe_policy *p, int k) {
+    p->rpos[k] = (int)p->rlist.size();
+    p->rlist.push_back(k);
+}
+
+void list_remove(moe_policy *p, int k) {
+    const int i = p->rpos[k], last = p->rlist.back();
+    p->rlist[i] = last;
+    p->rpos[last] = i;
+    p->rlist.pop_back();
+    p->rpos[k] = -1;
+}
+
 void make_resident(moe_policy *p, int k) {
     p->res[k] = 1;
     ++p->n_res;
+    list_add(p, k);
     if (p->pr.kind == MOE_POLICY_LRU) lru_push_front(p, k);
 }
 
 void make_absent(moe_policy *p, int k) {
     p->res[k] = 0;
     --p->n_res;
+    list_remove(p, k);
     if (p->pr.kind == MOE_POLICY_LRU) lru_unlink(p, k);
 }
 
-double decayed(const moe_policy *p, int k) { return p->score[k] * std::pow(p->f, (double)(p->token - p->tau[k])); }
+// pow(f, d) for d tokens, the same value a direct pow call gives
+double fpow(moe_policy *p, long long d) {
+    while ((long long)p->fpow.size() <= d) p->fpow.push_back(std::pow(p->f, (double)p->fpow.size()));
+    return p->fpow[d];
+}
+
+double decayed(moe_policy *p, int k) { return p->score[k] * fpow(p, p->token - p->tau[k]); }
 
 // Victim for a load, or -1: never a pair of the event being served.
-int pick_victim(const moe_policy *p) {
+int pick_victim(moe_policy *p) {
     if (p->pr.kind == MOE_POLICY_LRU) {
         for (int k = p->tail; k >= 0; k = p->prev[k])
             if (!p->mark[k]) return k;
@@ -89,11 +114,12 @@ int pick_victim(const moe_policy *p) {
     for (int guarded = 1; guarded >= 0; --guarded) {
         int best = -1;
         double bs = 0.0;
-        for (int k = 0; k < p->n; ++k) {
-            if (!p->res[k] || p->mark[k]) continue;
+        for (int k : p->rlist) {
+            if (p->mark[k]) continue;
             if (guarded && p->last[k] >= 0 && p->token - p->last[k] < p->pr.recency_guard) continue;
             const double s = decayed(p, k);
-            if (best < 0 || s < bs || (s == bs && p->stamp[k] < p->stamp[best])) {
+            if (best < 0 || s < bs || (s == bs && (p->stamp[k] < p->stamp[best] ||
+                                                   (p->stamp[k] == p->stamp[best] && k < best)))) {
                 best = k;
                 bs = s;
             }
@@ -133,6 +159,8 @@ MOE_API int moe_policy_create(const moe_policy_params *params, int n_layers, int
     p->last.assign(p->n, -1);
     p->stamp.assign(p->n, 0);
     p->cnt.assign(p->n, 0.f);
+    p->rpos.assign(p->n, -1);
+    p->rlist.reserve(q.capacity);
     if (q.kind == MOE_POLICY_DECAYED_FREQ) p->f = std::pow(2.0, -1.0 / q.half_life);
     *out = p;
     return MOE_OK;
@@ -155,6 +183,7 @@ MOE_API int moe_policy_seed(moe_policy *p, const int32_t *layers, const int32_t 
         // the first listed the most recent of them
         p->res[k] = 1;
         ++p->n_res;
+        list_add(p, k);
         if (p->pr.kind == MOE_POLICY_LRU) lru_push_back(p, k);
         ++placed;
     }
@@ -192,7 +221,7 @@ MOE_API int moe_policy_route(moe_policy *p, int layer, const int32_t *ids, int n
                     lru_push_front(p, k);
                 }
             } else {
-                p->score[k] = p->score[k] * std::pow(p->f, (double)(p->token - p->tau[k])) + 1.0;
+                p->score[k] = p->score[k] * fpow(p, p->token - p->tau[k]) + 1.0;
                 p->tau[k] = p->token;
                 p->last[k] = p->token;
                 p->stamp[k] = ++p->clock;
@@ -285,6 +314,100 @@ MOE_API int moe_policy_resident(const moe_policy *p, int layer, int expert, int 
 MOE_API int moe_policy_count(const moe_policy *p, int *n_resident) {
     if (!p || !n_resident) return set_error(MOE_ERR_ARG, "null argument");
     *n_resident = p->n_res;
+    return MOE_OK;
+}
+
+MOE_API int moe_policy_belady(const int32_t *ids, int T, int n_layers, int K, int n_experts, int capacity,
+                              const int32_t *seed_layers, const int32_t *seed_experts, int n_seed, long long *hits) {
+    if (!hits || (T > 0 && !ids) || (n_seed > 0 && (!seed_layers || !seed_experts)))
+        return set_error(MOE_ERR_ARG, "null argument");
+    if (T < 0 || n_layers < 1 || K < 1 || n_experts < 1 || capacity < 1 ||
+        (long long)n_layers * n_experts > (1LL << 26))
+        return set_error(MOE_ERR_SHAPE, "T=%d n_layers=%d K=%d n_experts=%d capacity=%d", T, n_layers, K, n_experts,
+                         capacity);
+    const long long never = std::numeric_limits<long long>::max();
+    // the events' distinct pairs in order, and each position's next use
+    std::vector<int> seq;
+    std::vector<long long> ev_end;  // end position of each event
+    seq.reserve((size_t)T * n_layers * K);
+    std::vector<int> mark((size_t)n_layers * n_experts, -1);
+    long long ev = 0;
+    for (int t = 0; t < T; ++t)
+        for (int l = 0; l < n_layers; ++l, ++ev) {
+            for (int k = 0; k < K; ++k) {
+                const int e = ids[((size_t)t * n_layers + l) * K + k];
+                if (e < 0 || e >= n_experts) return set_error(MOE_ERR_ARG, "expert %d out of range", e);
+                const int key = l * n_experts + e;
+                if (mark[key] == ev) continue;
+                mark[key] = (int)ev;
+                seq.push_back(key);
+            }
+            ev_end.push_back((long long)seq.size());
+        }
+    const size_t n = seq.size();
+    std::vector<long long> nxt(n), next_use((size_t)n_layers * n_experts, never);
+    for (size_t i = n; i-- > 0;) {
+        nxt[i] = next_use[seq[i]];
+        next_use[seq[i]] = (long long)i;
+    }
+    // next_use now holds each pair's first use
+    std::vector<uint8_t> res((size_t)n_layers * n_experts, 0), in_ev((size_t)n_layers * n_experts, 0);
+    std::priority_queue<std::pair<long long, int>> heap;  // (next use, pair), farthest first
+    int n_res = 0;
+    for (int i = 0; i < n_seed && n_res < capacity; ++i) {
+        const int l = seed_layers[i], e = seed_experts[i];
+        if (l < 0 || l >= n_layers || e < 0 || e >= n_experts) return set_error(MOE_ERR_ARG, "seed pair out of range");
+        const int key = l * n_experts + e;
+        if (res[key]) continue;
+        res[key] = 1;
+        ++n_res;
+        heap.push({next_use[key], key});
+    }
+    long long h = 0;
+    size_t pos = 0;
+    std::vector<std::pair<long long, int>> skipped;
+    for (long long end : ev_end) {
+        const size_t b = pos;
+        for (size_t i = b; i < (size_t)end; ++i) in_ev[seq[i]] = 1;
+        for (size_t i = b; i < (size_t)end; ++i) {
+            const int key = seq[i];
+            if (res[key]) {
+                ++h;
+                next_use[key] = nxt[i];
+                heap.push({nxt[i], key});
+            }
+        }
+        for (size_t i = b; i < (size_t)end; ++i) {
+            const int key = seq[i];
+            if (res[key]) continue;
+            if (n_res >= capacity) {
+                int victim = -1;
+                skipped.clear();
+                while (!heap.empty()) {
+                    const std::pair<long long, int> top = heap.top();
+                    heap.pop();
+                    if (!res[top.second] || next_use[top.second] != top.first) continue;  // stale
+                    if (in_ev[top.second]) {
+                        skipped.push_back(top);
+                        continue;
+                    }
+                    victim = top.second;
+                    break;
+                }
+                for (const auto &sk : skipped) heap.push(sk);
+                if (victim < 0) continue;
+                res[victim] = 0;
+                --n_res;
+            }
+            res[key] = 1;
+            ++n_res;
+            next_use[key] = nxt[i];
+            heap.push({nxt[i], key});
+        }
+        for (size_t i = b; i < (size_t)end; ++i) in_ev[seq[i]] = 0;
+        pos = (size_t)end;
+    }
+    *hits = h;
     return MOE_OK;
 }
 

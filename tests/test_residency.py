@@ -167,3 +167,14 @@ def test_policy_argument_checks():
             p.route(0, [8])
     finally:
         p.close()
+
+
+@pytest.mark.parametrize("seed,cap", [(8, 40), (9, 100), (10, 7)])
+def test_engine_belady_matches_reference(seed, cap):
+    tr = traces.routing_trace(40, 3, 40, 6, seed=seed)
+    prof = traces.profile_ranking(tr[:6])
+    events = [[(l, tr[t, l]) for l in range(3)] for t in range(40)]
+    assert L.moe_policy_belady(tr, 40, cap, *prof) == R.belady_hits(events, cap, list(zip(*prof)))
+    assert L.moe_policy_belady(tr, 40, cap) == R.belady_hits(events, cap)
+    seq = np.array([7, 0, 1, 2, 0, 3, 0, 4, 2, 3, 0, 3, 2], dtype=np.int32).reshape(-1, 1, 1)
+    assert L.moe_policy_belady(seq, 8, 3) == 6
