@@ -144,6 +144,14 @@ MOE_API int moe_ctx_get_option(moe_ctx *ctx, int option, int *value);
  * follows the same rule, so a window routes identically through either entry. */
 #define MOE_OPT_PREFILL_MIN_T 3
 
+/* MOE_OPT_TEST_SKIP_ARRIVAL (default -1, settable, >= -1): a test hook for the
+ * bounded waits. With value v >= 0, in every persistent decode launch CTA 0 leaves
+ * out its arrival at the first grid barrier of layer v of the launch (a signal
+ * that never comes): every CTA's wait at that barrier gives up after about a
+ * second, MOE_STATUS_TIMEOUT is set, the kernel stops and returns, and the context
+ * stays usable (the call's outputs are then undefined). Nothing faults or traps. */
+#define MOE_OPT_TEST_SKIP_ARRIVAL 4
+
 /* Synchronise `stream`, then read and clear the device status bits into *bits.
  * Returns MOE_OK even when bits are set; the caller inspects them. */
 MOE_API int moe_status(moe_ctx *ctx, moe_stream_t stream, uint32_t *bits);

@@ -17,6 +17,7 @@ struct moe_ctx {
     int last_path;    // MOE_OPT_LAST_PATH
     int prefill_min;  // MOE_OPT_PREFILL_MIN_T
     int max_smem;    // opt-in shared memory per block
+    int fault_layer;  // MOE_OPT_TEST_SKIP_ARRIVAL (-1: off)
 };
 
 struct moe_arena {
@@ -393,6 +394,7 @@ int try_persistent(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers, boo
     a.wr_bf16 = d0.wr_dtype == MOE_BF16;
     a.x_f32 = xt == MOE_F32;
     a.eps = eps;
+    a.fault_layer = ctx->fault_layer;
     a.L = s0->layout;
     a.LS = d0.shared ? d0.shared->layout : s0->layout;
     a.un = make_unpack(s0->fmt.zero_point);
@@ -519,7 +521,7 @@ int moe_ctx_create(int device, moe_ctx **out) {
         return set_error(MOE_ERR_CUDA, "no CUDA device %d (%d visible)", device, n);
     DeviceGuard g(device);
     if (!g.ok) return set_error(MOE_ERR_CUDA, "cudaSetDevice(%d) failed", device);
-    moe_ctx *c = new moe_ctx{device, nullptr, 1, 0, 64, 0};
+    moe_ctx *c = new moe_ctx{device, nullptr, 1, 0, 64, 0, -1};
     cudaError_t e = cudaMalloc(&c->d_status, sizeof(uint32_t));
     if (e != cudaSuccess) {
         delete c;
@@ -575,6 +577,11 @@ int moe_ctx_set_option(moe_ctx *ctx, int option, int value) {
         ctx->prefill_min = value;
         return MOE_OK;
     }
+    if (option == MOE_OPT_TEST_SKIP_ARRIVAL) {
+        if (value < -1) return set_error(MOE_ERR_ARG, "MOE_OPT_TEST_SKIP_ARRIVAL must be >= -1, got %d", value);
+        ctx->fault_layer = value;
+        return MOE_OK;
+    }
     return set_error(MOE_ERR_ARG, "unknown option %d", option);
 }
 
@@ -590,6 +597,10 @@ int moe_ctx_get_option(moe_ctx *ctx, int option, int *value) {
     }
     if (option == MOE_OPT_PREFILL_MIN_T) {
         *value = ctx->prefill_min;
+        return MOE_OK;
+    }
+    if (option == MOE_OPT_TEST_SKIP_ARRIVAL) {
+        *value = ctx->fault_layer;
         return MOE_OK;
     }
     return set_error(MOE_ERR_ARG, "unknown option %d", option);

@@ -88,13 +88,16 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // Barrier over all CTAs of the (co-resident) grid. bar[0] counts arrivals
 // monotonically within the launch; bar[1] is the stop word. Returns false when
 // the kernel must stop (this or another CTA gave up waiting).
-__device__ bool grid_sync(unsigned *bar, unsigned &target, uint32_t *status, int *s_flag) {
+// skip_arrival (a test hook, never set by the layer code) leaves this CTA's arrival
+// out, so that every wait on this barrier runs into its time limit.
+__device__ bool grid_sync(unsigned *bar, unsigned &target, uint32_t *status, int *s_flag,
+                          bool skip_arrival = false) {
     target += gridDim.x;
     __syncthreads();
     if (threadIdx.x == 0) {
         // release: every write of this CTA (ordered before by the bar.sync above)
         // is visible before the arrival is
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
+        if (!skip_arrival) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
         const long long t0 = clock64();
         int stop = 0;
         // the stop word is set only by a CTA that gave up, and then the count never
@@ -467,7 +470,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                 if (a.trace_logits) a.trace_logits[((size_t)l * T + t) * E + e] = v;
             }
         }
-        if (!grid_sync(a.bar, target, a.status, s_flag)) break;
+        if (!grid_sync(a.bar, target, a.status, s_flag, a.fault_layer == l && cta == 0)) break;
         // ------------------------------------------------ T: top-K and the plan (every CTA)
         {
             // ord keys of the logits; token rows are padded to Ep (a multiple of 32)

@@ -42,6 +42,7 @@ struct PersistLayer {
 
 struct PersistArgs {
     int n_layers, T, H, E, K, act, stack, wr_bf16, x_f32;
+    int fault_layer;  // test hook: CTA 0 skips its arrival at layer fault_layer's first grid barrier (-1: off)
     float eps;
     QLayout L, LS;
     Unpack un, un_s;

@@ -139,3 +139,42 @@ def test_option_query(torch, ctx):
         L.moe_ctx_set_option(ctx, L.OPT_LAST_PATH, 1)
     with pytest.raises(L.MoeError):
         L.moe_ctx_get_option(ctx, 99)
+
+
+def test_bounded_wait_gives_up_and_the_context_recovers(torch, ctx):
+    # a grid-barrier arrival that never comes (test hook): every wait runs into its
+    # time limit, the kernel returns with MOE_STATUS_TIMEOUT, and the next call on
+    # the same context runs normally
+    import time
+    cfg = C.CONFIGS["q2_stack"]
+    n = 3
+    g = GpuLayers(ctx, cfg, n_layers=n)
+    try:
+        descs = [g.desc(l) for l in range(n)]
+        ws = g.workspace(1)
+        r0 = torch.from_numpy(C.as_f64(C.activations(cfg, 1, step=450)).astype(np.float32)).cuda()
+        good = r0.clone()
+        L.moe_stack_forward(g.ctx, descs, good, 1e-6, ws)
+        assert L.moe_status(ctx) == 0
+        for layer in (0, 2):
+            L.moe_ctx_set_option(ctx, L.OPT_TEST_SKIP_ARRIVAL, layer)
+            assert L.moe_ctx_get_option(ctx, L.OPT_TEST_SKIP_ARRIVAL) == layer
+            try:
+                r = r0.clone()
+                t0 = time.time()
+                L.moe_stack_forward(g.ctx, descs, r, 1e-6, ws)
+                bits = L.moe_status(ctx)
+                dt = time.time() - t0
+            finally:
+                L.moe_ctx_set_option(ctx, L.OPT_TEST_SKIP_ARRIVAL, -1)
+            assert bits & L.STATUS_TIMEOUT
+            assert L.moe_ctx_get_option(ctx, L.OPT_LAST_PATH) == 1
+            assert 0.2 < dt < 30.0  # gave up after about a second, did not hang
+            again = r0.clone()
+            L.moe_stack_forward(g.ctx, descs, again, 1e-6, ws)
+            assert L.moe_status(ctx) == 0
+            assert torch.equal(again, good)
+        with pytest.raises(L.MoeError):
+            L.moe_ctx_set_option(ctx, L.OPT_TEST_SKIP_ARRIVAL, -2)
+    finally:
+        g.close()
