@@ -121,3 +121,33 @@ def test_swap_policy_applies_its_rounds_and_misses_are_flagged(torch, ctx):
         torch.cuda.synchronize()
         L.moe_slots_destroy(slots)
         L.moe_arena_destroy(arena)
+
+
+def test_pinned_pageable_and_device_blobs_load_the_same_bytes(torch, ctx):
+    # pinned (asynchronous copy) and pageable (synchronous copy) host blobs go through
+    # the pool's staging buffer, device blobs are read directly: same layer bits
+    cfg = C.CONFIGS["tiny"]
+    blobs = C.experts(cfg, 0, range(cfg.E))
+    Wr = torch.from_numpy(C.router_weights(cfg, 0)).cuda()
+    x = torch.from_numpy(C.activations(cfg, 4, step=79)).cuda()
+    eb = cfg.expert_bytes()
+    outs = []
+    for how in ("pinned", "pageable", "device"):
+        arena = L.moe_arena_create(ctx, cfg.E * ((eb + 255) // 256 * 256) + 4096)
+        slots = L.moe_slots_create(ctx, arena, 1, cfg.E, cfg.kind, cfg.zero_point, cfg.H, cfg.F, cfg.E)
+        keep = []
+        for e in range(cfg.E):
+            t = torch.from_numpy(blobs[e])
+            t = t.pin_memory() if how == "pinned" else (t.cuda() if how == "device" else t)
+            keep.append(t)
+            L.moe_slot_load(slots, 0, e, t)
+        desc = L.layer_desc(slots, 0, cfg.H, cfg.E, cfg.K, cfg.F, Wr)
+        ws = torch.empty(L.moe_layer_workspace(desc, 4), dtype=torch.uint8, device="cuda")
+        y = torch.empty(4, cfg.H, device="cuda")
+        L.moe_layer_forward(ctx, desc, x, y, ws)
+        assert L.moe_status(ctx) == 0
+        outs.append(y.clone())
+        torch.cuda.synchronize()
+        L.moe_slots_destroy(slots)
+        L.moe_arena_destroy(arena)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
