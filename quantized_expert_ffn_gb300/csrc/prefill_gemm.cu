@@ -24,9 +24,13 @@
 //      writes h as fp16 (row = plan column); down tiles write fp32 y_pair rows.
 //
 // A tile is (column group of <= 256 live pairs of one expert, 128-row M-tile);
-// CTAs (one per SM) take tiles round-robin. Every barrier wait gives up after
-// about a second (MOE_STATUS_TIMEOUT) and the CTA stops; the TMEM it allocated is
-// released on every path.
+// CTAs (one per SM) take tiles round-robin. A second form (k_umma<true>, off by
+// default) runs a cluster of two CTAs per pair of M-tiles with cta_group::2
+// (M = 256): each CTA dequantises its own 128 rows and loads half of the group's
+// columns, rank 0 issues the MMAs and commits to the barriers of both; it gives the
+// same bits and was measured slower. Every barrier wait gives up after about a
+// second (MOE_STATUS_TIMEOUT) and the CTA stops; the TMEM it allocated is released
+// on every path.
 #include <cudaTypedefs.h>
 
 #include "decode_common.cuh"
@@ -37,10 +41,8 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64;
-constexpr int kAStages = 4, kBStages = 4;  // A (dequantised locally) and B (TMA from L2) rings
-constexpr int kPSlots = 3;                                   // packed ring: one 128-k chunk per slot
-constexpr int kBoxRows = 256;                                // rows per B box (32 KB: one box per stage)
-constexpr int kABoxRows = 128;                               // rows per router A box
+constexpr int kPSlots = 3;     // packed ring: one 128-k chunk per slot
+constexpr int kABoxRows = 128; // rows per router A box
 // two groups of 8 dequant warps take alternate stages (two stages in flight)
 // one TMA warp for the packed weights, one for the B rows (each blocks only on its own
 // barriers)
@@ -49,17 +51,26 @@ constexpr int kThreads = 32 * (kDqWarps + 3 + kEpiWarps);  // 736
 constexpr int kDqThreads = 32 * kDqWarps;
 constexpr int kDqGroup = kDqThreads / 2;
 constexpr int kATile = kBM * kBK * 2;      // 16 KB
-constexpr int kBTile = kBN * kBK * 2;      // 32 KB
 constexpr int kPacked = 9216;              // packed codes + scales of one 128-k chunk (Q4, 128 rows)
 constexpr int kTmemCols = 512;             // two 256-column fp32 accumulators
-constexpr int kTileCache = 96;             // tile descriptors staged in shared memory per CTA
 constexpr long long kSpin = 2000000000LL;  // about 1 s
 
-constexpr size_t kSmemA = 0;
-constexpr size_t kSmemB = kSmemA + (size_t)kAStages * kATile;
-constexpr size_t kSmemP = kSmemB + (size_t)kBStages * kBTile;
-constexpr size_t kSmemBytes = kSmemP + (size_t)kPSlots * kPacked;  // 219,136
-static_assert(kSmemB % 1024 == 0 && kSmemP % 16 == 0, "swizzled tiles need 1024-byte alignment");
+// Shared-memory plan. One CTA per tile (PAIR false): A and B rings of 4 stages, a B
+// stage holding the tile's 256 columns (32 KB). A CTA pair per tile (PAIR true,
+// cta_group::2, M = 256): each CTA holds its own 128 weight rows and half of the
+// columns, so a B stage is 16 KB and both rings get 6 stages in the same space.
+template <bool PAIR>
+struct Plan {
+    static constexpr int kAStages = PAIR ? 6 : 4, kBStages = PAIR ? 6 : 4;
+    static constexpr int kBoxRows = PAIR ? kBN / 2 : kBN;  // rows of a CTA's largest B box
+    static constexpr int kBTile = kBoxRows * kBK * 2;
+    static constexpr int kTileCache = PAIR ? 64 : 96;      // tile descriptors staged per CTA
+    static constexpr size_t kSmemA = 0;
+    static constexpr size_t kSmemB = kSmemA + (size_t)kAStages * kATile;
+    static constexpr size_t kSmemP = kSmemB + (size_t)kBStages * kBTile;
+    static constexpr size_t kSmemBytes = kSmemP + (size_t)kPSlots * kPacked;  // 219,136 / 224,256
+    static_assert(kSmemB % 1024 == 0 && kSmemP % 16 == 0, "swizzled tiles need 1024-byte alignment");
+};
 
 __device__ __forceinline__ unsigned su32(const void *p) { return (unsigned)__cvta_generic_to_shared(p); }
 
@@ -77,10 +88,10 @@ __device__ __forceinline__ uint64_t sdesc(unsigned addr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B both fp16 (bf16 when
-// `bf16`), both K-major, M = 128, N = n (multiple of 16, <= 256).
-__device__ __forceinline__ uint32_t idesc_f16(int n, bool bf16) {
+// `bf16`), both K-major, M = m (128; 256 for a CTA pair), N = n (multiple of 16, <= 256).
+__device__ __forceinline__ uint32_t idesc_f16(int n, bool bf16, int m) {
     const uint32_t ab = bf16 ? 1u : 0u;
-    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t *m, unsigned count) {
@@ -123,6 +134,57 @@ __device__ __forceinline__ void tma_box3(void *dst, const CUtensorMap *map, int 
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
         "[%5];" ::"r"(su32(dst)),
         "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(su32(m))
+        : "memory");
+}
+
+// ---- CTA pairs: clusters of two CTAs; rank 0 issues the MMAs of both (cta_group::2)
+__device__ __forceinline__ int cluster_rank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return (int)r;
+}
+__device__ __forceinline__ int cluster_index() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return (int)r;
+}
+__device__ __forceinline__ int cluster_count() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return (int)r;
+}
+// Cluster address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ unsigned map_rank(const void *p, int rank) {
+    unsigned r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(su32(p)), "r"(rank));
+    return r;
+}
+// Arrival (release at cluster scope) on a barrier given by its cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(unsigned addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+// Phase check with acquire at cluster scope (for barriers the other CTA arrives on).
+__device__ __forceinline__ bool mbar_try_cluster(uint64_t *m, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(su32(m)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Every thread of both CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// One box of a 2-D tensor map into this CTA's shared memory, completing on the
+// barrier at cluster address `mbar` (rank 0's, for both CTAs of a pair).
+__device__ __forceinline__ void tma_box_pair(void *dst, const CUtensorMap *map, int c0, int c1, unsigned mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+        "[%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(mbar)
         : "memory");
 }
 
@@ -201,63 +263,115 @@ __device__ __forceinline__ float act_fast(int act, float g) {
 }
 __device__ __forceinline__ int col_token(int cv, int K) { return cv >= 0 ? cv / K : -cv - 1; }
 
+// The completion of every MMA this thread has issued arrives on `bar`; pairs: on the
+// barrier at the same offset in both CTAs of the cluster.
+template <bool PAIR>
+__device__ __forceinline__ void commit_to(uint64_t *bar) {
+    if (PAIR)
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                su32(bar)),
+            "h"((unsigned short)3)
+            : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+                     : "memory");
+}
+
+// 32 consecutive accumulator columns of this warp's 32 TMEM lanes, waited for.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t v[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 struct TileInfo {
     Group grp;
     int mt;
     bool shared;
-    int nk;  // K stages
+    bool mvalid;  // the M-tile lies inside the weights (a pair's second tile can lie past an odd count)
+    int nk;       // K stages
 };
 
-__device__ __forceinline__ bool tile_info(const UmmaArgs &a, int n_routed, int t, TileInfo &ti) {
+// Tile t of one launch. One CTA per tile: t = (group, M-tile). CTA pairs: t = (group,
+// pair of M-tiles 2j, 2j + 1), CTA rank r taking M-tile 2j + r.
+template <bool PAIR>
+__device__ __forceinline__ bool tile_info(const UmmaArgs &a, int n_routed, int t, int rank, TileInfo &ti) {
     if (a.mode == 2) {
         // router: tile t = (128 experts mt, 256 tokens nt)
         const int mt = t % a.n_mt, nt = t / a.n_mt;
         ti.grp = Group{-1, kBN * nt, min(kBN, a.T - kBN * nt), 0};
         ti.mt = mt;
         ti.shared = false;
+        ti.mvalid = true;
         ti.nk = a.H / kBK;
         return ti.grp.ncols > 0;
     }
-    const int nr = n_routed * a.n_mt;
+    const int mp = PAIR ? (a.n_mt + 1) / 2 : a.n_mt;
+    const int mps = PAIR ? (a.n_mt_s + 1) / 2 : a.n_mt_s;
+    const int nr = n_routed * mp;
+    int j;
     if (t < nr) {
-        ti.grp = a.groups[t / a.n_mt];
-        ti.mt = t % a.n_mt;
+        ti.grp = a.groups[t / mp];
+        j = t % mp;
         ti.shared = false;
     } else {
         const int t2 = t - nr;
-        if (t2 >= a.n_shared * a.n_mt_s) return false;
-        ti.grp = a.groups[a.max_routed + t2 / a.n_mt_s];
-        ti.mt = t2 % a.n_mt_s;
+        if (t2 >= a.n_shared * mps) return false;
+        ti.grp = a.groups[a.max_routed + t2 / mps];
+        j = t2 % mps;
         ti.shared = true;
     }
+    ti.mt = PAIR ? 2 * j + rank : j;
+    ti.mvalid = ti.mt < (ti.shared ? a.n_mt_s : a.n_mt);
     const QLayout &L = ti.shared ? a.src.LS : a.src.L;
     ti.nk = (a.mode == 0 ? L.H : L.F) / kBK;
     return true;
 }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ UmmaArgs a) {
+    using Pl = Plan<PAIR>;
+    constexpr int kAS = Pl::kAStages, kBS = Pl::kBStages;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t fullA[kAStages], emptyA[kAStages], fullB[kBStages], emptyB[kBStages];
+    __shared__ __align__(8) uint64_t fullA[kAS], emptyA[kAS], fullB[kBS], emptyB[kBS];
     __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2];
     __shared__ __align__(8) uint64_t pfull_bar[kPSlots], pempty_bar[kPSlots];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ int epi_rows[kEpiWarps][kBN];  // down epilogue: output row of each column, per warp
-    __shared__ TileInfo tiles_s[kTileCache];  // this CTA's tiles (the first kTileCache of them)
+    __shared__ int epi_rows[kEpiWarps][kBN];        // down epilogue: output row of each column, per warp
+    __shared__ TileInfo tiles_s[Pl::kTileCache];  // this CTA's tiles (the first kTileCache of them)
     uint8_t *const sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int G = gridDim.x;
+    if (PAIR && a.mode == 2) {  // the router runs one CTA per tile only
+        if (tid == 0) set_status(a.status, MOE_STATUS_BOUNDS);
+        return;
+    }
+    // one CTA per tile: CTA b takes tiles b, b + G, ...; pairs: cluster c takes c, c + G, ...
+    const int rank = PAIR ? cluster_rank() : 0;
+    const bool leader = rank == 0;  // the CTA that issues the MMAs
+    const int G = PAIR ? cluster_count() : (int)gridDim.x;
+    const int wid = PAIR ? cluster_index() : (int)blockIdx.x;
     const int n_routed = a.mode == 2 ? 0 : *a.n_groups;
-    const int n_tiles = a.mode == 2 ? a.n_mt * ((a.T + kBN - 1) / kBN) : n_routed * a.n_mt + a.n_shared * a.n_mt_s;
+    const int mp = PAIR ? (a.n_mt + 1) / 2 : a.n_mt, mps = PAIR ? (a.n_mt_s + 1) / 2 : a.n_mt_s;
+    const int n_tiles = a.mode == 2 ? a.n_mt * ((a.T + kBN - 1) / kBN) : n_routed * mp + a.n_shared * mps;
     const int P = a.T * a.K;
 
     if (tid == 0) {
-        for (int s = 0; s < kAStages; ++s) {
-            mbar_init(&fullA[s], a.mode == 2 ? 1 : kDqGroup);  // the TMA thread, or one dequant group
+        // pairs: rank 0's fullA also takes one arrival per dequant warp of the other CTA,
+        // and its acce one per epilogue warp of the other CTA
+        for (int s = 0; s < kAS; ++s) {
+            mbar_init(&fullA[s], a.mode == 2 ? 1 : kDqGroup + (PAIR ? kDqWarps / 2 : 0));
             mbar_init(&emptyA[s], 1);
         }
-        for (int s = 0; s < kBStages; ++s) {
-            mbar_init(&fullB[s], 1);  // the TMA thread (with bytes)
+        for (int s = 0; s < kBS; ++s) {
+            mbar_init(&fullB[s], 1);  // the TMA thread (with bytes; pairs: the bytes of both CTAs)
             mbar_init(&emptyB[s], 1);
         }
         for (int s = 0; s < kPSlots; ++s) {
@@ -266,42 +380,53 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf_bar[b], 1);
-            mbar_init(&acce_bar[b], 32 * kEpiWarps);
+            mbar_init(&acce_bar[b], 32 * kEpiWarps + (PAIR ? kEpiWarps : 0));
         }
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // this CTA's tiles t = blockIdx.x + G i: descriptors staged once (one round trip)
-    for (int i = tid; i < kTileCache; i += kThreads) {
-        const int t = blockIdx.x + G * i;
+    // this CTA's tiles: descriptors staged once (one round trip)
+    for (int i = tid; i < Pl::kTileCache; i += kThreads) {
+        const int t = wid + G * i;
         TileInfo ti;
-        if (t < n_tiles && tile_info(a, n_routed, t, ti)) tiles_s[i] = ti;
+        if (t < n_tiles && tile_info<PAIR>(a, n_routed, t, rank, ti)) tiles_s[i] = ti;
     }
     if (warp == kMmaWarp) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        // pairs: one warp of each CTA allocates, collectively, the same columns in both
+        if (PAIR) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)),
+                         "r"(kTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)),
+                         "r"(kTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
+    if (PAIR) cluster_sync_all();  // both CTAs' barriers initialised before any remote arrival
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base;
 
     auto get_tile = [&](int t, TileInfo &ti) -> bool {
-        const int i = (t - (int)blockIdx.x) / G;
-        if (i < kTileCache) {
+        const int i = (t - wid) / G;
+        if (i < Pl::kTileCache) {
             ti = tiles_s[i];
             return true;
         }
-        return tile_info(a, n_routed, t, ti);
+        return tile_info<PAIR>(a, n_routed, t, rank, ti);
     };
 
-    // bounded wait on a barrier phase; on timeout every role of the CTA stops
-    auto wait = [&](uint64_t *m, unsigned parity) -> bool {
-        if (mbar_try(m, parity)) return true;
+    // bounded wait on a barrier phase; on timeout every role of the CTA stops. `cl`:
+    // acquire at cluster scope (a barrier the other CTA of a pair arrives on)
+    auto wait = [&](uint64_t *m, unsigned parity, bool cl = false) -> bool {
+        auto probe = [&]() { return (PAIR && cl) ? mbar_try_cluster(m, parity) : mbar_try(m, parity); };
+        if (probe()) return true;
         const long long t0 = clock64();
-        while (!mbar_try(m, parity)) {
+        while (!probe()) {
             if (*(volatile int *)&abort_flag) return false;
             if (clock64() - t0 > kSpin) {
                 atomicExch(&abort_flag, 1);
@@ -311,12 +436,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         }
         return true;
     };
+    // pairs: warps that arrive once per warp take their waits' outcome as a warp
+    auto wait_warp = [&](uint64_t *m, unsigned parity) -> bool {
+        const bool ok = wait(m, parity);
+        return PAIR ? __all_sync(0xffffffffu, ok) : ok;
+    };
 
     if (warp == kTmaWarp || warp == kTmaBWarp) {
         // ---------------------------------------------------------------- TMA warps
         // warp kTmaWarp: the packed chunk of stages s, s + 1 of each tile (HBM, up to
         // kPSlots chunks ahead); warp kTmaBWarp: the B rows of each stage (L2, up to
-        // kBStages ahead) and, for the router, the A rows.
+        // kBStages ahead) and, for the router, the A rows. A pair splits a group's
+        // round-up(n, 16) columns in halves, rank r loading half r; both halves
+        // complete on rank 0's full barrier, whose TMA thread expects the bytes of both.
         if (lane == 0) {
             const bool packed = warp == kTmaWarp;
             if (!packed) {
@@ -327,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
             }
             int it = 0, ch = 0;
             bool good = !(packed && a.mode == 2);
-            for (int t = blockIdx.x; t < n_tiles && good; t += G) {
+            for (int t = wid; t < n_tiles && good; t += G) {
                 TileInfo ti;
                 if (!get_tile(t, ti)) break;
                 for (int s2 = 0; s2 < ti.nk && good; ++s2, ++it) {
@@ -339,12 +471,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                             break;
                         }
                         // one chunk of the 128-row M-tile: gate/up codes + scales boxes, or
-                        // one down box (a half box for a last half chunk)
+                        // one down box (a half box for a last half chunk). An M-tile past
+                        // the weights (a pair's second tile of an odd count) lies outside the
+                        // tensor: the boxes read as zeros.
                         const QLayout &L = ti.shared ? a.src.LS : a.src.L;
                         const CUtensorMap *pk = ti.shared ? &a.pk[2] : &a.pk[0];
                         const int slot = ti.shared ? 0 : ti.grp.slot;
                         const int c = s2 >> 1;
-                        uint8_t *dst = sm + kSmemP + (size_t)ps * kPacked;
+                        uint8_t *dst = sm + Pl::kSmemP + (size_t)ps * kPacked;
                         if (a.mode == 0) {
                             mbar_expect_tx(&pfull_bar[ps], 4u * 2304u);
                             tma_box3(dst, &pk[0], c * 288, 4 * ti.mt, slot, &pfull_bar[ps]);
@@ -356,31 +490,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                         }
                         ++ch;
                     } else {
-                        const int bb = it % kBStages;
-                        if (it >= kBStages && !wait(&emptyB[bb], ((it / kBStages) - 1) & 1)) {
+                        const int bb = it % kBS;
+                        if (it >= kBS && !wait(&emptyB[bb], ((it / kBS) - 1) & 1)) {
                             good = false;
                             break;
                         }
-                        // the smallest box holding the group's columns (rows past them
-                        // belong to the next group or read as zeros; the MMA's N stops
+                        // the smallest box holding this CTA's columns of the group (rows past
+                        // them belong to the next group or read as zeros; the MMA's N stops
                         // at round-up(ncols, 16))
-                        int bi = 4;
+                        int bi = 4, r0 = ti.grp.col0;
                         if (a.mode != 2) {
                             const int nr = (ti.grp.ncols + 15) & ~15;
-                            bi = nr <= 16 ? 0 : nr <= 32 ? 1 : nr <= 64 ? 2 : nr <= 128 ? 3 : 4;
+                            const int rows = PAIR ? nr / 2 : nr;
+                            const int lo = PAIR ? 8 : 16;
+                            bi = rows <= lo ? 0 : rows <= 2 * lo ? 1 : rows <= 4 * lo ? 2 : rows <= 8 * lo ? 3 : 4;
+                            if (PAIR) r0 += rank * (nr / 2);
                         }
                         const CUtensorMap *mb = bi < 4 ? &a.tmap_bn[bi] : &a.tmap_b;
-                        const int box_rows = bi < 4 ? 16 << bi : kBoxRows;
-                        mbar_expect_tx(&fullB[bb], (unsigned)(box_rows * kBK * 2));
-                        tma_box(sm + kSmemB + (size_t)bb * kBTile, mb, s2 * kBK, ti.grp.col0, &fullB[bb]);
+                        const int box_rows = bi < 4 ? (PAIR ? 8 : 16) << bi : Pl::kBoxRows;
+                        uint8_t *dstB = sm + Pl::kSmemB + (size_t)bb * Pl::kBTile;
+                        if (PAIR) {
+                            if (leader) mbar_expect_tx(&fullB[bb], (unsigned)(2 * box_rows * kBK * 2));
+                            tma_box_pair(dstB, mb, s2 * kBK, r0, map_rank(&fullB[bb], 0));
+                        } else {
+                            mbar_expect_tx(&fullB[bb], (unsigned)(box_rows * kBK * 2));
+                            tma_box(dstB, mb, s2 * kBK, r0, &fullB[bb]);
+                        }
                         if (a.mode == 2) {
-                            const int ba = it % kAStages;
-                            if (it >= kAStages && !wait(&emptyA[ba], ((it / kAStages) - 1) & 1)) {
+                            const int ba = it % kAS;
+                            if (it >= kAS && !wait(&emptyA[ba], ((it / kAS) - 1) & 1)) {
                                 good = false;
                                 break;
                             }
                             mbar_expect_tx(&fullA[ba], (unsigned)(kABoxRows * kBK * 2));
-                            tma_box(sm + kSmemA + (size_t)ba * kATile, &a.tmap_a, s2 * kBK, kBM * ti.mt, &fullA[ba]);
+                            tma_box(sm + Pl::kSmemA + (size_t)ba * kATile, &a.tmap_a, s2 * kBK, kBM * ti.mt, &fullA[ba]);
                         }
                     }
                 }
@@ -391,7 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         // ---------------------------------------------------------------- dequant warps
         // Stage s of a tile dequantises half s & 1 of chunk s / 2 into the A tile; item
         // `it` belongs to group it % 2, and warp w of a group takes one 16-row slice
-        // (gate/up tile w / 2, gate if w is even; down tile w).
+        // (gate/up tile w / 2, gate if w is even; down tile w). Pairs: rank 1's warps
+        // arrive on rank 0's full barrier, once per warp.
         const int g = lane >> 2;
         const int grp = warp >> 3, lw = warp & 7;
         // stmatrix row addresses: lane l gives row l % 8 of matrix l / 8 (matrices:
@@ -399,13 +543,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         const int mrow = (lane & 7) + 8 * ((lane >> 3) & 1), mk = 8 * (lane >> 4);
         int it = 0, ch = 0;
         bool good = true;
-        for (int t = blockIdx.x; t < n_tiles && good; t += G) {
+        for (int t = wid; t < n_tiles && good; t += G) {
             TileInfo ti;
             if (!get_tile(t, ti)) break;
             const QLayout &L = ti.shared ? a.src.LS : a.src.L;
             if (a.mode == 2) break;  // the router has nothing to dequantise
             for (int s2 = 0; s2 < ti.nk; ++s2, ++it) {
-                const int b = it % kAStages;
+                const int b = it % kAS;
                 const int ps = ch % kPSlots;
                 const bool single = (s2 & 1) == 0 && s2 == ti.nk - 1;  // a chunk of one stage
                 const bool chunk_done = (s2 & 1) == 1 || s2 == ti.nk - 1;
@@ -413,18 +557,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                     if (chunk_done) ++ch;
                     continue;
                 }
-                if (!wait(&pfull_bar[ps], (ch / kPSlots) & 1)) {
+                if (!wait_warp(&pfull_bar[ps], (ch / kPSlots) & 1)) {
                     good = false;
                     break;
                 }
                 // the A tile of this buffer is free once the MMA of item it - kAStages is done
-                if (it >= kAStages && !wait(&emptyA[b], ((it / kAStages) - 1) & 1)) {
+                if (it >= kAS && !wait_warp(&emptyA[b], ((it / kAS) - 1) & 1)) {
                     good = false;
                     break;
                 }
-                if (a.mode != 2) {
-                    const uint8_t *pk = sm + kSmemP + (size_t)ps * kPacked;
-                    uint8_t *sA = sm + kSmemA + (size_t)b * kATile;
+                {
+                    const uint8_t *pk = sm + Pl::kSmemP + (size_t)ps * kPacked;
+                    uint8_t *sA = sm + Pl::kSmemA + (size_t)b * kATile;
                     const int h = s2 & 1;
                     int row0, off_codes, off_scales;
                     if (a.mode == 0) {
@@ -460,7 +604,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                     // generic-proxy writes -> visible to the tensor cores' async proxy
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                mbar_arrive(&fullA[b]);
+                if (PAIR && !leader) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(map_rank(&fullA[b], 0));
+                } else {
+                    mbar_arrive(&fullA[b]);
+                }
                 // this half of the chunk is no longer needed (a chunk of one stage counts for
                 // both halves)
                 mbar_arrive(&pempty_bar[ps]);
@@ -470,52 +619,55 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // Pairs: rank 0 alone issues M = 256 MMAs (its A rows and B half, and rank 1's
+        // at the same offsets); the commits arrive on the barriers of both CTAs.
+        if (lane == 0 && leader) {
             int it = 0, ti_local = 0;
             bool good = true;
             int last_b = -1;
             unsigned last_par = 0;
-            for (int t = blockIdx.x; t < n_tiles && good; t += G, ++ti_local) {
+            for (int t = wid; t < n_tiles && good; t += G, ++ti_local) {
                 TileInfo ti;
                 if (!get_tile(t, ti)) break;
                 const int ab = ti_local & 1;
-                if (ti_local >= 2 && !wait(&acce_bar[ab], ((ti_local >> 1) - 1) & 1)) break;
+                if (ti_local >= 2 && !wait(&acce_bar[ab], ((ti_local >> 1) - 1) & 1, true)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const int n = (ti.grp.ncols + 15) & ~15;
-                const uint32_t idesc = idesc_f16(n, a.mode == 2);
+                const uint32_t idesc = idesc_f16(n, a.mode == 2, PAIR ? 2 * kBM : kBM);
                 const uint32_t dt = tmem + (uint32_t)(256 * ab);
                 for (int s = 0; s < ti.nk; ++s, ++it) {
-                    const int ba = it % kAStages, b = it % kBStages;
-                    if (!wait(&fullB[b], (it / kBStages) & 1) || !wait(&fullA[ba], (it / kAStages) & 1)) {
+                    const int ba = it % kAS, b = it % kBS;
+                    if (!wait(&fullB[b], (it / kBS) & 1, true) || !wait(&fullA[ba], (it / kAS) & 1, true)) {
                         good = false;
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const unsigned aa = su32(sm + kSmemA + (size_t)ba * kATile);
-                    const unsigned bb = su32(sm + kSmemB + (size_t)b * kBTile);
+                    const unsigned aa = su32(sm + Pl::kSmemA + (size_t)ba * kATile);
+                    const unsigned bb = su32(sm + Pl::kSmemB + (size_t)b * Pl::kBTile);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t da = sdesc(aa + 32 * kk), db = sdesc(bb + 32 * kk);
                         const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-                        asm volatile(
-                            "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
-                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
-                            "l"(da), "l"(db), "r"(idesc), "r"(acc)
-                            : "memory");
+                        if (PAIR)
+                            asm volatile(
+                                "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+                                "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
+                                "l"(da), "l"(db), "r"(idesc), "r"(acc)
+                                : "memory");
+                        else
+                            asm volatile(
+                                "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+                                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
+                                "l"(da), "l"(db), "r"(idesc), "r"(acc)
+                                : "memory");
                     }
-                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                     su32(&emptyA[ba]))
-                                 : "memory");
-                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                     su32(&emptyB[b]))
-                                 : "memory");
+                    commit_to<PAIR>(&emptyA[ba]);
+                    commit_to<PAIR>(&emptyB[b]);
                     last_b = b;
-                    last_par = (unsigned)(it / kBStages) & 1u;
+                    last_par = (unsigned)(it / kBS) & 1u;
                 }
                 if (!good) break;
-                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 su32(&accf_bar[ab]))
-                             : "memory");
+                commit_to<PAIR>(&accf_bar[ab]);
             }
             // every MMA this thread issued has completed before TMEM can be released
             if (last_b >= 0) {
@@ -529,13 +681,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         // ---------------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lanes 32q .. 32q + 31
         int ti_local = 0;
-        for (int t = blockIdx.x; t < n_tiles; t += G, ++ti_local) {
+        for (int t = wid; t < n_tiles; t += G, ++ti_local) {
             TileInfo ti;
             if (!get_tile(t, ti)) break;
             const int ab = ti_local & 1;
-            if (!wait(&accf_bar[ab], (ti_local >> 1) & 1)) break;
+            if (!wait_warp(&accf_bar[ab], (ti_local >> 1) & 1)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const int ncols = ti.grp.ncols;
+            // a pair's M-tile past the weights holds zeros: nothing to write
+            const int ncols = ti.mvalid ? ti.grp.ncols : 0;
             const QLayout &L = ti.shared ? a.src.LS : a.src.L;
             int *rows = epi_rows[q];
             if (a.mode == 2) {
@@ -544,17 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                 const float be = (a.bias && e < a.E) ? a.bias[e] : 0.f;
                 for (int c0 = 0; c0 < ncols; c0 += 32) {
                     uint32_t v[32];
-                    const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * ab + c0);
-                    asm volatile(
-                        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-                          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-                          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
-                          "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
-                          "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-                        : "r"(taddr));
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * ab + c0), v);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (c0 + j < ncols && e < a.E)
@@ -570,17 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
             }
             for (int c0 = 0; c0 < ncols; c0 += 32) {
                 uint32_t v[32];
-                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * ab + c0);
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-                      "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-                      "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
-                      "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
-                      "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-                    : "r"(taddr));
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(256 * ab + c0), v);
                 if (a.mode == 0) {
                     // lanes 0..15: gate rows, 16..31: up rows of f = 64 mt + 16 q + lane % 16;
                     // lane < 16 forms h for token j, lane >= 16 for token j + 1
@@ -607,15 +740,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                 }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            mbar_arrive(&acce_bar[ab]);
+            if (PAIR && !leader) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(map_rank(&acce_bar[ab], 0));
+            } else {
+                mbar_arrive(&acce_bar[ab]);
+            }
             __syncwarp();  // the row cache is rewritten for the next tile
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
+    if (PAIR) cluster_sync_all();  // rank 0's MMAs into rank 1's memory are done; both CTAs' reads too
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                         : "memory");
     }
 }
 
@@ -656,9 +800,27 @@ bool umma_supported(const QLayout &L) { return L.kind == MOE_Q4_32 && L.H % 128 
 
 bool umma_router_supported(int H) { return H % kBK == 0; }
 
-int launch_umma(const UmmaArgs &a, int n_ctas, cudaStream_t s) {
-    k_umma<<<n_ctas, kThreads, kSmemBytes + 1024, s>>>(a);
-    MOE_CUDA_TRY(cudaGetLastError());
+int launch_umma(const UmmaArgs &a, int n_ctas, bool pair, cudaStream_t s) {
+    if (!pair) {
+        k_umma<false><<<n_ctas, kThreads, Plan<false>::kSmemBytes + 1024, s>>>(a);
+        MOE_CUDA_TRY(cudaGetLastError());
+        return MOE_OK;
+    }
+    // clusters of two CTAs on neighbouring SMs
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(n_ctas & ~1));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Plan<true>::kSmemBytes + 1024;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_umma<true>, a));
     return MOE_OK;
 }
 
@@ -686,7 +848,7 @@ int make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, unsigned long lo
         return set_error(MOE_ERR_ARG, "tensor map base / row stride not 16-byte aligned");
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {row_stride_bytes};
-    if (box_rows <= 0) box_rows = kBoxRows;
+    if (box_rows <= 0) box_rows = kBN;
     const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
@@ -736,10 +898,19 @@ int make_packed_maps(CUtensorMap maps[2], int mode, const QLayout &L, const uint
 }
 
 int init_umma_attributes(int max_smem) {
-    if ((size_t)max_smem < kSmemBytes + 1024 + 256) return MOE_OK;  // too little shared memory: never launched
-    return set_max_dynamic_smem((const void *)k_umma, max_smem);
+    // a form whose shared memory does not fit is never launched (umma_fits says so)
+    int rc = MOE_OK;
+    if (umma_fits(max_smem, false)) rc = set_max_dynamic_smem((const void *)k_umma<false>, max_smem);
+    if (!rc && umma_fits(max_smem, true)) rc = set_max_dynamic_smem((const void *)k_umma<true>, max_smem);
+    return rc;
 }
 
-size_t umma_smem_bytes() { return kSmemBytes + 1024; }
+bool umma_fits(int max_smem, bool pair) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, pair ? (const void *)k_umma<true> : (const void *)k_umma<false>) != cudaSuccess)
+        return false;
+    const size_t dyn = (pair ? Plan<true>::kSmemBytes : Plan<false>::kSmemBytes) + 1024;
+    return dyn + fa.sharedSizeBytes <= (size_t)max_smem;
+}
 
 }  // namespace moe

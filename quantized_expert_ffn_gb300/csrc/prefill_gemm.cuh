@@ -19,8 +19,9 @@ struct UmmaArgs {
     // order, fp16; mode 1: h; mode 2: x, bf16) and, for mode 2, the router rows
     alignas(64) CUtensorMap tmap_b;
     alignas(64) CUtensorMap tmap_a;
-    // modes 0 and 1: the B tensor again with boxes of 16, 32, 64 and 128 rows, so a
-    // group of n columns moves the smallest box that holds round-up(n, 16) rows
+    // modes 0 and 1: the B tensor again with boxes of 16, 32, 64 and 128 rows (CTA
+    // pairs: 8 to 64, tmap_b 128), so a CTA moves the smallest box that holds its
+    // rows of the group's round-up(n, 16) columns
     alignas(64) CUtensorMap tmap_bn[4];
     // packed weights as 3-D byte tensors [slot][row tile][bytes] (8-byte elements):
     // pk[0] / pk[1] routed experts, pk[2] / pk[3] the shared expert. Gate/up: [0|2]
@@ -52,7 +53,9 @@ struct UmmaArgs {
 bool umma_supported(const QLayout &L);
 // The router GEMM runs for bf16 x and Wr with H a multiple of 64.
 bool umma_router_supported(int H);
-int launch_umma(const UmmaArgs &a, int n_ctas, cudaStream_t s);
+// One CTA per tile, or (pair) clusters of two CTAs sharing each M = 256 tile
+// (modes 0 and 1 only; n_ctas rounded down to even).
+int launch_umma(const UmmaArgs &a, int n_ctas, bool pair, cudaStream_t s);
 // out[i] = fp16(x[token of plan column i]) for the n_cols (device count) columns
 int launch_gather_f16(const int32_t *cols, const int32_t *n_cols, const void *x, int xf32, int K, int H, int max_rows,
                       __half *out, cudaStream_t s);
@@ -65,6 +68,7 @@ int make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, unsigned long lo
 int make_packed_maps(CUtensorMap maps[2], int mode, const QLayout &L, const uint8_t *base, long long slot_stride,
                      int n_slots);
 int init_umma_attributes(int max_smem);
-size_t umma_smem_bytes();
+// The form's shared memory (dynamic + static) fits in max_smem bytes per block.
+bool umma_fits(int max_smem, bool pair);
 
 }  // namespace moe
