@@ -189,12 +189,13 @@ int router_logits(moe_ctx *ctx, const void *x, moe_dtype xt, int T, int H, const
         ua.T = T;
         ua.n_mt = (E + 127) / 128;
         ua.status = ctx->d_status;
+        // tiles of 64 tokens: a 4,096-token window keeps 64 SMs busy instead of 16
         int rc = make_tmap_2d(&ua.tmap_b, x, true, (unsigned long long)T, (unsigned long long)H,
-                              (unsigned long long)H * 2);
+                              (unsigned long long)H * 2, 64);
         if (!rc) rc = make_tmap_2d(&ua.tmap_a, Wr, true, (unsigned long long)E, (unsigned long long)H,
                                    (unsigned long long)H * 2, 128);
         if (rc) return rc;
-        const int tiles = ua.n_mt * ((T + 255) / 256);
+        const int tiles = ua.n_mt * ((T + 63) / 64);
         return launch_umma(ua, tiles < sms ? tiles : sms, false, s);
     }
     return launch_router_logits(x, xt, T, H, Wr, wt, bias, router_scale, E, logits, s);

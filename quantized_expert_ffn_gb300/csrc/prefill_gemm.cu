@@ -43,6 +43,7 @@ namespace {
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr int kPSlots = 3;     // packed ring: one 128-k chunk per slot
 constexpr int kABoxRows = 128; // rows per router A box
+constexpr int kRN = 64;        // router tiles: tokens per tile (and rows per router B box)
 // two groups of 8 dequant warps take alternate stages (two stages in flight)
 // one TMA warp for the packed weights, one for the B rows (each blocks only on its own
 // barriers)
@@ -304,9 +305,9 @@ struct TileInfo {
 template <bool PAIR>
 __device__ __forceinline__ bool tile_info(const UmmaArgs &a, int n_routed, int t, int rank, TileInfo &ti) {
     if (a.mode == 2) {
-        // router: tile t = (128 experts mt, 256 tokens nt)
+        // router: tile t = (128 experts mt, kRN tokens nt)
         const int mt = t % a.n_mt, nt = t / a.n_mt;
-        ti.grp = Group{-1, kBN * nt, min(kBN, a.T - kBN * nt), 0};
+        ti.grp = Group{-1, kRN * nt, min(kRN, a.T - kRN * nt), 0};
         ti.mt = mt;
         ti.shared = false;
         ti.mvalid = true;
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
     const int wid = PAIR ? cluster_index() : (int)blockIdx.x;
     const int n_routed = a.mode == 2 ? 0 : *a.n_groups;
     const int mp = PAIR ? (a.n_mt + 1) / 2 : a.n_mt, mps = PAIR ? (a.n_mt_s + 1) / 2 : a.n_mt_s;
-    const int n_tiles = a.mode == 2 ? a.n_mt * ((a.T + kBN - 1) / kBN) : n_routed * mp + a.n_shared * mps;
+    const int n_tiles = a.mode == 2 ? a.n_mt * ((a.T + kRN - 1) / kRN) : n_routed * mp + a.n_shared * mps;
     const int P = a.T * a.K;
 
     if (tid == 0) {
@@ -507,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                             if (PAIR) r0 += rank * (nr / 2);
                         }
                         const CUtensorMap *mb = bi < 4 ? &a.tmap_bn[bi] : &a.tmap_b;
-                        const int box_rows = bi < 4 ? (PAIR ? 8 : 16) << bi : Pl::kBoxRows;
+                        const int box_rows = a.mode == 2 ? kRN : bi < 4 ? (PAIR ? 8 : 16) << bi : Pl::kBoxRows;
                         uint8_t *dstB = sm + Pl::kSmemB + (size_t)bb * Pl::kBTile;
                         if (PAIR) {
                             if (leader) mbar_expect_tx(&fullB[bb], (unsigned)(2 * box_rows * kBK * 2));

@@ -13,7 +13,7 @@ namespace moe {
 // the plan (groups of at most 256 live columns of one expert; the shared expert's
 // groups start at max_routed) and every 128-row M-tile of the weights; or the
 // router GEMM (mode 2: logits = Wr x + bias, bf16 operands) over 128-expert by
-// 256-token tiles.
+// 64-token tiles.
 struct UmmaArgs {
     // 2-D tensor maps (128-byte swizzle): B rows (mode 0: x in plan
     // order, fp16; mode 1: h; mode 2: x, bf16) and, for mode 2, the router rows
