@@ -292,6 +292,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t v[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// One K = 64 stage: four MMAs of K = 16 (descriptor start +2 = +32 bytes per step);
+// the first accumulates onto D only when `acc`, the others always.
+template <bool PAIR>
+__device__ __forceinline__ void mma_k64(uint32_t dt, uint64_t da, uint64_t db, uint32_t idesc, bool acc) {
+    if (PAIR) {
+        asm volatile(
+            "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
+            "l"(da), "l"(db), "r"(idesc), "r"(acc ? 1u : 0u)
+            : "memory");
+#pragma unroll
+        for (int kk = 1; kk < kBK / 16; ++kk)
+            asm volatile("{ .reg .pred p; setp.ne.b32 p, 1, 0; tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
+                         "l"(da + (uint64_t)(2 * kk)), "l"(db + (uint64_t)(2 * kk)), "r"(idesc)
+                         : "memory");
+    } else {
+        asm volatile(
+            "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
+            "l"(da), "l"(db), "r"(idesc), "r"(acc ? 1u : 0u)
+            : "memory");
+#pragma unroll
+        for (int kk = 1; kk < kBK / 16; ++kk)
+            asm volatile("{ .reg .pred p; setp.ne.b32 p, 1, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
+                         "l"(da + (uint64_t)(2 * kk)), "l"(db + (uint64_t)(2 * kk)), "r"(idesc)
+                         : "memory");
+    }
+}
+
 struct TileInfo {
     Group grp;
     int mt;
@@ -341,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
     using Pl = Plan<PAIR>;
     constexpr int kAS = Pl::kAStages, kBS = Pl::kBStages;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t fullA[kAS], emptyA[kAS], fullB[kBS], emptyB[kBS];
+    static_assert(kAS == kBS, "one barrier pair per stage serves both rings");
+    __shared__ __align__(8) uint64_t fullA[kAS], emptyA[kAS];
     __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2];
     __shared__ __align__(8) uint64_t pfull_bar[kPSlots], pempty_bar[kPSlots];
     __shared__ uint32_t tmem_base;
@@ -368,12 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         // pairs: rank 0's fullA also takes one arrival per dequant warp of the other CTA,
         // and its acce one per epilogue warp of the other CTA
         for (int s = 0; s < kAS; ++s) {
-            mbar_init(&fullA[s], a.mode == 2 ? 1 : kDqGroup + (PAIR ? kDqWarps / 2 : 0));
+            // one "full" barrier per stage counts the A and the B side: the B thread's
+            // arrival with the stage's bytes (pairs: both CTAs' bytes, rank 0 only),
+            // then the dequant group's threads (the router: the A copy's arrival)
+            mbar_init(&fullA[s], a.mode == 2 ? 2 : kDqGroup + (PAIR ? kDqWarps / 2 : 0) + 1);
             mbar_init(&emptyA[s], 1);
-        }
-        for (int s = 0; s < kBS; ++s) {
-            mbar_init(&fullB[s], 1);  // the TMA thread (with bytes; pairs: the bytes of both CTAs)
-            mbar_init(&emptyB[s], 1);
         }
         for (int s = 0; s < kPSlots; ++s) {
             mbar_init(&pfull_bar[s], 1);
@@ -459,10 +488,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                     for (int i = 0; i < 4; ++i) asm volatile("prefetch.tensormap [%0];" ::"l"(&a.tmap_bn[i]) : "memory");
             }
             int it = 0, ch = 0;
+            int bslot = 0;
+            unsigned bphase = 0;
             bool good = !(packed && a.mode == 2);
             for (int t = wid; t < n_tiles && good; t += G) {
                 TileInfo ti;
                 if (!get_tile(t, ti)) break;
+                // B side, per tile: the smallest box holding this CTA's columns of the
+                // group (rows past them belong to the next group or read as zeros; the
+                // MMA's N stops at round-up(ncols, 16))
+                int bi = 4, r0 = ti.grp.col0;
+                if (a.mode != 2) {
+                    const int nr = (ti.grp.ncols + 15) & ~15;
+                    const int rows = PAIR ? nr / 2 : nr;
+                    const int lo = PAIR ? 8 : 16;
+                    bi = rows <= lo ? 0 : rows <= 2 * lo ? 1 : rows <= 4 * lo ? 2 : rows <= 8 * lo ? 3 : 4;
+                    if (PAIR) r0 += rank * (nr / 2);
+                }
+                const CUtensorMap *mb = bi < 4 ? &a.tmap_bn[bi] : &a.tmap_b;
+                const int box_rows = a.mode == 2 ? kRN : bi < 4 ? (PAIR ? 8 : 16) << bi : Pl::kBoxRows;
+                const unsigned bbytes = (unsigned)((PAIR ? 2 : 1) * box_rows * kBK * 2);
                 for (int s2 = 0; s2 < ti.nk && good; ++s2, ++it) {
                     if (packed) {
                         if (s2 & 1) continue;
@@ -491,40 +536,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                         }
                         ++ch;
                     } else {
-                        const int bb = it % kBS;
-                        if (it >= kBS && !wait(&emptyB[bb], ((it / kBS) - 1) & 1)) {
+                        const int bb = bslot;
+                        if (it >= kBS && !wait(&emptyA[bb], bphase ^ 1u)) {
                             good = false;
                             break;
                         }
-                        // the smallest box holding this CTA's columns of the group (rows past
-                        // them belong to the next group or read as zeros; the MMA's N stops
-                        // at round-up(ncols, 16))
-                        int bi = 4, r0 = ti.grp.col0;
-                        if (a.mode != 2) {
-                            const int nr = (ti.grp.ncols + 15) & ~15;
-                            const int rows = PAIR ? nr / 2 : nr;
-                            const int lo = PAIR ? 8 : 16;
-                            bi = rows <= lo ? 0 : rows <= 2 * lo ? 1 : rows <= 4 * lo ? 2 : rows <= 8 * lo ? 3 : 4;
-                            if (PAIR) r0 += rank * (nr / 2);
-                        }
-                        const CUtensorMap *mb = bi < 4 ? &a.tmap_bn[bi] : &a.tmap_b;
-                        const int box_rows = a.mode == 2 ? kRN : bi < 4 ? (PAIR ? 8 : 16) << bi : Pl::kBoxRows;
                         uint8_t *dstB = sm + Pl::kSmemB + (size_t)bb * Pl::kBTile;
                         if (PAIR) {
-                            if (leader) mbar_expect_tx(&fullB[bb], (unsigned)(2 * box_rows * kBK * 2));
-                            tma_box_pair(dstB, mb, s2 * kBK, r0, map_rank(&fullB[bb], 0));
+                            if (leader) mbar_expect_tx(&fullA[bb], bbytes);
+                            tma_box_pair(dstB, mb, s2 * kBK, r0, map_rank(&fullA[bb], 0));
                         } else {
-                            mbar_expect_tx(&fullB[bb], (unsigned)(box_rows * kBK * 2));
-                            tma_box(dstB, mb, s2 * kBK, r0, &fullB[bb]);
+                            mbar_expect_tx(&fullA[bb], bbytes);
+                            tma_box(dstB, mb, s2 * kBK, r0, &fullA[bb]);
                         }
-                        if (a.mode == 2) {
-                            const int ba = it % kAS;
-                            if (it >= kAS && !wait(&emptyA[ba], ((it / kAS) - 1) & 1)) {
-                                good = false;
-                                break;
-                            }
-                            mbar_expect_tx(&fullA[ba], (unsigned)(kABoxRows * kBK * 2));
-                            tma_box(sm + Pl::kSmemA + (size_t)ba * kATile, &a.tmap_a, s2 * kBK, kBM * ti.mt, &fullA[ba]);
+                        if (a.mode == 2) {  // the router's A rows, into the same slot
+                            mbar_expect_tx(&fullA[bb], (unsigned)(kABoxRows * kBK * 2));
+                            tma_box(sm + Pl::kSmemA + (size_t)bb * kATile, &a.tmap_a, s2 * kBK, kBM * ti.mt, &fullA[bb]);
+                        }
+                        if (++bslot == kBS) {
+                            bslot = 0;
+                            bphase ^= 1u;
                         }
                     }
                 }
@@ -623,10 +654,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         // Pairs: rank 0 alone issues M = 256 MMAs (its A rows and B half, and rank 1's
         // at the same offsets); the commits arrive on the barriers of both CTAs.
         if (lane == 0 && leader) {
-            int it = 0, ti_local = 0;
+            // The issue loop is on the critical path of every stage (a stage of a narrow
+            // group runs in ~180 cycles): ring position as a running slot and phase,
+            // descriptors as offsets from per-ring bases.
+            const uint64_t dA0 = sdesc(su32(sm + Pl::kSmemA)), dB0 = sdesc(su32(sm + Pl::kSmemB));
+            int slot = 0, ti_local = 0, last_slot = -1;
+            unsigned phase = 0, last_phase = 0;
             bool good = true;
-            int last_b = -1;
-            unsigned last_par = 0;
             for (int t = wid; t < n_tiles && good; t += G, ++ti_local) {
                 TileInfo ti;
                 if (!get_tile(t, ti)) break;
@@ -636,44 +670,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                 const int n = (ti.grp.ncols + 15) & ~15;
                 const uint32_t idesc = idesc_f16(n, a.mode == 2, PAIR ? 2 * kBM : kBM);
                 const uint32_t dt = tmem + (uint32_t)(256 * ab);
-                for (int s = 0; s < ti.nk; ++s, ++it) {
-                    const int ba = it % kAS, b = it % kBS;
-                    if (!wait(&fullB[b], (it / kBS) & 1, true) || !wait(&fullA[ba], (it / kAS) & 1, true)) {
+                for (int s = 0; s < ti.nk; ++s) {
+                    if (!wait(&fullA[slot], phase, true)) {
                         good = false;
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const unsigned aa = su32(sm + Pl::kSmemA + (size_t)ba * kATile);
-                    const unsigned bb = su32(sm + Pl::kSmemB + (size_t)b * Pl::kBTile);
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t da = sdesc(aa + 32 * kk), db = sdesc(bb + 32 * kk);
-                        const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-                        if (PAIR)
-                            asm volatile(
-                                "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
-                                "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
-                                "l"(da), "l"(db), "r"(idesc), "r"(acc)
-                                : "memory");
-                        else
-                            asm volatile(
-                                "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
-                                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
-                                "l"(da), "l"(db), "r"(idesc), "r"(acc)
-                                : "memory");
+                    // descriptor start addresses count 16-byte units; a K step of 16 is 32 bytes
+                    const uint64_t da = dA0 + (uint64_t)(slot * (kATile >> 4));
+                    const uint64_t db = dB0 + (uint64_t)(slot * (Pl::kBTile >> 4));
+                    mma_k64<PAIR>(dt, da, db, idesc, s > 0);
+                    // one commit frees the stage's A and B slots (both rings have the
+                    // same depth: the B producer waits on the A ring's empty barrier)
+                    commit_to<PAIR>(&emptyA[slot]);
+                    last_slot = slot;
+                    last_phase = phase;
+                    if (++slot == kAS) {
+                        slot = 0;
+                        phase ^= 1u;
                     }
-                    commit_to<PAIR>(&emptyA[ba]);
-                    commit_to<PAIR>(&emptyB[b]);
-                    last_b = b;
-                    last_par = (unsigned)(it / kBS) & 1u;
                 }
                 if (!good) break;
                 commit_to<PAIR>(&accf_bar[ab]);
             }
             // every MMA this thread issued has completed before TMEM can be released
-            if (last_b >= 0) {
+            if (last_slot >= 0) {
                 const long long t0 = clock64();
-                while (!mbar_try(&emptyB[last_b], last_par) && clock64() - t0 < kSpin) {
+                while (!mbar_try(&emptyA[last_slot], last_phase) && clock64() - t0 < kSpin) {
                 }
             }
         }
@@ -686,12 +709,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
             TileInfo ti;
             if (!get_tile(t, ti)) break;
             const int ab = ti_local & 1;
-            if (!wait_warp(&accf_bar[ab], (ti_local >> 1) & 1)) break;
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             // a pair's M-tile past the weights holds zeros: nothing to write
             const int ncols = ti.mvalid ? ti.grp.ncols : 0;
             const QLayout &L = ti.shared ? a.src.LS : a.src.L;
             int *rows = epi_rows[q];
+            // the down tile's output rows, loaded while its MMAs run
+            if (a.mode == 1) {
+                for (int j = lane; j < ncols; j += 32) rows[j] = col_row(a.cols[ti.grp.col0 + j], P);
+                __syncwarp();
+            }
+            if (!wait_warp(&accf_bar[ab], (ti_local >> 1) & 1)) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             if (a.mode == 2) {
                 // logits[t][e] = acc + bias[e]: lane holds expert 128 mt + 32 q + lane
                 const int e = kBM * ti.mt + 32 * q + lane;
@@ -707,10 +735,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                 mbar_arrive(&acce_bar[ab]);
                 continue;
-            }
-            if (a.mode == 1) {
-                for (int j = lane; j < ncols; j += 32) rows[j] = col_row(a.cols[ti.grp.col0 + j], P);
-                __syncwarp();
             }
             for (int c0 = 0; c0 < ncols; c0 += 32) {
                 uint32_t v[32];
