@@ -49,8 +49,6 @@ constexpr int kRN = 64;        // router tiles: tokens per tile (and rows per ro
 // barriers)
 constexpr int kDqWarps = 16, kTmaWarp = 16, kTmaBWarp = 17, kMmaWarp = 18, kEpiWarps = 4;
 constexpr int kThreads = 32 * (kDqWarps + 3 + kEpiWarps);  // 736
-constexpr int kDqThreads = 32 * kDqWarps;
-constexpr int kDqGroup = kDqThreads / 2;
 constexpr int kATile = kBM * kBK * 2;      // 16 KB
 constexpr int kPacked = 9216;              // packed codes + scales of one 128-k chunk (Q4, 128 rows)
 constexpr int kTmemCols = 512;             // two 256-column fp32 accumulators
@@ -113,12 +111,6 @@ __device__ __forceinline__ bool mbar_try(uint64_t *m, unsigned parity) {
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *m, unsigned bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(m)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *m) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     su32(dst)),
-                 "l"(src), "r"(bytes), "r"(su32(m))
-                 : "memory");
 }
 // One box (64 elements x the map's box rows, 128-byte swizzle) of a 2-D tensor map at column
 // c0 (a multiple of 64) and row c1.
@@ -197,22 +189,6 @@ __device__ __forceinline__ void stmatrix4(void *row_addr, uint32_t r0, uint32_t 
                  : "memory");
 }
 
-// Non-blocking check of a barrier phase (try_wait may suspend the thread for a while).
-__device__ __forceinline__ bool mbar_test(uint64_t *m, unsigned parity) {
-    unsigned ok;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(ok)
-        : "r"(su32(m)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ void cp16(void *dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(su32(dst)), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-
 __device__ __forceinline__ uint32_t lop_or(uint32_t a, uint32_t mask, uint32_t orv) {
     uint32_t d;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(orv));
@@ -262,7 +238,6 @@ __device__ __forceinline__ float act_fast(int act, float g) {
     }
     return __fdividef(g, 1.0f + __expf(-g));
 }
-__device__ __forceinline__ int col_token(int cv, int K) { return cv >= 0 ? cv / K : -cv - 1; }
 
 // The completion of every MMA this thread has issued arrives on `bar`; pairs: on the
 // barrier at the same offset in both CTAs of the cluster.
@@ -400,13 +375,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         for (int s = 0; s < kAS; ++s) {
             // one "full" barrier per stage counts the A and the B side: the B thread's
             // arrival with the stage's bytes (pairs: both CTAs' bytes, rank 0 only),
-            // then the dequant group's threads (the router: the A copy's arrival)
-            mbar_init(&fullA[s], a.mode == 2 ? 2 : kDqGroup + (PAIR ? kDqWarps / 2 : 0) + 1);
+            // then the dequant group's warps (the router: the A copy's arrival)
+            mbar_init(&fullA[s], a.mode == 2 ? 2 : kDqWarps / 2 + (PAIR ? kDqWarps / 2 : 0) + 1);
             mbar_init(&emptyA[s], 1);
         }
         for (int s = 0; s < kPSlots; ++s) {
             mbar_init(&pfull_bar[s], 1);
-            mbar_init(&pempty_bar[s], kDqThreads);
+            mbar_init(&pempty_bar[s], kDqWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf_bar[b], 1);
@@ -466,10 +441,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         }
         return true;
     };
-    // pairs: warps that arrive once per warp take their waits' outcome as a warp
+    // warps that arrive once per warp take their waits' outcome as a warp (a timeout
+    // never leaves part of a warp behind at __syncwarp)
     auto wait_warp = [&](uint64_t *m, unsigned parity) -> bool {
         const bool ok = wait(m, parity);
-        return PAIR ? __all_sync(0xffffffffu, ok) : ok;
+        return __all_sync(0xffffffffu, ok);
     };
 
     if (warp == kTmaWarp || warp == kTmaBWarp) {
@@ -566,8 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         // ---------------------------------------------------------------- dequant warps
         // Stage s of a tile dequantises half s & 1 of chunk s / 2 into the A tile; item
         // `it` belongs to group it % 2, and warp w of a group takes one 16-row slice
-        // (gate/up tile w / 2, gate if w is even; down tile w). Pairs: rank 1's warps
-        // arrive on rank 0's full barrier, once per warp.
+        // (gate/up tile w / 2, gate if w is even; down tile w). Each warp arrives once
+        // per stage (pairs: rank 1's warps on rank 0's full barrier).
         const int g = lane >> 2;
         const int grp = warp >> 3, lw = warp & 7;
         // stmatrix row addresses: lane l gives row l % 8 of matrix l / 8 (matrices:
@@ -636,16 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                     // generic-proxy writes -> visible to the tensor cores' async proxy
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                if (PAIR && !leader) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(map_rank(&fullA[b], 0));
-                } else {
-                    mbar_arrive(&fullA[b]);
+                __syncwarp();
+                if (lane == 0) {
+                    if (PAIR && !leader) mbar_arrive_cluster(map_rank(&fullA[b], 0));
+                    else mbar_arrive(&fullA[b]);
+                    mbar_arrive(&pempty_bar[ps]);
+                    if (single) mbar_arrive(&pempty_bar[ps]);
                 }
-                // this half of the chunk is no longer needed (a chunk of one stage counts for
-                // both halves)
-                mbar_arrive(&pempty_bar[ps]);
-                if (single) mbar_arrive(&pempty_bar[ps]);
                 if (chunk_done) ++ch;
             }
         }
