@@ -761,8 +761,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
     }
 }
 
-// x (bf16 or fp32) -> fp16 rows in plan-column order: one CTA per row, 8
-// elements per thread and step
+// x (bf16 or fp32) -> fp16 rows in plan-column order: one CTA per row; a thread's
+// loads of the row (up to kGatherUnits 16-byte output units) are all in flight
+// before it converts and stores.
+constexpr int kGatherUnits = 4;
 __global__ void __launch_bounds__(128) k_gather_f16(const int32_t *__restrict__ cols, const int32_t *__restrict__ n_cols,
                                                     const void *__restrict__ x, int xf32, int K, int H,
                                                     __half *__restrict__ out) {
@@ -770,25 +772,47 @@ __global__ void __launch_bounds__(128) k_gather_f16(const int32_t *__restrict__ 
     if (row >= *n_cols) return;
     const int cv = cols[row];
     const int t = cv >= 0 ? cv / K : -cv - 1;
-    for (int v = threadIdx.x; v < H / 8; v += blockDim.x) {
-        float f[8];
-        if (xf32) {
-            const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + (size_t)t * H + 8 * v);
-            const float4 a0 = p[0], a1 = p[1];
-            f[0] = a0.x; f[1] = a0.y; f[2] = a0.z; f[3] = a0.w; f[4] = a1.x; f[5] = a1.y; f[6] = a1.z; f[7] = a1.w;
-        } else {
-            const uint4 w = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H + 8 * v);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    const int V = H / 8;
+    for (int v0 = 0; v0 < V; v0 += kGatherUnits * blockDim.x) {
+        float4 a[kGatherUnits][2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                f[2 * j] = __uint_as_float(ww[j] << 16);
-                f[2 * j + 1] = __uint_as_float(ww[j] & 0xFFFF0000u);
+        for (int u = 0; u < kGatherUnits; ++u) {
+            const int v = v0 + u * blockDim.x + threadIdx.x;
+            if (v >= V) continue;
+            if (xf32) {
+                const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + (size_t)t * H + 8 * v);
+                a[u][0] = p[0];
+                a[u][1] = p[1];
+            } else {
+                const uint4 w =
+                    *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)t * H + 8 * v);
+                a[u][0] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                                      __uint_as_float(w.w));
             }
         }
-        __align__(16) __half o[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o[j] = __float2half_rn(f[j]);
-        __stcs(reinterpret_cast<uint4 *>(out + (size_t)row * H + 8 * v), *reinterpret_cast<const uint4 *>(o));
+        for (int u = 0; u < kGatherUnits; ++u) {
+            const int v = v0 + u * blockDim.x + threadIdx.x;
+            if (v >= V) continue;
+            float f[8];
+            if (xf32) {
+                f[0] = a[u][0].x; f[1] = a[u][0].y; f[2] = a[u][0].z; f[3] = a[u][0].w;
+                f[4] = a[u][1].x; f[5] = a[u][1].y; f[6] = a[u][1].z; f[7] = a[u][1].w;
+            } else {
+                // bf16 pairs carried as raw words: low half, then high half
+                const uint32_t ww[4] = {__float_as_uint(a[u][0].x), __float_as_uint(a[u][0].y),
+                                        __float_as_uint(a[u][0].z), __float_as_uint(a[u][0].w)};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    f[2 * j] = __uint_as_float(ww[j] << 16);
+                    f[2 * j + 1] = __uint_as_float(ww[j] & 0xFFFF0000u);
+                }
+            }
+            __align__(16) __half o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] = __float2half_rn(f[j]);
+            __stcs(reinterpret_cast<uint4 *>(out + (size_t)row * H + 8 * v), *reinterpret_cast<const uint4 *>(o));
+        }
     }
 }
 

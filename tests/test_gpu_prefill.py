@@ -71,6 +71,21 @@ def test_prefill_matches_oracle_on_sampled_rows(gemma, T, n_rows, pair):
     assert err <= TOL, err
 
 
+def test_prefill_fp32_activations(gemma):
+    # fp32 x (the bf16 values, exactly) through the tensor-core path: the gather
+    # converts it to fp16 rows; the router runs on CUDA cores (its GEMM wants bf16)
+    cfg = gemma.cfg
+    T = 300
+    x = _x(cfg, T, step=940)
+    x32 = C.as_f64(x).astype(np.float32)
+    y, lg, ids, path = _forward(gemma, to_dev(x32))
+    assert path == 2
+    rows = np.array([0, 1, 77, 150, 299])
+    r = oracle_layer(cfg, 0, C.as_f64(x), lg.cpu().numpy(), tokens=rows)
+    assert np.array_equal(ids.cpu().numpy()[rows], r["ids"])
+    assert rel_err(y.cpu().numpy()[rows], r["y"]) <= TOL
+
+
 def test_prefill_close_to_mma_sync_path_on_every_row(gemma):
     cfg = gemma.cfg
     T = 256
