@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill (T=4096 Gemma-shaped layer) line")
     ap.add_argument("--no-residency", action="store_true", help="skip the residency-policy replay and load line")
+    ap.add_argument("--no-gemma-decode", action="store_true",
+                    help="skip the Gemma-shaped layer's decode and verify windows (T = 1, 2, 8)")
     return ap.parse_args()
 
 
@@ -302,6 +304,79 @@ def run_prefill(L, torch, ctx, steps: int = 20, warmup: int = 3):
     return dict(ms=ms, flops=flops, status=status, path=path, T=T)
 
 
+def run_gemma_decode(L, torch, ctx, Ts=(1, 2, 8), n_layers: int = 16, steps: int = 30, warmup: int = 3):
+    """Decode and verify windows of the Gemma-shaped Q4 layer (H=2816, 128 experts,
+    top-8, F=704, shared expert F=2112; Zipf(1.2) router bias): 16 distinct layers
+    (~7 GB of weights, so every window's expert bytes come from HBM), each layer
+    called through moe_layer_forward on the same T-token input, the 16 calls
+    captured in a graph and replayed. Bytes per layer = distinct routed experts x
+    3,345,408 + the shared expert 10,036,224 + the router 720,896."""
+    import synth.device as sdev
+    cfg = C.CONFIGS["gemma_layer"]
+    eb, sh_bytes = cfg.expert_bytes(), cfg.expert_bytes(cfg.F_shared)
+    arena = L.moe_arena_create(ctx, n_layers * (cfg.E * ((eb + 255) // 256 * 256) + sh_bytes + 4096) + (1 << 20))
+    slots = L.moe_slots_create(ctx, arena, n_layers, cfg.E, cfg.kind, cfg.zero_point, cfg.H, cfg.F,
+                               n_layers * cfg.E)
+    shared = [L.moe_slots_create(ctx, arena, 1, 1, cfg.kind, cfg.zero_point, cfg.H, cfg.F_shared, 1)
+              for _ in range(n_layers)]
+    staging = torch.empty(cfg.E * eb, dtype=torch.uint8, device="cuda")
+    sh_blob = torch.from_numpy(C.shared_expert(cfg, 0)).cuda()  # one blob, a copy per layer
+    descs, keep = [], []
+    for l in range(n_layers):
+        sdev.expert_blobs_into(staging, cfg.seed, cfg.tag_expert(l, 0), cfg.E, 3 * cfg.matrix_blocks(), cfg.d_lo,
+                               cfg.d_hi)
+        for e in range(cfg.E):
+            L.moe_slot_load(slots, l, e, staging.data_ptr() + e * eb, eb)
+        L.moe_slot_load(shared[l], 0, 0, sh_blob)
+        Wr = torch.from_numpy(C.router_weights(cfg, l).view(np.int16)).view(torch.bfloat16).cuda()
+        bias = torch.from_numpy(C.router_bias(cfg, l)).cuda()
+        keep += [Wr, bias]
+        descs.append(L.layer_desc(slots, l, cfg.H, cfg.E, cfg.K, cfg.F, Wr, bias, shared[l], cfg.F_shared))
+    torch.cuda.synchronize()
+    del staging
+    stream = torch.cuda.Stream()
+    ws = torch.empty(L.moe_layer_workspace(descs[0], max(Ts)), dtype=torch.uint8, device="cuda")
+    rows = []
+    for T in Ts:
+        x = torch.from_numpy(C.activations(cfg, T, step=7000 + T).view(np.int16)).view(torch.bfloat16).cuda()
+        y = torch.empty(T, cfg.H, device="cuda")
+        ids = torch.empty(n_layers, T, cfg.K, dtype=torch.int32, device="cuda")
+        with torch.cuda.stream(stream):
+            for l in range(n_layers):
+                L.moe_layer_forward(ctx, descs[l], x, y, ws, ids=ids[l], stream=stream)
+        stream.synchronize()
+        status = L.moe_status(ctx, stream)
+        path = L.moe_ctx_get_option(ctx, L.OPT_LAST_PATH)
+        ids_h = ids.cpu().numpy()
+        distinct = [len(np.unique(ids_h[l])) for l in range(n_layers)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for l in range(n_layers):
+                L.moe_layer_forward(ctx, descs[l], x, y, ws, stream=stream)
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_layer = e0.elapsed_time(e1) / (steps * n_layers)
+        layer_bytes = float(np.mean(distinct)) * eb + sh_bytes + cfg.E * cfg.H * 2
+        rows.append(dict(T=T, ms_per_layer=ms_layer, layer_tokens_per_s=T / (ms_layer / 1e3),
+                         distinct_experts=float(np.mean(distinct)), bytes_per_layer=layer_bytes,
+                         gbs=layer_bytes / (ms_layer / 1e3) / 1e9, status=status,
+                         path={1: "persistent", 2: "tcgen05 grouped GEMMs", 0: "mma.sync"}.get(path, str(path))))
+        del graph
+    for sh in shared:
+        L.moe_slots_destroy(sh)
+    L.moe_slots_destroy(slots)
+    L.moe_arena_destroy(arena)
+    return rows
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from quantized_expert_ffn_gb300 import _lib as L
@@ -392,6 +467,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     pre = None if args.no_prefill else run_prefill(L, torch, ctx)
+    gemma = None if args.no_gemma_decode else run_gemma_decode(L, torch, ctx)
     resid_line = None if (args.no_residency or rank != 0) else run_residency(L, torch, ctx)
 
     times = torch.tensor([ms, e2e_ms], device="cuda")
@@ -399,7 +475,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
     ms, e2e_ms_max = float(times[0]), float(times[1])
     return dict(ms=ms, e2e_ms=e2e_ms_max, layer_ms=layer_ms, clocks=clocks, status=status, cfg=cfg, path=path,
-                distinct=distinct, prefill=pre, residency=resid_line)
+                distinct=distinct, prefill=pre, gemma=gemma, residency=resid_line)
 
 
 # ------------------------------------------------------------------ oracle (CPU)
@@ -526,6 +602,13 @@ def main():
             else "fallback", "frac": tf / bf16_peak,
             "path": {2: "tcgen05 grouped GEMMs", 1: "persistent", 0: "mma.sync"}.get(pre["path"], str(pre["path"])),
             "device_status": pre["status"]}
+    if r.get("gemma"):
+        hbm = pk["hbm_gbs"] if pk and "hbm_gbs" in pk else 6800.0
+        line["gemma_decode"] = {
+            "workload": "Gemma-shaped Q4 layer H=2816 E=128 top-8 F=704 + shared F=2112, Zipf(1.2) router bias; "
+                        "16 distinct layers (~7 GB) replayed, one moe_layer_forward per layer",
+            "unit": "layer-tokens/s", "hbm_peak_gbs": hbm,
+            "rows": [dict(row, frac_of_hbm=row["gbs"] / hbm) for row in r["gemma"]]}
     if r.get("residency"):
         line["residency"] = r["residency"]
     if rank == 0 and not args.no_cpu_baseline:
