@@ -13,11 +13,15 @@
 //      it into fp16 w = fp16(d * (q - 8)) (one rounding; q - 8 is exact) and store
 //      it with stmatrix, K-major with the 128-byte swizzle the MMA descriptor names;
 //   B  the group's rows, 64 fp16 each per stage, loaded by the TMA warp through a
-//      tensor map in boxes of 32 rows (gate/up: x gathered into plan order and
-//      converted to fp16 once per layer; down: h in plan order);
-//   MMA one thread issues 4 x tcgen05.mma (K = 16 each) per stage and commits to
-//      the stage's "empty" barrier; after the last stage it commits the tile to an
-//      "accumulator full" barrier; two accumulators of 256 TMEM columns alternate;
+//      tensor map in the smallest box (16 to 256 rows) that holds the group
+//      (gate/up: x gathered into plan order and converted to fp16 once per layer;
+//      down: h in plan order);
+//   MMA one thread waits on the stage's "full" barrier (the B bytes and the dequant
+//      warps' arrivals on one barrier), issues 4 x tcgen05.mma (K = 16 each) and
+//      commits to the stage's "empty" barrier (which frees the A and the B slot);
+//      after the last stage it commits the tile to an "accumulator full" barrier;
+//      two accumulators of 256 TMEM columns alternate. This thread's instructions
+//      sit on every stage's critical path, so its loop is kept short;
 //   epilogue 4 warps read the accumulator with tcgen05.ld (warp q: TMEM lanes
 //      32q..32q+31). Gate/up tiles hold rows [gate 16 | up 16] x 4, so a warp pairs
 //      gate and up of the same row with one shuffle, applies the activation and
