@@ -34,6 +34,19 @@ struct moe_policy {
     unsigned long long clock = 0;
     double f = 1.0;  // score factor per token, 2^(-1 / half_life)
     std::vector<double> fpow;  // fpow[d] = pow(f, d), the factor after d tokens
+    // Victim search without a scan. Every score decays by the same factor per token,
+    // so log2(score) + tau / half_life orders the resident pairs as their decayed
+    // scores do (up to rounding). Accessed resident pairs sit in a min-heap on that
+    // key; never-accessed ones (score 0, the lowest of all) in a min-heap on the pair
+    // index. Records carry the pair's version and go stale when it changes.
+    struct Rec {
+        double key;
+        int k;
+        unsigned v;
+    };
+    std::vector<Rec> heap;
+    std::vector<std::pair<int, unsigned>> zheap;
+    std::vector<unsigned> ver;
     // LFU with swaps
     std::vector<float> cnt;
     long long token = 0;
@@ -80,11 +93,47 @@ void list_remove(moe_policy *p, int k) {
     p->rpos[k] = -1;
 }
 
+struct RecAfter {  // heap order: lowest key (then lowest pair) on top
+    bool operator()(const moe_policy::Rec &a, const moe_policy::Rec &b) const {
+        return a.key > b.key || (a.key == b.key && a.k > b.k);
+    }
+};
+
+void heap_push(moe_policy *p, const moe_policy::Rec &r) {
+    p->heap.push_back(r);
+    std::push_heap(p->heap.begin(), p->heap.end(), RecAfter());
+}
+
+void zheap_push(moe_policy *p, int k, unsigned v) {
+    p->zheap.emplace_back(k, v);
+    std::push_heap(p->zheap.begin(), p->zheap.end(), std::greater<std::pair<int, unsigned>>());
+}
+
+// (Re)file resident pair k of the decayed-frequency policy after its score changed or
+// it became resident; stale records are dropped when they reach the top, and the
+// heaps are rebuilt from the resident list when stale records pile up.
+void df_file(moe_policy *p, int k) {
+    if (p->pr.kind != MOE_POLICY_DECAYED_FREQ || !p->res[k]) return;
+    const unsigned v = ++p->ver[k];
+    if (p->score[k] > 0.0) heap_push(p, {std::log2(p->score[k]) + (double)p->tau[k] / p->pr.half_life, k, v});
+    else zheap_push(p, k, v);
+    if (p->heap.size() + p->zheap.size() > 4 * (size_t)p->n_res + 256) {
+        p->heap.clear();
+        p->zheap.clear();
+        for (int r : p->rlist) {
+            if (p->score[r] > 0.0)
+                heap_push(p, {std::log2(p->score[r]) + (double)p->tau[r] / p->pr.half_life, r, p->ver[r]});
+            else zheap_push(p, r, p->ver[r]);
+        }
+    }
+}
+
 void make_resident(moe_policy *p, int k) {
     p->res[k] = 1;
     ++p->n_res;
     list_add(p, k);
     if (p->pr.kind == MOE_POLICY_LRU) lru_push_front(p, k);
+    df_file(p, k);
 }
 
 void make_absent(moe_policy *p, int k) {
@@ -92,6 +141,7 @@ void make_absent(moe_policy *p, int k) {
     --p->n_res;
     list_remove(p, k);
     if (p->pr.kind == MOE_POLICY_LRU) lru_unlink(p, k);
+    ++p->ver[k];
 }
 
 // pow(f, d) for d tokens, the same value a direct pow call gives
@@ -102,6 +152,84 @@ double fpow(moe_policy *p, long long d) {
 
 double decayed(moe_policy *p, int k) { return p->score[k] * fpow(p, p->token - p->tau[k]); }
 
+bool guarded_now(const moe_policy *p, int k) {
+    return p->last[k] >= 0 && p->token - p->last[k] < p->pr.recency_guard;
+}
+
+// The decayed-frequency order: lower decayed score; equal scores to the least
+// recently used, then the lower pair.
+bool df_before(moe_policy *p, int k, double s, int best, double bs) {
+    return best < 0 || s < bs || (s == bs && (p->stamp[k] < p->stamp[best] || (p->stamp[k] == p->stamp[best] && k < best)));
+}
+
+int scan_victim(moe_policy *p);
+
+// Decayed-frequency victim from the heaps. A never-accessed pair (score 0) comes first.
+// Otherwise the lowest key among eligible pairs, and every eligible pair whose key is
+// within a slack far above rounding of it, are compared exactly as the scan compares
+// them (decayed score, recency, pair): a pair beyond the slack has a decayed score
+// larger by a factor of at least 2^slack, which rounding cannot undo. Scores that
+// underflow go to the scan.
+int heap_victim(moe_policy *p) {
+    {
+        std::vector<std::pair<int, unsigned>> back;
+        int victim = -1;
+        auto zafter = std::greater<std::pair<int, unsigned>>();
+        while (!p->zheap.empty()) {
+            const std::pair<int, unsigned> r = p->zheap.front();
+            const int k = r.first;
+            std::pop_heap(p->zheap.begin(), p->zheap.end(), zafter);
+            p->zheap.pop_back();
+            if (r.second != p->ver[k] || !p->res[k]) continue;  // stale
+            back.push_back(r);
+            if (p->mark[k]) continue;
+            victim = k;
+            break;
+        }
+        for (const auto &r : back) zheap_push(p, r.first, r.second);
+        if (victim >= 0) return victim;
+    }
+    constexpr double kSlack = 1e-6;  // in log2 units: a factor of 1 + 6.9e-7
+    constexpr int kMaxSkip = 64;     // more passed-over pairs than this: the scan is cheaper
+    for (int guarded = 1; guarded >= 0; --guarded) {
+        std::vector<moe_policy::Rec> back;
+        int best = -1, skipped = 0;
+        double bs = 0.0, k0 = 0.0;
+        bool have = false, scan = false;
+        while (!p->heap.empty()) {
+            const moe_policy::Rec r = p->heap.front();
+            if (have && r.key > k0 + kSlack * (1.0 + std::fabs(k0))) break;
+            std::pop_heap(p->heap.begin(), p->heap.end(), RecAfter());
+            p->heap.pop_back();
+            const int k = r.k;
+            if (r.v != p->ver[k] || !p->res[k]) continue;  // stale
+            back.push_back(r);
+            if (p->mark[k] || (guarded && guarded_now(p, k))) {
+                // a pool where most pairs sit in the event or the guard (a small pool
+                // under heavy turnover): hand the search to the scan
+                if (++skipped > kMaxSkip) {
+                    scan = true;
+                    break;
+                }
+                continue;
+            }
+            if (!have) {
+                have = true;
+                k0 = r.key;
+            }
+            const double s = decayed(p, k);
+            if (df_before(p, k, s, best, bs)) {
+                best = k;
+                bs = s;
+            }
+        }
+        for (const auto &r : back) heap_push(p, r);
+        if (scan) return scan_victim(p);
+        if (best >= 0) return bs >= std::numeric_limits<double>::min() ? best : scan_victim(p);
+    }
+    return -1;
+}
+
 // Victim for a load, or -1: never a pair of the event being served.
 int pick_victim(moe_policy *p) {
     if (p->pr.kind == MOE_POLICY_LRU) {
@@ -109,17 +237,19 @@ int pick_victim(moe_policy *p) {
             if (!p->mark[k]) return k;
         return -1;
     }
-    // decayed frequency: lowest decayed score; equal scores to the least recently
-    // used, then the lower pair; first among entries outside the recency guard
+    return heap_victim(p);
+}
+
+// The decayed-frequency victim by a scan of the resident pairs: lowest decayed score
+// first among entries outside the recency guard, then among all.
+int scan_victim(moe_policy *p) {
     for (int guarded = 1; guarded >= 0; --guarded) {
         int best = -1;
         double bs = 0.0;
         for (int k : p->rlist) {
-            if (p->mark[k]) continue;
-            if (guarded && p->last[k] >= 0 && p->token - p->last[k] < p->pr.recency_guard) continue;
+            if (p->mark[k] || (guarded && guarded_now(p, k))) continue;
             const double s = decayed(p, k);
-            if (best < 0 || s < bs || (s == bs && (p->stamp[k] < p->stamp[best] ||
-                                                   (p->stamp[k] == p->stamp[best] && k < best)))) {
+            if (df_before(p, k, s, best, bs)) {
                 best = k;
                 bs = s;
             }
@@ -160,6 +290,7 @@ MOE_API int moe_policy_create(const moe_policy_params *params, int n_layers, int
     p->stamp.assign(p->n, 0);
     p->cnt.assign(p->n, 0.f);
     p->rpos.assign(p->n, -1);
+    p->ver.assign(p->n, 0);
     p->rlist.reserve(q.capacity);
     if (q.kind == MOE_POLICY_DECAYED_FREQ) p->f = std::pow(2.0, -1.0 / q.half_life);
     *out = p;
@@ -185,6 +316,7 @@ MOE_API int moe_policy_seed(moe_policy *p, const int32_t *layers, const int32_t 
         ++p->n_res;
         list_add(p, k);
         if (p->pr.kind == MOE_POLICY_LRU) lru_push_back(p, k);
+        df_file(p, k);
         ++placed;
     }
     if (n_placed) *n_placed = placed;
@@ -225,6 +357,7 @@ MOE_API int moe_policy_route(moe_policy *p, int layer, const int32_t *ids, int n
                 p->tau[k] = p->token;
                 p->last[k] = p->token;
                 p->stamp[k] = ++p->clock;
+                df_file(p, k);
             }
         }
         for (int k : ev) {

@@ -145,6 +145,16 @@ def test_engine_matches_reference_lfu_swap(seed):
     _replay(R.LFU_SWAP, tr, 60, seed_pairs=traces.profile_ranking(tr[:4]), max_swaps=3, swap_every=2)
 
 
+@pytest.mark.parametrize("half_life,guard,cap,seeded", [(1.0, 0, 3, False), (1.0, 2, 4, True), (0.5, 1, 5, True),
+                                                        (4.0, 0, 6, False), (1000.0, 2, 7, True)])
+def test_engine_matches_reference_decayed_frequency_on_ties(half_life, guard, cap, seeded):
+    # few experts and short or very long half-lives: many pairs share a history, so
+    # decayed scores tie exactly and the recency and pair-index tie-breaks decide
+    tr = traces.routing_trace(160, 2, 8, 3, seed=int(half_life * 10) + cap, zipf_s=0.3, stick=0.2)
+    prof = traces.profile_ranking(tr[:5]) if seeded else None
+    _replay(R.DECAYED_FREQ, tr, cap, seed_pairs=prof, half_life=half_life, guard=guard)
+
+
 def test_hit_rates_are_bounded_by_belady():
     tr = traces.routing_trace(64, 4, 64, 8, seed=7)
     events = [[(l, tr[t, l]) for l in range(4)] for t in range(64)]
