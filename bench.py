@@ -508,7 +508,7 @@ def oracle_sample_rate(seconds: float, T: int = 1, max_steps: int | None = None)
         busy += (t1 - t0) + (t3 - t2)
         done += 1
         l += 1
-    return done * T / busy, done, busy
+    return (done * T / busy if busy > 0 else 0.0), done, busy
 
 
 # ------------------------------------------------------------------ main
@@ -524,9 +524,8 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        warm = min(args.warmup, 1)
-        if warm:
-            oracle_sample_rate(0.0, args.T, max_steps=1)
+        if args.warmup > 0:  # W untimed steps of the same work
+            oracle_sample_rate(1e9, args.T, max_steps=args.warmup)
         rate, done, busy = oracle_sample_rate(1e9, args.T, max_steps=args.steps)
         line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": n_gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": busy / max(done, 1) * 1e3,
