@@ -304,6 +304,22 @@ def run_prefill(L, torch, ctx, steps: int = 20, warmup: int = 3):
     return dict(ms=ms, flops=flops, status=status, path=path, T=T)
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over every rank of the job (the slowest rank
+    sets the time); the values themselves with one process."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist = torch.distributed
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_value(n_gpus: int, units_per_rank: float, max_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return n_gpus * units_per_rank / (max_ms / 1e3)
+
+
 def run_gemma_decode(L, torch, ctx, Ts=(1, 2, 8), n_layers: int = 16, steps: int = 30, warmup: int = 3):
     """Decode and verify windows of the Gemma-shaped Q4 layer (H=2816, 128 experts,
     top-8, F=704, shared expert F=2112; Zipf(1.2) router bias): 16 distinct layers
@@ -470,10 +486,7 @@ def run_ours(args, rank, world, local_rank):
     gemma = None if args.no_gemma_decode else run_gemma_decode(L, torch, ctx)
     resid_line = None if (args.no_residency or rank != 0) else run_residency(L, torch, ctx)
 
-    times = torch.tensor([ms, e2e_ms], device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(times, op=torch.distributed.ReduceOp.MAX)
-    ms, e2e_ms_max = float(times[0]), float(times[1])
+    ms, e2e_ms_max = max_over_ranks([ms, e2e_ms], "cuda")
     return dict(ms=ms, e2e_ms=e2e_ms_max, layer_ms=layer_ms, clocks=clocks, status=status, cfg=cfg, path=path,
                 distinct=distinct, prefill=pre, gemma=gemma, residency=resid_line)
 
@@ -545,8 +558,8 @@ def main():
     cfg = r["cfg"]
     T = args.T
     layer_tokens = args.layers * T
-    value = n_gpus * layer_tokens * args.steps / (r["ms"] / 1e3)
-    e2e_value = n_gpus * layer_tokens / (r["e2e_ms"] / 1e3)
+    value = job_value(n_gpus, layer_tokens * args.steps, r["ms"])
+    e2e_value = job_value(n_gpus, layer_tokens, r["e2e_ms"])
     pk = peaks()
     hbm_peak = pk["hbm_gbs"] if pk else 6800.0
     expert_bytes = cfg.expert_bytes()
