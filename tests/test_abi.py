@@ -54,3 +54,23 @@ def test_context_without_a_device_fails_cleanly():
         L.moe_ctx_create(0)
     assert e.value.code == -4
     assert "device" in str(e.value)
+
+
+def test_header_is_plain_c_without_cuda_headers():
+    # the boundary is a C ABI: include/moe.h compiles as strict C99 and as C++ with no
+    # CUDA or torch header on the include path
+    import shutil
+    import subprocess
+    import tempfile
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = '#include "moe.h"\nint main(void) { moe_ctx *c = 0; (void)c; return (int)sizeof(moe_layer_desc) > 0 ? 0 : 1; }\n'
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "use.c")
+        with open(path, "w") as f:
+            f.write(src)
+        for cc, flags in (("gcc", ["-std=c99", "-pedantic"]), ("g++", ["-std=c++17", "-x", "c++"])):
+            if shutil.which(cc) is None:
+                continue
+            r = subprocess.run([cc, *flags, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I",
+                                os.path.join(root, "include"), path], capture_output=True, text=True)
+            assert r.returncode == 0, r.stderr
