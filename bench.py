@@ -181,9 +181,9 @@ class Stack:
 def run_residency(L, torch, ctx):
     """Replay of the residency policies on a sticky Zipf routing trace of the
     48-layer stack's shape (hit rates with 5, 10 and 20% of the (layer, expert)
-    pairs resident, Belady's ceiling beside them; us_per_event includes the Python
-    call), and the rate at which moe_policy_apply makes experts resident from
-    pinned host memory."""
+    pairs resident, Belady's ceiling beside them; us_per_event is the host time of a
+    token's 48 events routed in one moe_policy_route_token call, per event), and the
+    rate at which moe_policy_apply makes experts resident from pinned host memory."""
     import time
     import synth.device as sdev
     from synth import traces
@@ -203,9 +203,7 @@ def run_residency(L, torch, ctx):
             hits = 0
             t0 = time.perf_counter()
             for t in range(T_rep):
-                for l in range(Ln):
-                    h = pol.route(l, rep[t, l])[0]
-                    hits += int(h.sum())
+                hits += int(pol.route_token(rep[t])[0].sum())
                 pol.end_token()
             dt = time.perf_counter() - t0
             pol.close()

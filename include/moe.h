@@ -435,6 +435,19 @@ MOE_API int moe_policy_route(moe_policy *p, int layer, const int32_t *ids, int n
                              int32_t *load_expert, int32_t *evict_layer, int32_t *evict_expert,
                              int *n_loads);
 
+/* A whole token's routing in one call, as a chained decode step reports it after
+ * the step: ids [n_layers][K] (host), row l the event of layer l, routed for
+ * layers 0 .. n_layers - 1 in that order. Exactly the decisions of n_layers calls
+ * of moe_policy_route in layer order. hit [n_layers][K] (host, may be NULL). The
+ * loads of all events are appended in event order to load_layer / load_expert
+ * with evict_layer / evict_expert (cap entries each; cap must be at least
+ * n_layers * K for LRU and DECAYED_FREQ, and the buffers may be NULL for
+ * LFU_SWAP, which loads nothing here), their number in *n_loads. Every id is
+ * checked before any state changes: MOE_ERR_ARG leaves the policy as it was. */
+MOE_API int moe_policy_route_token(moe_policy *p, const int32_t *ids, int n_layers, int K, uint8_t *hit,
+                                   int32_t *load_layer, int32_t *load_expert, int32_t *evict_layer,
+                                   int32_t *evict_expert, int cap, int *n_loads);
+
 /* End of the current token. LFU_SWAP makes its swap round's decisions and, with
  * plan buffers, returns them (at most cap swaps are made then): load_layer /
  * load_expert with evict_layer / evict_expert, *n_swaps (NULL buffers: a replay

@@ -85,6 +85,7 @@ _SIGS = {
     "moe_policy_destroy": [_P],
     "moe_policy_seed": [_P, _P, _P, _I, ctypes.POINTER(_I)],
     "moe_policy_route": [_P, _I, _P, _I, _P, _P, _P, _P, ctypes.POINTER(_I)],
+    "moe_policy_route_token": [_P, _P, _I, _I, _P, _P, _P, _P, _P, _I, ctypes.POINTER(_I)],
     "moe_policy_end_token": [_P, _P, _P, _P, _P, _I, ctypes.POINTER(_I)],
     "moe_policy_resident": [_P, _I, _I, ctypes.POINTER(_I)],
     "moe_policy_count": [_P, ctypes.POINTER(_I)],
@@ -352,6 +353,21 @@ class Policy:
         k = m.value
         return hit, le[:k].copy(), el[:k].copy(), ee[:k].copy()
 
+    def route_token(self, ids):
+        """ids [n_layers][K]: one token's events for layers 0 .. n_layers - 1, in order.
+        Returns (hit [n_layers][K] uint8, load_layer [m], load_expert [m],
+        evict_layer [m], evict_expert [m])."""
+        np = self._np
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        nl, K = ids.shape
+        hit = np.zeros((nl, K), dtype=np.uint8)
+        cap = max(nl * K, 1)
+        bufs = [np.zeros(cap, dtype=np.int32) for _ in range(4)]
+        m = _I()
+        _check(load().moe_policy_route_token(self.h, _np_ptr(ids), nl, K, _np_ptr(hit), *[_np_ptr(b) for b in bufs],
+                                             cap, ctypes.byref(m)))
+        return (hit,) + tuple(b[:m.value].copy() for b in bufs)
+
     def end_token(self, plan: bool = True):
         """Returns (load_layer, load_expert, evict_layer, evict_expert) of the swaps made."""
         np = self._np
@@ -411,6 +427,14 @@ def moe_policy_route(h: int, layer: int, ids, hit, load_expert, evict_layer, evi
     n = _I()
     _check(load().moe_policy_route(h, layer, _np_ptr(ids), ids.size, _np_ptr(hit), _np_ptr(load_expert),
                                    _np_ptr(evict_layer), _np_ptr(evict_expert), ctypes.byref(n)))
+    return n.value
+
+
+def moe_policy_route_token(h: int, ids, hit, load_layer, load_expert, evict_layer, evict_expert, cap: int) -> int:
+    n = _I()
+    _check(load().moe_policy_route_token(h, _np_ptr(ids), ids.shape[0], ids.shape[1], _np_ptr(hit),
+                                         _np_ptr(load_layer), _np_ptr(load_expert), _np_ptr(evict_layer),
+                                         _np_ptr(evict_expert), cap, ctypes.byref(n)))
     return n.value
 
 

@@ -47,6 +47,14 @@ struct moe_policy {
     std::vector<Rec> heap;
     std::vector<std::pair<int, unsigned>> zheap;
     std::vector<unsigned> ver;
+    // accessed pairs inside the recency guard wait here, on the token their guard
+    // ends, and join the heap then: the heap holds unguarded pairs only
+    struct Held {
+        long long release;
+        int k;
+        unsigned v;
+    };
+    std::vector<Held> held;
     // LFU with swaps
     std::vector<float> cnt;
     long long token = 0;
@@ -109,22 +117,50 @@ void zheap_push(moe_policy *p, int k, unsigned v) {
     std::push_heap(p->zheap.begin(), p->zheap.end(), std::greater<std::pair<int, unsigned>>());
 }
 
+struct HeldAfter {  // earliest release on top
+    bool operator()(const moe_policy::Held &a, const moe_policy::Held &b) const { return a.release > b.release; }
+};
+
+bool guarded_now(const moe_policy *p, int k) {
+    return p->last[k] >= 0 && p->token - p->last[k] < p->pr.recency_guard;
+}
+
+double df_key(const moe_policy *p, int k) { return std::log2(p->score[k]) + (double)p->tau[k] / p->pr.half_life; }
+
+// File resident pair k (version v) where it belongs now: held while inside the guard,
+// else the heap (accessed) or the never-accessed heap.
+void df_place(moe_policy *p, int k, unsigned v) {
+    if (guarded_now(p, k)) {
+        p->held.push_back({p->last[k] + p->pr.recency_guard, k, v});
+        std::push_heap(p->held.begin(), p->held.end(), HeldAfter());
+    } else if (p->score[k] > 0.0) {
+        heap_push(p, {df_key(p, k), k, v});
+    } else {
+        zheap_push(p, k, v);
+    }
+}
+
 // (Re)file resident pair k of the decayed-frequency policy after its score changed or
 // it became resident; stale records are dropped when they reach the top, and the
-// heaps are rebuilt from the resident list when stale records pile up.
+// structures are rebuilt from the resident list when stale records pile up.
 void df_file(moe_policy *p, int k) {
     if (p->pr.kind != MOE_POLICY_DECAYED_FREQ || !p->res[k]) return;
-    const unsigned v = ++p->ver[k];
-    if (p->score[k] > 0.0) heap_push(p, {std::log2(p->score[k]) + (double)p->tau[k] / p->pr.half_life, k, v});
-    else zheap_push(p, k, v);
-    if (p->heap.size() + p->zheap.size() > 4 * (size_t)p->n_res + 256) {
+    df_place(p, k, ++p->ver[k]);
+    if (p->heap.size() + p->zheap.size() + p->held.size() > 4 * (size_t)p->n_res + 256) {
         p->heap.clear();
         p->zheap.clear();
-        for (int r : p->rlist) {
-            if (p->score[r] > 0.0)
-                heap_push(p, {std::log2(p->score[r]) + (double)p->tau[r] / p->pr.half_life, r, p->ver[r]});
-            else zheap_push(p, r, p->ver[r]);
-        }
+        p->held.clear();
+        for (int r : p->rlist) df_place(p, r, p->ver[r]);
+    }
+}
+
+// The token advanced: pairs whose guard has ended join the heap.
+void df_release(moe_policy *p) {
+    while (!p->held.empty() && p->held.front().release <= p->token) {
+        const moe_policy::Held h = p->held.front();
+        std::pop_heap(p->held.begin(), p->held.end(), HeldAfter());
+        p->held.pop_back();
+        if (h.v == p->ver[h.k] && p->res[h.k]) heap_push(p, {df_key(p, h.k), h.k, h.v});
     }
 }
 
@@ -151,10 +187,6 @@ double fpow(moe_policy *p, long long d) {
 }
 
 double decayed(moe_policy *p, int k) { return p->score[k] * fpow(p, p->token - p->tau[k]); }
-
-bool guarded_now(const moe_policy *p, int k) {
-    return p->last[k] >= 0 && p->token - p->last[k] < p->pr.recency_guard;
-}
 
 // The decayed-frequency order: lower decayed score; equal scores to the least
 // recently used, then the lower pair.
@@ -189,45 +221,44 @@ int heap_victim(moe_policy *p) {
         for (const auto &r : back) zheap_push(p, r.first, r.second);
         if (victim >= 0) return victim;
     }
+    // unguarded accessed pairs: the heap holds exactly these (held pairs join it when
+    // their guard ends), so the event's own pairs are the only ones passed over
     constexpr double kSlack = 1e-6;  // in log2 units: a factor of 1 + 6.9e-7
     constexpr int kMaxSkip = 64;     // more passed-over pairs than this: the scan is cheaper
-    for (int guarded = 1; guarded >= 0; --guarded) {
-        std::vector<moe_policy::Rec> back;
-        int best = -1, skipped = 0;
-        double bs = 0.0, k0 = 0.0;
-        bool have = false, scan = false;
-        while (!p->heap.empty()) {
-            const moe_policy::Rec r = p->heap.front();
-            if (have && r.key > k0 + kSlack * (1.0 + std::fabs(k0))) break;
-            std::pop_heap(p->heap.begin(), p->heap.end(), RecAfter());
-            p->heap.pop_back();
-            const int k = r.k;
-            if (r.v != p->ver[k] || !p->res[k]) continue;  // stale
-            back.push_back(r);
-            if (p->mark[k] || (guarded && guarded_now(p, k))) {
-                // a pool where most pairs sit in the event or the guard (a small pool
-                // under heavy turnover): hand the search to the scan
-                if (++skipped > kMaxSkip) {
-                    scan = true;
-                    break;
-                }
-                continue;
+    std::vector<moe_policy::Rec> back;
+    int best = -1, skipped = 0;
+    double bs = 0.0, k0 = 0.0;
+    bool have = false, scan = false;
+    while (!p->heap.empty()) {
+        const moe_policy::Rec r = p->heap.front();
+        if (have && r.key > k0 + kSlack * (1.0 + std::fabs(k0))) break;
+        std::pop_heap(p->heap.begin(), p->heap.end(), RecAfter());
+        p->heap.pop_back();
+        const int k = r.k;
+        if (r.v != p->ver[k] || !p->res[k]) continue;  // stale
+        back.push_back(r);
+        if (p->mark[k] || guarded_now(p, k)) {
+            if (++skipped > kMaxSkip) {
+                scan = true;
+                break;
             }
-            if (!have) {
-                have = true;
-                k0 = r.key;
-            }
-            const double s = decayed(p, k);
-            if (df_before(p, k, s, best, bs)) {
-                best = k;
-                bs = s;
-            }
+            continue;
         }
-        for (const auto &r : back) heap_push(p, r);
-        if (scan) return scan_victim(p);
-        if (best >= 0) return bs >= std::numeric_limits<double>::min() ? best : scan_victim(p);
+        if (!have) {
+            have = true;
+            k0 = r.key;
+        }
+        const double s = decayed(p, k);
+        if (df_before(p, k, s, best, bs)) {
+            best = k;
+            bs = s;
+        }
     }
-    return -1;
+    for (const auto &r : back) heap_push(p, r);
+    if (!scan && best >= 0 && bs >= std::numeric_limits<double>::min()) return best;
+    // underflowed scores, or every pair outside the event inside the guard (then the
+    // guarded ones compete): the scan decides
+    return scan_victim(p);
 }
 
 // Victim for a load, or -1: never a pair of the event being served.
@@ -257,6 +288,59 @@ int scan_victim(moe_policy *p) {
         if (best >= 0) return best;
     }
     return -1;
+}
+
+// One routing event (arguments checked by the caller): hits, then for the demand
+// policies the loads with their victims, appended at the given plan pointers
+// (load_layer may be NULL); returns the number of loads.
+int route_event(moe_policy *p, int layer, const int32_t *ids, int n, uint8_t *hit, int32_t *load_layer,
+                int32_t *load_expert, int32_t *evict_layer, int32_t *evict_expert) {
+    // the event's distinct pairs, in event order
+    std::vector<int> ev;
+    ev.reserve(n);
+    for (int i = 0; i < n; ++i) {
+        const int k = layer * p->E + ids[i];
+        if (hit) hit[i] = p->res[k];
+        if (p->mark[k]) continue;
+        p->mark[k] = 1;
+        ev.push_back(k);
+    }
+    int nl = 0;
+    if (p->pr.kind == MOE_POLICY_LFU_SWAP) {
+        for (int k : ev) p->cnt[k] += 1.0f;
+    } else {
+        for (int k : ev) {
+            if (p->pr.kind == MOE_POLICY_LRU) {
+                if (p->res[k]) {
+                    lru_unlink(p, k);
+                    lru_push_front(p, k);
+                }
+            } else {
+                p->score[k] = p->score[k] * fpow(p, p->token - p->tau[k]) + 1.0;
+                p->tau[k] = p->token;
+                p->last[k] = p->token;
+                p->stamp[k] = ++p->clock;
+                df_file(p, k);
+            }
+        }
+        for (int k : ev) {
+            if (p->res[k]) continue;
+            int victim = -1;
+            if (p->n_res >= p->pr.capacity) {
+                victim = pick_victim(p);
+                if (victim < 0) continue;  // the pool holds only this event's experts
+                make_absent(p, victim);
+            }
+            make_resident(p, k);
+            if (load_layer) load_layer[nl] = layer;
+            load_expert[nl] = k % p->E;
+            evict_layer[nl] = victim < 0 ? -1 : victim / p->E;
+            evict_expert[nl] = victim < 0 ? -1 : victim % p->E;
+            ++nl;
+        }
+    }
+    for (int k : ev) p->mark[k] = 0;
+    return nl;
 }
 
 }  // namespace
@@ -332,50 +416,29 @@ MOE_API int moe_policy_route(moe_policy *p, int layer, const int32_t *ids, int n
     const bool demand = p->pr.kind != MOE_POLICY_LFU_SWAP;
     if (demand && (!load_expert || !evict_layer || !evict_expert || !n_loads))
         return set_error(MOE_ERR_ARG, "null plan buffers");
-    // the event's distinct pairs, in event order
-    std::vector<int> ev;
-    ev.reserve(n);
-    for (int i = 0; i < n; ++i) {
-        const int k = layer * p->E + ids[i];
-        if (hit) hit[i] = p->res[k];
-        if (p->mark[k]) continue;
-        p->mark[k] = 1;
-        ev.push_back(k);
-    }
+    const int nl = route_event(p, layer, ids, n, hit, nullptr, load_expert, evict_layer, evict_expert);
+    if (n_loads) *n_loads = nl;
+    return MOE_OK;
+}
+
+MOE_API int moe_policy_route_token(moe_policy *p, const int32_t *ids, int n_layers, int K, uint8_t *hit,
+                                   int32_t *load_layer, int32_t *load_expert, int32_t *evict_layer,
+                                   int32_t *evict_expert, int cap, int *n_loads) {
+    if (!p || n_layers < 0 || K < 0 || ((long long)n_layers * K > 0 && !ids))
+        return set_error(MOE_ERR_ARG, "null argument or negative size");
+    if (n_layers > p->L) return set_error(MOE_ERR_ARG, "%d layers routed, the policy has %d", n_layers, p->L);
+    const long long total = (long long)n_layers * K;
+    for (long long i = 0; i < total; ++i)
+        if (ids[i] < 0 || ids[i] >= p->E) return set_error(MOE_ERR_ARG, "expert %d out of range", ids[i]);
+    const bool demand = p->pr.kind != MOE_POLICY_LFU_SWAP;
+    if (demand && (!load_layer || !load_expert || !evict_layer || !evict_expert || !n_loads))
+        return set_error(MOE_ERR_ARG, "null plan buffers");
+    if (demand && cap < total) return set_error(MOE_ERR_ARG, "cap %d < n_layers * K = %lld", cap, total);
     int nl = 0;
-    if (p->pr.kind == MOE_POLICY_LFU_SWAP) {
-        for (int k : ev) p->cnt[k] += 1.0f;
-    } else {
-        for (int k : ev) {
-            if (p->pr.kind == MOE_POLICY_LRU) {
-                if (p->res[k]) {
-                    lru_unlink(p, k);
-                    lru_push_front(p, k);
-                }
-            } else {
-                p->score[k] = p->score[k] * fpow(p, p->token - p->tau[k]) + 1.0;
-                p->tau[k] = p->token;
-                p->last[k] = p->token;
-                p->stamp[k] = ++p->clock;
-                df_file(p, k);
-            }
-        }
-        for (int k : ev) {
-            if (p->res[k]) continue;
-            int victim = -1;
-            if (p->n_res >= p->pr.capacity) {
-                victim = pick_victim(p);
-                if (victim < 0) continue;  // the pool holds only this event's experts
-                make_absent(p, victim);
-            }
-            make_resident(p, k);
-            load_expert[nl] = k % p->E;
-            evict_layer[nl] = victim < 0 ? -1 : victim / p->E;
-            evict_expert[nl] = victim < 0 ? -1 : victim % p->E;
-            ++nl;
-        }
-    }
-    for (int k : ev) p->mark[k] = 0;
+    for (int l = 0; l < n_layers; ++l)
+        nl += route_event(p, l, ids + (size_t)l * K, K, hit ? hit + (size_t)l * K : nullptr,
+                          demand ? load_layer + nl : nullptr, demand ? load_expert + nl : nullptr,
+                          demand ? evict_layer + nl : nullptr, demand ? evict_expert + nl : nullptr);
     if (n_loads) *n_loads = nl;
     return MOE_OK;
 }
@@ -385,6 +448,7 @@ MOE_API int moe_policy_end_token(moe_policy *p, int32_t *load_layer, int32_t *lo
     if (!p) return set_error(MOE_ERR_ARG, "null argument");
     int ns = 0;
     ++p->token;
+    if (p->pr.kind == MOE_POLICY_DECAYED_FREQ) df_release(p);
     if (p->pr.kind == MOE_POLICY_LFU_SWAP) {
         if (p->token % p->pr.swap_every == 0) {
             struct Swap {

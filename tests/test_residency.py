@@ -188,3 +188,59 @@ def test_engine_belady_matches_reference(seed, cap):
     assert L.moe_policy_belady(tr, 40, cap) == R.belady_hits(events, cap)
     seq = np.array([7, 0, 1, 2, 0, 3, 0, 4, 2, 3, 0, 3, 2], dtype=np.int32).reshape(-1, 1, 1)
     assert L.moe_policy_belady(seq, 8, 3) == 6
+
+
+# ------------------------------------------------------------------ a whole token per call
+
+@pytest.mark.parametrize("kind,kw", [(L.POLICY_LRU, {}), (L.POLICY_DECAYED_FREQ, {"half_life": 4.0}),
+                                     (L.POLICY_DECAYED_FREQ, {"half_life": 1.0, "recency_guard": 0}),
+                                     (L.POLICY_LFU_SWAP, {"swap_every": 2, "max_swaps": 5})])
+@pytest.mark.parametrize("seeded", [False, True])
+def test_route_token_equals_per_layer_routes(kind, kw, seeded):
+    tr = traces.routing_trace(40, 6, 24, 4, seed=21 + kind)
+    a = L.Policy(L.policy_params(kind, 30, **kw), 6, 24)
+    b = L.Policy(L.policy_params(kind, 30, **kw), 6, 24)
+    try:
+        if seeded:
+            prof = traces.profile_ranking(tr[:5])
+            assert a.seed(*prof) == b.seed(*prof)
+        for t in range(40):
+            hits, plan = [], [[], [], [], []]
+            for l in range(6):
+                h, le, el, ee = a.route(l, tr[t, l])
+                hits.append(h)
+                for lst, vals in zip(plan, (np.full(le.size, l, np.int32), le, el, ee)):
+                    lst.extend(int(v) for v in vals)
+            hb, ll, le, el, ee = b.route_token(tr[t])
+            assert np.array_equal(hb, np.stack(hits))
+            assert [list(map(int, x)) for x in (ll, le, el, ee)] == plan
+            sa, sb = a.end_token(), b.end_token()
+            assert all(np.array_equal(x, y) for x, y in zip(sa, sb))
+        assert a.count() == b.count()
+        assert all(a.resident(l, e) == b.resident(l, e) for l in range(6) for e in range(24))
+    finally:
+        a.close()
+        b.close()
+
+
+def test_route_token_checks_before_changing_anything():
+    p = L.Policy(L.policy_params(L.POLICY_LRU, 8), 3, 16)
+    try:
+        p.route_token(np.array([[0, 1], [2, 3], [4, 5]], dtype=np.int32))
+        assert p.count() == 6
+        bad = np.array([[6, 7], [8, 9], [10, 16]], dtype=np.int32)  # the last id is out of range
+        with pytest.raises(L.MoeError):
+            p.route_token(bad)
+        assert p.count() == 6 and not p.resident(0, 6)
+        with pytest.raises(L.MoeError):
+            p.route_token(np.zeros((4, 2), dtype=np.int32))  # more layers than the policy has
+        ids = np.array([[6, 7]], dtype=np.int32)
+        hit = np.zeros((1, 2), np.uint8)
+        short = [np.zeros(1, np.int32) for _ in range(4)]
+        with pytest.raises(L.MoeError):
+            L.moe_policy_route_token(p.h, ids, hit, *short, 1)  # cap below n_layers * K
+        assert p.count() == 6
+        hit, ll, le, el, ee = p.route_token(np.zeros((0, 2), dtype=np.int32))
+        assert hit.shape == (0, 2) and ll.size == 0 and p.count() == 6
+    finally:
+        p.close()
