@@ -243,6 +243,8 @@ def run_residency(L, torch, ctx):
     return {"trace": f"sticky Zipf(1.1) routing, {Ln} layers x {E} experts, top-{K}, {T_rep} tokens replayed "
                      f"after a {T_prof}-token profile seeds the pool; adjacent tokens share "
                      f"{traces.sharing(rep):.0%} of a layer's experts",
+            "us_per_event": "host time per routing event, a token's 48 events routed in one "
+                            "moe_policy_route_token call (swap rounds included)",
             "replay": rows,
             "load": {"what": f"{n} Q2_0 experts ({eb:,} B each) evicted and reloaded through moe_policy_apply "
                              "from pinned host memory (copy, repack, publish)",
