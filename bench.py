@@ -55,8 +55,8 @@ def parse():
     return ap.parse_args()
 
 
-# DRAM traffic of k_decode per layer from one ncu capture (profiles/k_decode_q2_stack48_T1.md:
-# 4-layer chain, T=1, dram__bytes_read.sum + dram__bytes_write.sum = 65,948,928 + 917,760 B);
+# DRAM traffic of k_decode per layer from one ncu capture of a 4-layer chain at T=1
+# (dram__bytes_read.sum + dram__bytes_write.sum = 65,946,112 + 1,005,312 B);
 # traffic grows in proportion to the layers. It holds only for the kernel sources it
 # was taken on: any change to them makes the figure stale, and it is reported as null.
 TRAFFIC_REF = {"T": 1, "bytes_per_layer": (65_946_112 + 1_005_312) / 4,

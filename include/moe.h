@@ -152,17 +152,6 @@ MOE_API int moe_ctx_get_option(moe_ctx *ctx, int option, int *value);
  * stays usable (the call's outputs are then undefined). Nothing faults or traps. */
 #define MOE_OPT_TEST_SKIP_ARRIVAL 4
 
-/* MOE_OPT_UMMA_PAIR (default 0, settable): 1 runs the tensor-core grouped GEMMs
- * of prefill windows (MOE_OPT_PREFILL_MIN_T) with each 256-row weight tile on a
- * pair of CTAs (a cluster of two, cta_group::2, M = 256): each CTA stages its own
- * 128 weight rows and half of the tile's token columns, and one of them issues the
- * MMAs for both. 0 runs one CTA per 128-row tile. Both give the same bits (every
- * output element is the same fp32 sum over K in the same order). On a GB300 the
- * pairs are slower on the 4,096-token Gemma-shaped layer (1.27 against 0.90 ms):
- * their stages wait on handshakes between the two SMs. The router GEMM always runs
- * one CTA per tile. */
-#define MOE_OPT_UMMA_PAIR 5
-
 /* Synchronise `stream`, then read and clear the device status bits into *bits.
  * Returns MOE_OK even when bits are set; the caller inspects them. */
 MOE_API int moe_status(moe_ctx *ctx, moe_stream_t stream, uint32_t *bits);
@@ -421,7 +410,8 @@ MOE_API int moe_policy_create(const moe_policy_params *params, int n_layers, int
 MOE_API int moe_policy_destroy(moe_policy *p);
 
 /* Make the listed pairs resident without counting accesses (a shipped profile),
- * in list order, until the pool is full; returns how many were placed in *n_placed. */
+ * in list order, until the pool is full; returns how many were placed in *n_placed.
+ * Every pair is checked first: one out of range gives MOE_ERR_ARG and places none. */
 MOE_API int moe_policy_seed(moe_policy *p, const int32_t *layers, const int32_t *experts, int n,
                             int *n_placed);
 

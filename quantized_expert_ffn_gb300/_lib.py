@@ -164,7 +164,6 @@ OPT_PERSISTENT_DECODE = 1
 OPT_LAST_PATH = 2
 OPT_PREFILL_MIN_T = 3
 OPT_TEST_SKIP_ARRIVAL = 4
-OPT_UMMA_PAIR = 5
 
 
 def moe_ctx_set_option(ctx: int, option: int, value: int):

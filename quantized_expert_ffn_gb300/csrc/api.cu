@@ -18,7 +18,6 @@ struct moe_ctx {
     int prefill_min;  // MOE_OPT_PREFILL_MIN_T
     int max_smem;    // opt-in shared memory per block
     int fault_layer;  // MOE_OPT_TEST_SKIP_ARRIVAL (-1: off)
-    int umma_pair;    // MOE_OPT_UMMA_PAIR
 };
 
 struct moe_arena {
@@ -174,7 +173,7 @@ int check_ws(void *ws, size_t ws_bytes, size_t need) {
 int router_logits(moe_ctx *ctx, const void *x, moe_dtype xt, int T, int H, const void *Wr, moe_dtype wt,
                   const float *bias, const float *router_scale, int E, float *logits, cudaStream_t s) {
     if (!router_scale && T >= ctx->prefill_min && xt == MOE_BF16 && wt == MOE_BF16 && umma_router_supported(H) &&
-        umma_fits(ctx->max_smem, false) && (uintptr_t)x % 16 == 0 && (uintptr_t)Wr % 16 == 0) {
+        umma_fits(ctx->max_smem) && (uintptr_t)x % 16 == 0 && (uintptr_t)Wr % 16 == 0) {
         int sms = 0;
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device));
         UmmaArgs ua;
@@ -196,7 +195,7 @@ int router_logits(moe_ctx *ctx, const void *x, moe_dtype xt, int T, int H, const
                                    (unsigned long long)H * 2, 128);
         if (rc) return rc;
         const int tiles = ua.n_mt * ((T + 63) / 64);
-        return launch_umma(ua, tiles < sms ? tiles : sms, false, s);
+        return launch_umma(ua, tiles < sms ? tiles : sms, s);
     }
     return launch_router_logits(x, xt, T, H, Wr, wt, bias, router_scale, E, logits, s);
 }
@@ -221,7 +220,7 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
     // up to 256 live pairs; otherwise the mma.sync kernels on groups of 8 (4) columns
     const bool umma = T >= ctx->prefill_min && umma_supported(sl->layout) &&
                       (!d->shared || umma_supported(d->shared->layout)) &&
-                      umma_fits(ctx->max_smem, false);
+                      umma_fits(ctx->max_smem);
     const int nc_gu = umma ? 256 : (xt == MOE_F32 ? 4 : 8);
     PlanArgs pa;
     pa.ids = ids;
@@ -280,9 +279,7 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
         if (rc) return rc;
         int sms = 0;
         MOE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device));
-        // CTA pairs (M = 256 per tile, half of B per CTA) where their shared memory fits
-        const bool pair = ctx->umma_pair && umma_fits(ctx->max_smem, true);
-        const int box0 = pair ? 8 : 16, box_big = pair ? 128 : 256;
+        const int box0 = 16, box_big = 256;
         UmmaArgs ua;
         memset(&ua, 0, sizeof ua);
         ua.mode = 0;
@@ -310,7 +307,7 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
         if (!rc) rc = make_packed_maps(&ua.pk[0], 0, sl->layout, sl->base, (long long)sl->stride, sl->capacity);
         if (!rc && d->shared) rc = make_packed_maps(&ua.pk[2], 0, d->shared->layout, ea.src.shared, 0, 1);
         if (rc) return rc;
-        rc = launch_umma(ua, sms, pair, s);
+        rc = launch_umma(ua, sms, s);
         if (rc) return rc;
         rc = make_tmap_2d(&ua.tmap_b, ua.h16, false, (unsigned long long)maxc, (unsigned long long)W.h_ld,
                           (unsigned long long)W.h_ld * 2, box_big);
@@ -326,7 +323,7 @@ int run_experts(moe_ctx *ctx, const moe_layer_desc *d, const void *x, moe_dtype 
         ua.max_routed = W.max_routed_d;
         ua.n_mt = sl->layout.H / 128;
         ua.n_mt_s = d->shared ? d->shared->layout.H / 128 : 0;
-        rc = launch_umma(ua, sms, pair, s);
+        rc = launch_umma(ua, sms, s);
         if (rc) return rc;
         ctx->last_path = 2;
         return launch_combine(ea.yp, w, pa.live, T, d->K, d->H, d->shared != nullptr, accumulate, y, s);
@@ -526,7 +523,7 @@ int moe_ctx_create(int device, moe_ctx **out) {
         return set_error(MOE_ERR_CUDA, "no CUDA device %d (%d visible)", device, n);
     DeviceGuard g(device);
     if (!g.ok) return set_error(MOE_ERR_CUDA, "cudaSetDevice(%d) failed", device);
-    moe_ctx *c = new moe_ctx{device, nullptr, 1, 0, 64, 0, -1, 0};
+    moe_ctx *c = new moe_ctx{device, nullptr, 1, 0, 64, 0, -1};
     cudaError_t e = cudaMalloc(&c->d_status, sizeof(uint32_t));
     if (e != cudaSuccess) {
         delete c;
@@ -587,10 +584,6 @@ int moe_ctx_set_option(moe_ctx *ctx, int option, int value) {
         ctx->fault_layer = value;
         return MOE_OK;
     }
-    if (option == MOE_OPT_UMMA_PAIR) {
-        ctx->umma_pair = value != 0;
-        return MOE_OK;
-    }
     return set_error(MOE_ERR_ARG, "unknown option %d", option);
 }
 
@@ -610,10 +603,6 @@ int moe_ctx_get_option(moe_ctx *ctx, int option, int *value) {
     }
     if (option == MOE_OPT_TEST_SKIP_ARRIVAL) {
         *value = ctx->fault_layer;
-        return MOE_OK;
-    }
-    if (option == MOE_OPT_UMMA_PAIR) {
-        *value = ctx->umma_pair;
         return MOE_OK;
     }
     return set_error(MOE_ERR_ARG, "unknown option %d", option);

@@ -28,13 +28,9 @@
 //      writes h as fp16 (row = plan column); down tiles write fp32 y_pair rows.
 //
 // A tile is (column group of <= 256 live pairs of one expert, 128-row M-tile);
-// CTAs (one per SM) take tiles round-robin. A second form (k_umma<true>, off by
-// default) runs a cluster of two CTAs per pair of M-tiles with cta_group::2
-// (M = 256): each CTA dequantises its own 128 rows and loads half of the group's
-// columns, rank 0 issues the MMAs and commits to the barriers of both; it gives the
-// same bits and was measured slower. Every barrier wait gives up after about a
-// second (MOE_STATUS_TIMEOUT) and the CTA stops; the TMEM it allocated is released
-// on every path.
+// CTAs (one per SM) take tiles round-robin. Every barrier wait gives up after about
+// a second (MOE_STATUS_TIMEOUT) and the CTA stops; the TMEM it allocated is
+// released on every path.
 #include <cudaTypedefs.h>
 
 #include "decode_common.cuh"
@@ -58,20 +54,17 @@ constexpr int kPacked = 9216;              // packed codes + scales of one 128-k
 constexpr int kTmemCols = 512;             // two 256-column fp32 accumulators
 constexpr long long kSpin = 2000000000LL;  // about 1 s
 
-// Shared-memory plan. One CTA per tile (PAIR false): A and B rings of 4 stages, a B
-// stage holding the tile's 256 columns (32 KB). A CTA pair per tile (PAIR true,
-// cta_group::2, M = 256): each CTA holds its own 128 weight rows and half of the
-// columns, so a B stage is 16 KB and both rings get 6 stages in the same space.
-template <bool PAIR>
+// Shared-memory plan: A and B rings of 4 stages, a B stage holding the tile's 256
+// columns (32 KB), and the packed-weight ring.
 struct Plan {
-    static constexpr int kAStages = PAIR ? 6 : 4, kBStages = PAIR ? 6 : 4;
-    static constexpr int kBoxRows = PAIR ? kBN / 2 : kBN;  // rows of a CTA's largest B box
+    static constexpr int kAStages = 4, kBStages = 4;
+    static constexpr int kBoxRows = kBN;  // rows of the largest B box
     static constexpr int kBTile = kBoxRows * kBK * 2;
-    static constexpr int kTileCache = PAIR ? 64 : 96;      // tile descriptors staged per CTA
+    static constexpr int kTileCache = 96;  // tile descriptors staged per CTA
     static constexpr size_t kSmemA = 0;
     static constexpr size_t kSmemB = kSmemA + (size_t)kAStages * kATile;
     static constexpr size_t kSmemP = kSmemB + (size_t)kBStages * kBTile;
-    static constexpr size_t kSmemBytes = kSmemP + (size_t)kPSlots * kPacked;  // 219,136 / 224,256
+    static constexpr size_t kSmemBytes = kSmemP + (size_t)kPSlots * kPacked;  // 219,136
     static_assert(kSmemB % 1024 == 0 && kSmemP % 16 == 0, "swizzled tiles need 1024-byte alignment");
 };
 
@@ -91,7 +84,7 @@ __device__ __forceinline__ uint64_t sdesc(unsigned addr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B both fp16 (bf16 when
-// `bf16`), both K-major, M = m (128; 256 for a CTA pair), N = n (multiple of 16, <= 256).
+// `bf16`), both K-major, M = m (128), N = n (multiple of 16, <= 256).
 __device__ __forceinline__ uint32_t idesc_f16(int n, bool bf16, int m) {
     const uint32_t ab = bf16 ? 1u : 0u;
     return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
@@ -131,57 +124,6 @@ __device__ __forceinline__ void tma_box3(void *dst, const CUtensorMap *map, int 
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
         "[%5];" ::"r"(su32(dst)),
         "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(su32(m))
-        : "memory");
-}
-
-// ---- CTA pairs: clusters of two CTAs; rank 0 issues the MMAs of both (cta_group::2)
-__device__ __forceinline__ int cluster_rank() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return (int)r;
-}
-__device__ __forceinline__ int cluster_index() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return (int)r;
-}
-__device__ __forceinline__ int cluster_count() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return (int)r;
-}
-// Cluster address of the same shared-memory object in CTA `rank` of the cluster.
-__device__ __forceinline__ unsigned map_rank(const void *p, int rank) {
-    unsigned r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(su32(p)), "r"(rank));
-    return r;
-}
-// Arrival (release at cluster scope) on a barrier given by its cluster address.
-__device__ __forceinline__ void mbar_arrive_cluster(unsigned addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-// Phase check with acquire at cluster scope (for barriers the other CTA arrives on).
-__device__ __forceinline__ bool mbar_try_cluster(uint64_t *m, unsigned parity) {
-    unsigned ok;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
-        "selp.u32 %0, 1, 0, p; }"
-        : "=r"(ok)
-        : "r"(su32(m)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Every thread of both CTAs of the cluster.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// One box of a 2-D tensor map into this CTA's shared memory, completing on the
-// barrier at cluster address `mbar` (rank 0's, for both CTAs of a pair).
-__device__ __forceinline__ void tma_box_pair(void *dst, const CUtensorMap *map, int c0, int c1, unsigned mbar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
-        "[%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
-        "l"(map), "r"(c0), "r"(c1), "r"(mbar)
         : "memory");
 }
 
@@ -243,19 +185,10 @@ __device__ __forceinline__ float act_fast(int act, float g) {
     return __fdividef(g, 1.0f + __expf(-g));
 }
 
-// The completion of every MMA this thread has issued arrives on `bar`; pairs: on the
-// barrier at the same offset in both CTAs of the cluster.
-template <bool PAIR>
+// The completion of every MMA this thread has issued arrives on `bar`.
 __device__ __forceinline__ void commit_to(uint64_t *bar) {
-    if (PAIR)
-        asm volatile(
-            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                su32(bar)),
-            "h"((unsigned short)3)
-            : "memory");
-    else
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
-                     : "memory");
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+                 : "memory");
 }
 
 // 32 consecutive accumulator columns of this warp's 32 TMEM lanes, waited for.
@@ -273,57 +206,38 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t v[32]) {
 
 // One K = 64 stage: four MMAs of K = 16 (descriptor start +2 = +32 bytes per step);
 // the first accumulates onto D only when `acc`, the others always.
-template <bool PAIR>
 __device__ __forceinline__ void mma_k64(uint32_t dt, uint64_t da, uint64_t db, uint32_t idesc, bool acc) {
-    if (PAIR) {
-        asm volatile(
-            "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
-            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
-            "l"(da), "l"(db), "r"(idesc), "r"(acc ? 1u : 0u)
-            : "memory");
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
+        "l"(da), "l"(db), "r"(idesc), "r"(acc ? 1u : 0u)
+        : "memory");
 #pragma unroll
-        for (int kk = 1; kk < kBK / 16; ++kk)
-            asm volatile("{ .reg .pred p; setp.ne.b32 p, 1, 0; tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
-                         "l"(da + (uint64_t)(2 * kk)), "l"(db + (uint64_t)(2 * kk)), "r"(idesc)
-                         : "memory");
-    } else {
-        asm volatile(
-            "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
-            "l"(da), "l"(db), "r"(idesc), "r"(acc ? 1u : 0u)
-            : "memory");
-#pragma unroll
-        for (int kk = 1; kk < kBK / 16; ++kk)
-            asm volatile("{ .reg .pred p; setp.ne.b32 p, 1, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
-                         "l"(da + (uint64_t)(2 * kk)), "l"(db + (uint64_t)(2 * kk)), "r"(idesc)
-                         : "memory");
-    }
+    for (int kk = 1; kk < kBK / 16; ++kk)
+        asm volatile("{ .reg .pred p; setp.ne.b32 p, 1, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(dt),
+                     "l"(da + (uint64_t)(2 * kk)), "l"(db + (uint64_t)(2 * kk)), "r"(idesc)
+                     : "memory");
 }
 
 struct TileInfo {
     Group grp;
     int mt;
     bool shared;
-    bool mvalid;  // the M-tile lies inside the weights (a pair's second tile can lie past an odd count)
-    int nk;       // K stages
+    int nk;  // K stages
 };
 
-// Tile t of one launch. One CTA per tile: t = (group, M-tile). CTA pairs: t = (group,
-// pair of M-tiles 2j, 2j + 1), CTA rank r taking M-tile 2j + r.
-template <bool PAIR>
-__device__ __forceinline__ bool tile_info(const UmmaArgs &a, int n_routed, int t, int rank, TileInfo &ti) {
+// Tile t of one launch: t = (group, M-tile).
+__device__ __forceinline__ bool tile_info(const UmmaArgs &a, int n_routed, int t, TileInfo &ti) {
     if (a.mode == 2) {
         // router: tile t = (128 experts mt, kRN tokens nt)
         const int mt = t % a.n_mt, nt = t / a.n_mt;
         ti.grp = Group{-1, kRN * nt, min(kRN, a.T - kRN * nt), 0};
         ti.mt = mt;
         ti.shared = false;
-        ti.mvalid = true;
         ti.nk = a.H / kBK;
         return ti.grp.ncols > 0;
     }
-    const int mp = PAIR ? (a.n_mt + 1) / 2 : a.n_mt;
-    const int mps = PAIR ? (a.n_mt_s + 1) / 2 : a.n_mt_s;
+    const int mp = a.n_mt, mps = a.n_mt_s;
     const int nr = n_routed * mp;
     int j;
     if (t < nr) {
@@ -337,16 +251,14 @@ __device__ __forceinline__ bool tile_info(const UmmaArgs &a, int n_routed, int t
         j = t2 % mps;
         ti.shared = true;
     }
-    ti.mt = PAIR ? 2 * j + rank : j;
-    ti.mvalid = ti.mt < (ti.shared ? a.n_mt_s : a.n_mt);
+    ti.mt = j;
     const QLayout &L = ti.shared ? a.src.LS : a.src.L;
     ti.nk = (a.mode == 0 ? L.H : L.F) / kBK;
     return true;
 }
 
-template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ UmmaArgs a) {
-    using Pl = Plan<PAIR>;
+    using Pl = Plan;
     constexpr int kAS = Pl::kAStages, kBS = Pl::kBStages;
     extern __shared__ uint8_t smem_raw[];
     static_assert(kAS == kBS, "one barrier pair per stage serves both rings");
@@ -359,28 +271,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
     __shared__ TileInfo tiles_s[Pl::kTileCache];  // this CTA's tiles (the first kTileCache of them)
     uint8_t *const sm = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (PAIR && a.mode == 2) {  // the router runs one CTA per tile only
-        if (tid == 0) set_status(a.status, MOE_STATUS_BOUNDS);
-        return;
-    }
-    // one CTA per tile: CTA b takes tiles b, b + G, ...; pairs: cluster c takes c, c + G, ...
-    const int rank = PAIR ? cluster_rank() : 0;
-    const bool leader = rank == 0;  // the CTA that issues the MMAs
-    const int G = PAIR ? cluster_count() : (int)gridDim.x;
-    const int wid = PAIR ? cluster_index() : (int)blockIdx.x;
+    // CTA b takes tiles b, b + G, ...
+    const int G = (int)gridDim.x;
+    const int wid = (int)blockIdx.x;
     const int n_routed = a.mode == 2 ? 0 : *a.n_groups;
-    const int mp = PAIR ? (a.n_mt + 1) / 2 : a.n_mt, mps = PAIR ? (a.n_mt_s + 1) / 2 : a.n_mt_s;
+    const int mp = a.n_mt, mps = a.n_mt_s;
     const int n_tiles = a.mode == 2 ? a.n_mt * ((a.T + kRN - 1) / kRN) : n_routed * mp + a.n_shared * mps;
     const int P = a.T * a.K;
 
     if (tid == 0) {
-        // pairs: rank 0's fullA also takes one arrival per dequant warp of the other CTA,
-        // and its acce one per epilogue warp of the other CTA
         for (int s = 0; s < kAS; ++s) {
             // one "full" barrier per stage counts the A and the B side: the B thread's
-            // arrival with the stage's bytes (pairs: both CTAs' bytes, rank 0 only),
-            // then the dequant group's warps (the router: the A copy's arrival)
-            mbar_init(&fullA[s], a.mode == 2 ? 2 : kDqWarps / 2 + (PAIR ? kDqWarps / 2 : 0) + 1);
+            // arrival with the stage's bytes, then the dequant group's warps (the
+            // router: the A copy's arrival)
+            mbar_init(&fullA[s], a.mode == 2 ? 2 : kDqWarps / 2 + 1);
             mbar_init(&emptyA[s], 1);
         }
         for (int s = 0; s < kPSlots; ++s) {
@@ -389,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf_bar[b], 1);
-            mbar_init(&acce_bar[b], 32 * kEpiWarps + (PAIR ? kEpiWarps : 0));
+            mbar_init(&acce_bar[b], 32 * kEpiWarps);
         }
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -398,25 +302,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
     for (int i = tid; i < Pl::kTileCache; i += kThreads) {
         const int t = wid + G * i;
         TileInfo ti;
-        if (t < n_tiles && tile_info<PAIR>(a, n_routed, t, rank, ti)) tiles_s[i] = ti;
+        if (t < n_tiles && tile_info(a, n_routed, t, ti)) tiles_s[i] = ti;
     }
     if (warp == kMmaWarp) {
-        // pairs: one warp of each CTA allocates, collectively, the same columns in both
-        if (PAIR) {
-            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)),
-                         "r"(kTmemCols)
-                         : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-        } else {
-            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)),
-                         "r"(kTmemCols)
-                         : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-        }
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (PAIR) cluster_sync_all();  // both CTAs' barriers initialised before any remote arrival
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base;
 
@@ -426,16 +321,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
             ti = tiles_s[i];
             return true;
         }
-        return tile_info<PAIR>(a, n_routed, t, rank, ti);
+        return tile_info(a, n_routed, t, ti);
     };
 
-    // bounded wait on a barrier phase; on timeout every role of the CTA stops. `cl`:
-    // acquire at cluster scope (a barrier the other CTA of a pair arrives on)
-    auto wait = [&](uint64_t *m, unsigned parity, bool cl = false) -> bool {
-        auto probe = [&]() { return (PAIR && cl) ? mbar_try_cluster(m, parity) : mbar_try(m, parity); };
-        if (probe()) return true;
+    // bounded wait on a barrier phase; on timeout every role of the CTA stops
+    auto wait = [&](uint64_t *m, unsigned parity) -> bool {
+        if (mbar_try(m, parity)) return true;
         const long long t0 = clock64();
-        while (!probe()) {
+        while (!mbar_try(m, parity)) {
             if (*(volatile int *)&abort_flag) return false;
             if (clock64() - t0 > kSpin) {
                 atomicExch(&abort_flag, 1);
@@ -456,9 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         // ---------------------------------------------------------------- TMA warps
         // warp kTmaWarp: the packed chunk of stages s, s + 1 of each tile (HBM, up to
         // kPSlots chunks ahead); warp kTmaBWarp: the B rows of each stage (L2, up to
-        // kBStages ahead) and, for the router, the A rows. A pair splits a group's
-        // round-up(n, 16) columns in halves, rank r loading half r; both halves
-        // complete on rank 0's full barrier, whose TMA thread expects the bytes of both.
+        // kBStages ahead) and, for the router, the A rows.
         if (lane == 0) {
             const bool packed = warp == kTmaWarp;
             if (!packed) {
@@ -477,17 +368,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                 // B side, per tile: the smallest box holding this CTA's columns of the
                 // group (rows past them belong to the next group or read as zeros; the
                 // MMA's N stops at round-up(ncols, 16))
-                int bi = 4, r0 = ti.grp.col0;
+                int bi = 4;
+                const int r0 = ti.grp.col0;
                 if (a.mode != 2) {
-                    const int nr = (ti.grp.ncols + 15) & ~15;
-                    const int rows = PAIR ? nr / 2 : nr;
-                    const int lo = PAIR ? 8 : 16;
-                    bi = rows <= lo ? 0 : rows <= 2 * lo ? 1 : rows <= 4 * lo ? 2 : rows <= 8 * lo ? 3 : 4;
-                    if (PAIR) r0 += rank * (nr / 2);
+                    const int rows = (ti.grp.ncols + 15) & ~15;
+                    bi = rows <= 16 ? 0 : rows <= 32 ? 1 : rows <= 64 ? 2 : rows <= 128 ? 3 : 4;
                 }
                 const CUtensorMap *mb = bi < 4 ? &a.tmap_bn[bi] : &a.tmap_b;
-                const int box_rows = a.mode == 2 ? kRN : bi < 4 ? (PAIR ? 8 : 16) << bi : Pl::kBoxRows;
-                const unsigned bbytes = (unsigned)((PAIR ? 2 : 1) * box_rows * kBK * 2);
+                const int box_rows = a.mode == 2 ? kRN : bi < 4 ? 16 << bi : Pl::kBoxRows;
+                const unsigned bbytes = (unsigned)(box_rows * kBK * 2);
                 for (int s2 = 0; s2 < ti.nk && good; ++s2, ++it) {
                     if (packed) {
                         if (s2 & 1) continue;
@@ -497,9 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                             break;
                         }
                         // one chunk of the 128-row M-tile: gate/up codes + scales boxes, or
-                        // one down box (a half box for a last half chunk). An M-tile past
-                        // the weights (a pair's second tile of an odd count) lies outside the
-                        // tensor: the boxes read as zeros.
+                        // one down box (a half box for a last half chunk)
                         const QLayout &L = ti.shared ? a.src.LS : a.src.L;
                         const CUtensorMap *pk = ti.shared ? &a.pk[2] : &a.pk[0];
                         const int slot = ti.shared ? 0 : ti.grp.slot;
@@ -522,13 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                             break;
                         }
                         uint8_t *dstB = sm + Pl::kSmemB + (size_t)bb * Pl::kBTile;
-                        if (PAIR) {
-                            if (leader) mbar_expect_tx(&fullA[bb], bbytes);
-                            tma_box_pair(dstB, mb, s2 * kBK, r0, map_rank(&fullA[bb], 0));
-                        } else {
-                            mbar_expect_tx(&fullA[bb], bbytes);
-                            tma_box(dstB, mb, s2 * kBK, r0, &fullA[bb]);
-                        }
+                        mbar_expect_tx(&fullA[bb], bbytes);
+                        tma_box(dstB, mb, s2 * kBK, r0, &fullA[bb]);
                         if (a.mode == 2) {  // the router's A rows, into the same slot
                             mbar_expect_tx(&fullA[bb], (unsigned)(kABoxRows * kBK * 2));
                             tma_box(sm + Pl::kSmemA + (size_t)bb * kATile, &a.tmap_a, s2 * kBK, kBM * ti.mt, &fullA[bb]);
@@ -547,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         // Stage s of a tile dequantises half s & 1 of chunk s / 2 into the A tile; item
         // `it` belongs to group it % 2, and warp w of a group takes one 16-row slice
         // (gate/up tile w / 2, gate if w is even; down tile w). Each warp arrives once
-        // per stage (pairs: rank 1's warps on rank 0's full barrier).
+        // per stage.
         const int g = lane >> 2;
         const int grp = warp >> 3, lw = warp & 7;
         // stmatrix row addresses: lane l gives row l % 8 of matrix l / 8 (matrices:
@@ -618,8 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    if (PAIR && !leader) mbar_arrive_cluster(map_rank(&fullA[b], 0));
-                    else mbar_arrive(&fullA[b]);
+                    mbar_arrive(&fullA[b]);
                     mbar_arrive(&pempty_bar[ps]);
                     if (single) mbar_arrive(&pempty_bar[ps]);
                 }
@@ -628,9 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
         }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
-        // Pairs: rank 0 alone issues M = 256 MMAs (its A rows and B half, and rank 1's
-        // at the same offsets); the commits arrive on the barriers of both CTAs.
-        if (lane == 0 && leader) {
+        if (lane == 0) {
             // The issue loop is on the critical path of every stage (a stage of a narrow
             // group runs in ~180 cycles): ring position as a running slot and phase,
             // descriptors as offsets from per-ring bases.
@@ -642,13 +521,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                 TileInfo ti;
                 if (!get_tile(t, ti)) break;
                 const int ab = ti_local & 1;
-                if (ti_local >= 2 && !wait(&acce_bar[ab], ((ti_local >> 1) - 1) & 1, true)) break;
+                if (ti_local >= 2 && !wait(&acce_bar[ab], ((ti_local >> 1) - 1) & 1)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const int n = (ti.grp.ncols + 15) & ~15;
-                const uint32_t idesc = idesc_f16(n, a.mode == 2, PAIR ? 2 * kBM : kBM);
+                const uint32_t idesc = idesc_f16(n, a.mode == 2, kBM);
                 const uint32_t dt = tmem + (uint32_t)(256 * ab);
                 for (int s = 0; s < ti.nk; ++s) {
-                    if (!wait(&fullA[slot], phase, true)) {
+                    if (!wait(&fullA[slot], phase)) {
                         good = false;
                         break;
                     }
@@ -656,10 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                     // descriptor start addresses count 16-byte units; a K step of 16 is 32 bytes
                     const uint64_t da = dA0 + (uint64_t)(slot * (kATile >> 4));
                     const uint64_t db = dB0 + (uint64_t)(slot * (Pl::kBTile >> 4));
-                    mma_k64<PAIR>(dt, da, db, idesc, s > 0);
+                    mma_k64(dt, da, db, idesc, s > 0);
                     // one commit frees the stage's A and B slots (both rings have the
                     // same depth: the B producer waits on the A ring's empty barrier)
-                    commit_to<PAIR>(&emptyA[slot]);
+                    commit_to(&emptyA[slot]);
                     last_slot = slot;
                     last_phase = phase;
                     if (++slot == kAS) {
@@ -668,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                     }
                 }
                 if (!good) break;
-                commit_to<PAIR>(&accf_bar[ab]);
+                commit_to(&accf_bar[ab]);
             }
             // every MMA this thread issued has completed before TMEM can be released
             if (last_slot >= 0) {
@@ -686,8 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
             TileInfo ti;
             if (!get_tile(t, ti)) break;
             const int ab = ti_local & 1;
-            // a pair's M-tile past the weights holds zeros: nothing to write
-            const int ncols = ti.mvalid ? ti.grp.ncols : 0;
+            const int ncols = ti.grp.ncols;
             const QLayout &L = ti.shared ? a.src.LS : a.src.L;
             int *rows = epi_rows[q];
             // the down tile's output rows, loaded while its MMAs run
@@ -742,26 +620,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ Um
                 }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            if (PAIR && !leader) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(map_rank(&acce_bar[ab], 0));
-            } else {
-                mbar_arrive(&acce_bar[ab]);
-            }
+            mbar_arrive(&acce_bar[ab]);
             __syncwarp();  // the row cache is rewritten for the next tile
         }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (PAIR) cluster_sync_all();  // rank 0's MMAs into rank 1's memory are done; both CTAs' reads too
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (PAIR)
-            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
-                         : "memory");
-        else
-            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
-                         : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
     }
 }
 
@@ -826,27 +694,9 @@ bool umma_supported(const QLayout &L) { return L.kind == MOE_Q4_32 && L.H % 128 
 
 bool umma_router_supported(int H) { return H % kBK == 0; }
 
-int launch_umma(const UmmaArgs &a, int n_ctas, bool pair, cudaStream_t s) {
-    if (!pair) {
-        k_umma<false><<<n_ctas, kThreads, Plan<false>::kSmemBytes + 1024, s>>>(a);
-        MOE_CUDA_TRY(cudaGetLastError());
-        return MOE_OK;
-    }
-    // clusters of two CTAs on neighbouring SMs
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3((unsigned)(n_ctas & ~1));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Plan<true>::kSmemBytes + 1024;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    MOE_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_umma<true>, a));
+int launch_umma(const UmmaArgs &a, int n_ctas, cudaStream_t s) {
+    k_umma<<<n_ctas, kThreads, Plan::kSmemBytes + 1024, s>>>(a);
+    MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }
 
@@ -924,18 +774,14 @@ int make_packed_maps(CUtensorMap maps[2], int mode, const QLayout &L, const uint
 }
 
 int init_umma_attributes(int max_smem) {
-    // a form whose shared memory does not fit is never launched (umma_fits says so)
-    int rc = MOE_OK;
-    if (umma_fits(max_smem, false)) rc = set_max_dynamic_smem((const void *)k_umma<false>, max_smem);
-    if (!rc && umma_fits(max_smem, true)) rc = set_max_dynamic_smem((const void *)k_umma<true>, max_smem);
-    return rc;
+    // a kernel whose shared memory does not fit is never launched (umma_fits says so)
+    return umma_fits(max_smem) ? set_max_dynamic_smem((const void *)k_umma, max_smem) : MOE_OK;
 }
 
-bool umma_fits(int max_smem, bool pair) {
+bool umma_fits(int max_smem) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, pair ? (const void *)k_umma<true> : (const void *)k_umma<false>) != cudaSuccess)
-        return false;
-    const size_t dyn = (pair ? Plan<true>::kSmemBytes : Plan<false>::kSmemBytes) + 1024;
+    if (cudaFuncGetAttributes(&fa, (const void *)k_umma) != cudaSuccess) return false;
+    const size_t dyn = Plan::kSmemBytes + 1024;
     return dyn + fa.sharedSizeBytes <= (size_t)max_smem;
 }
 

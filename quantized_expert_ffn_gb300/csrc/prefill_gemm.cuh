@@ -53,9 +53,8 @@ struct UmmaArgs {
 bool umma_supported(const QLayout &L);
 // The router GEMM runs for bf16 x and Wr with H a multiple of 64.
 bool umma_router_supported(int H);
-// One CTA per tile, or (pair) clusters of two CTAs sharing each M = 256 tile
-// (modes 0 and 1 only; n_ctas rounded down to even).
-int launch_umma(const UmmaArgs &a, int n_ctas, bool pair, cudaStream_t s);
+// One CTA per SM; tiles round-robin over the CTAs.
+int launch_umma(const UmmaArgs &a, int n_ctas, cudaStream_t s);
 // out[i] = fp16(x[token of plan column i]) for the n_cols (device count) columns
 int launch_gather_f16(const int32_t *cols, const int32_t *n_cols, const void *x, int xf32, int K, int H, int max_rows,
                       __half *out, cudaStream_t s);
@@ -68,7 +67,7 @@ int make_tmap_2d(CUtensorMap *map, const void *base, bool bf16, unsigned long lo
 int make_packed_maps(CUtensorMap maps[2], int mode, const QLayout &L, const uint8_t *base, long long slot_stride,
                      int n_slots);
 int init_umma_attributes(int max_smem);
-// The form's shared memory (dynamic + static) fits in max_smem bytes per block.
-bool umma_fits(int max_smem, bool pair);
+// The kernel's shared memory (dynamic + static) fits in max_smem bytes per block.
+bool umma_fits(int max_smem);
 
 }  // namespace moe

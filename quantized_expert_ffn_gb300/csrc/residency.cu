@@ -388,10 +388,12 @@ MOE_API int moe_policy_destroy(moe_policy *p) {
 
 MOE_API int moe_policy_seed(moe_policy *p, const int32_t *layers, const int32_t *experts, int n, int *n_placed) {
     if (!p || (n > 0 && (!layers || !experts))) return set_error(MOE_ERR_ARG, "null argument");
-    int placed = 0;
-    for (int i = 0; i < n && p->n_res < p->pr.capacity; ++i) {
+    // every pair is checked before any is placed: a bad list changes nothing
+    for (int i = 0; i < n; ++i)
         if (layers[i] < 0 || layers[i] >= p->L || experts[i] < 0 || experts[i] >= p->E)
             return set_error(MOE_ERR_ARG, "pair (%d, %d) out of range", layers[i], experts[i]);
+    int placed = 0;
+    for (int i = 0; i < n && p->n_res < p->pr.capacity; ++i) {
         const int k = layers[i] * p->E + experts[i];
         if (p->res[k]) continue;
         // a profile lists the hottest first: seeded entries are older than any access,

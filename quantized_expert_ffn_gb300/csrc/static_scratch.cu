@@ -32,14 +32,22 @@ int scratch_address(int device, void **out) {
     if (device < 0 || device >= kMaxDevices) return moe::set_error(MOE_ERR_ARG, "device %d out of range", device);
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (!g_scratch_ptr[device]) {
-        int prev = -1;
-        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
-        if (prev != device && cudaSetDevice(device) != cudaSuccess)
-            return moe::set_error(MOE_ERR_CUDA, "cudaSetDevice(%d) failed", device);
+        // the lookup needs `device` current; the caller's current device is put
+        // back on every path, and a failure to put it back is reported
+        int prev = 0;
+        cudaError_t e = cudaGetDevice(&prev);
+        if (e != cudaSuccess) return moe::cuda_error(e, "cudaGetDevice");
+        if (prev != device) {
+            e = cudaSetDevice(device);
+            if (e != cudaSuccess) return moe::cuda_error(e, "cudaSetDevice (static scratch lookup)");
+        }
         void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
-        if (prev >= 0 && prev != device) cudaSetDevice(prev);
-        if (e != cudaSuccess) return moe::cuda_error(e, "cudaGetSymbolAddress(static scratch)");
+        const cudaError_t el = cudaGetSymbolAddress(&p, g_scratch);
+        if (prev != device) {
+            e = cudaSetDevice(prev);
+            if (e != cudaSuccess) return moe::cuda_error(e, "cudaSetDevice (restoring the caller's device)");
+        }
+        if (el != cudaSuccess) return moe::cuda_error(el, "cudaGetSymbolAddress(static scratch)");
         g_scratch_ptr[device] = p;
     }
     *out = g_scratch_ptr[device];

@@ -43,26 +43,11 @@ def _forward(g, x):
     return y, lg, ids, path
 
 
-class _pair:
-    """Run the grouped GEMMs with CTA pairs (1) or one CTA per tile (0) inside the block."""
-
-    def __init__(self, ctx, on):
-        self.ctx, self.on = ctx, on
-
-    def __enter__(self):
-        L.moe_ctx_set_option(self.ctx, L.OPT_UMMA_PAIR, self.on)
-
-    def __exit__(self, *exc):
-        L.moe_ctx_set_option(self.ctx, L.OPT_UMMA_PAIR, 0)
-
-
-@pytest.mark.parametrize("pair", [1, 0])
 @pytest.mark.parametrize("T,n_rows", [(64, 12), (100, 12), (1000, 10)])
-def test_prefill_matches_oracle_on_sampled_rows(gemma, T, n_rows, pair):
+def test_prefill_matches_oracle_on_sampled_rows(gemma, T, n_rows):
     cfg = gemma.cfg
     x = _x(cfg, T, step=900 + T)
-    with _pair(gemma.ctx, pair):
-        y, lg, ids, path = _forward(gemma, to_dev(x))
+    y, lg, ids, path = _forward(gemma, to_dev(x))
     assert path == 2  # tensor-core grouped GEMMs
     rows = np.sort(np.random.default_rng(T).choice(T, size=n_rows, replace=False))
     r = oracle_layer(cfg, 0, C.as_f64(x), lg.cpu().numpy(), tokens=rows)
@@ -104,30 +89,6 @@ def test_prefill_close_to_mma_sync_path_on_every_row(gemma):
     same = (ia == ib).all(dim=1).cpu().numpy()
     assert same.mean() >= 0.99
     assert rel_err(ya.cpu().numpy()[same], yb.cpu().numpy()[same]) <= TOL
-
-
-@pytest.mark.parametrize("T", [64, 1000, 4096])
-def test_pair_and_single_cta_tiles_agree_bitwise(gemma, T):
-    # a CTA pair computes each output element as the same fp32 sum over K, in the
-    # same order, as one CTA per 128-row tile; the 704- and 2112-wide experts give
-    # odd M-tile counts (a pair's second tile past the weights), T = 64 gives groups
-    # of a few columns (8-row B halves)
-    x = to_dev(_x(gemma.cfg, T, step=990 + T))
-    with _pair(gemma.ctx, 1):
-        ya, la, ia, pa = _forward(gemma, x)
-    with _pair(gemma.ctx, 0):
-        yb, lb, ib, pb = _forward(gemma, x)
-    import torch
-    assert (pa, pb) == (2, 2)
-    assert torch.equal(ia, ib) and torch.equal(la, lb)
-    assert torch.equal(ya, yb)
-
-
-def test_pair_option(gemma):
-    assert L.moe_ctx_get_option(gemma.ctx, L.OPT_UMMA_PAIR) == 0
-    L.moe_ctx_set_option(gemma.ctx, L.OPT_UMMA_PAIR, 1)
-    assert L.moe_ctx_get_option(gemma.ctx, L.OPT_UMMA_PAIR) == 1
-    L.moe_ctx_set_option(gemma.ctx, L.OPT_UMMA_PAIR, 0)
 
 
 def test_prefill_deterministic(gemma):

@@ -247,6 +247,45 @@ def test_expert_gelu_tanh_closed_form():
     np.testing.assert_allclose(y, gelu * x, rtol=1e-14, atol=1e-15)
 
 
+def _identity_act(act, x):
+    """act(x_j) through the oracle's expert: an identity-pattern expert (d = 1,
+    gate/up/down rows select x_j) gives y_j = act(x_j) * x_j, divided back by x_j."""
+    H = F = x.shape[1]
+    idx = np.arange(F)
+    blob = selector_expert(Q4, 8, H, F, idx, idx, idx, 9, 9, 9)
+    y = oracle.expert_ffn(Q4, 8, blob, H, F, x, act=act)
+    return y / x
+
+
+def test_expert_activations_against_independent_implementations():
+    # The activations checked against implementations written elsewhere, in fp64:
+    # SiLU against scipy's logistic function (x * expit(x)), the tanh-approximated
+    # GELU (Hendrycks & Gimpel's approximation, used by Gemma's experts) against
+    # torch's own gelu(approximate="tanh"). A wrong constant (sqrt(pi/2) for
+    # sqrt(2/pi), 0.0447 for 0.044715) or a dropped cubic term fails here.
+    torch = pytest.importorskip("torch")
+    from scipy.special import expit
+    x = np.concatenate([np.linspace(-8, 8, 63), np.random.default_rng(61).standard_normal(65) * 3])
+    x = x[np.abs(x) > 1e-3].reshape(1, -1)[:, :96]
+    silu = _identity_act(oracle.ACT_SWIGLU, x)
+    np.testing.assert_allclose(silu, x * expit(x), rtol=1e-13, atol=1e-300)
+    gelu = _identity_act(oracle.ACT_GEGLU_TANH, x)
+    want = torch.nn.functional.gelu(torch.from_numpy(x), approximate="tanh").numpy()
+    np.testing.assert_allclose(gelu, want, rtol=1e-13, atol=1e-300)
+
+
+def test_expert_gelu_tanh_properties():
+    # Properties of the tanh form that hold whatever the constants are written as:
+    # gelu(x) - gelu(-x) = x (odd part), and against the exact GELU x * Phi(x)
+    # (scipy's normal CDF) the approximation's error stays below 1e-3 everywhere
+    # (a wrong sqrt(2/pi) breaks this by more than 1e-2).
+    from scipy.special import ndtr
+    x = np.linspace(0.05, 6, 96).reshape(1, -1)
+    gp, gm = _identity_act(oracle.ACT_GEGLU_TANH, x), _identity_act(oracle.ACT_GEGLU_TANH, -x)
+    np.testing.assert_allclose(gp - gm, x, rtol=1e-14)
+    assert np.max(np.abs(gp - x * ndtr(x))) < 1e-3
+
+
 def _random_blob(rng, kind, H, F, d_lo=0.005, d_hi=0.02):
     bw = 64 if kind == Q2 else 32
     n_blocks = 3 * H * F // bw

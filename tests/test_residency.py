@@ -155,6 +155,31 @@ def test_engine_matches_reference_decayed_frequency_on_ties(half_life, guard, ca
     _replay(R.DECAYED_FREQ, tr, cap, seed_pairs=prof, half_life=half_life, guard=guard)
 
 
+@pytest.mark.parametrize("guard,cap,seeded", [(8, 60, False), (16, 60, True), (16, 120, True)])
+def test_engine_matches_reference_decayed_frequency_long_guard(guard, cap, seeded):
+    # long recency guards keep many pairs outside the victim heap at once (held until
+    # their guard ends, released in order, the heap rebuilt with them); pools large
+    # enough that the heap, not the fallback scan, picks most victims
+    tr = traces.routing_trace(120, 4, 64, 6, seed=guard * 7 + cap)
+    prof = traces.profile_ranking(tr[:8]) if seeded else None
+    _replay(R.DECAYED_FREQ, tr, cap, seed_pairs=prof, half_life=32.0, guard=guard)
+
+
+def test_seed_checks_every_pair_before_placing_any():
+    p = L.Policy(L.policy_params(L.POLICY_DECAYED_FREQ, 8), 2, 8)
+    try:
+        with pytest.raises(L.MoeError):
+            p.seed([0, 1, 5], [1, 2, 3])  # the third pair's layer is out of range
+        assert p.count() == 0
+        with pytest.raises(L.MoeError):
+            p.seed([0, 1], [1, 8])  # expert out of range
+        assert p.count() == 0
+        assert p.seed([0, 1], [1, 2]) == 2
+        assert p.count() == 2
+    finally:
+        p.close()
+
+
 def test_hit_rates_are_bounded_by_belady():
     tr = traces.routing_trace(64, 4, 64, 8, seed=7)
     events = [[(l, tr[t, l]) for l in range(4)] for t in range(64)]
