@@ -129,3 +129,56 @@ def oracle_layer(cfg: C.Config, l: int, x64, logits_gpu, zero_point=None, tokens
     return oracle.layer_forward(cfg.kind, zp, cfg.H, cfg.E, cfg.K, cfg.F, None, None, experts,
                                 np.ascontiguousarray(x64[rows]), shared=shared,
                                 F_shared=cfg.F_shared, logits_in=lg)
+
+
+def oracle_layer_by_bucket(cfg: C.Config, l: int, x64, logits_gpu, threads: int | None = None):
+    """Oracle output for EVERY token of a wide window, routed with the GPU's fp32
+    logits: the same definition as oracle.layer_forward (top-k and weights from
+    oracle.topk, each selected expert's FFN from oracle.expert_ffn, the combine in
+    k order in fp64, then the shared expert), evaluated one expert bucket at a time
+    so that each expert's weights are dequantised once. The oracle's C calls run on
+    a thread pool (ctypes releases the GIL during them).
+
+    Returns dict(y [T][H] fp64, ids [T][K], counts [E])."""
+    import concurrent.futures as cf
+    import os
+    T = x64.shape[0]
+    lg = np.asarray(logits_gpu, dtype=np.float64)
+    ids, w, _ = oracle.topk(lg, cfg.K)
+    counts = np.bincount(ids.ravel(), minlength=cfg.E)
+    need = np.flatnonzero(counts)
+    blobs = C.experts(cfg, l, need)
+    x64 = np.ascontiguousarray(x64, dtype=np.float64)
+    ye = {}
+
+    def run(i):
+        e = int(need[i])
+        rows = np.flatnonzero((ids == e).any(axis=1))
+        return e, rows, oracle.expert_ffn(cfg.kind, cfg.zero_point, blobs[i], cfg.H, cfg.F, x64[rows])
+
+    shared = C.shared_expert(cfg, l)
+    chunks = [np.arange(s, min(s + 64, T)) for s in range(0, T, 64)] if shared is not None else []
+
+    def run_shared(rows):
+        return rows, oracle.expert_ffn(cfg.kind, cfg.zero_point, shared, cfg.H, cfg.F_shared, x64[rows])
+
+    y_sh = np.zeros((T, cfg.H))
+    with cf.ThreadPoolExecutor(max_workers=threads or os.cpu_count() or 4) as ex:
+        futs = [ex.submit(run, i) for i in range(len(need))]
+        sfuts = [ex.submit(run_shared, r) for r in chunks]
+        for f in futs:
+            e, rows, y = f.result()
+            ye[e] = (rows, y)
+        for f in sfuts:
+            rows, y = f.result()
+            y_sh[rows] = y
+    # row of token t in its expert's bucket output
+    pos = {e: {int(t): j for j, t in enumerate(rows)} for e, (rows, _) in ye.items()}
+    y = np.zeros((T, cfg.H))
+    for t in range(T):
+        acc = np.zeros(cfg.H)
+        for k in range(cfg.K):
+            e = int(ids[t, k])
+            acc += w[t, k] * ye[e][1][pos[e][t]]
+        y[t] = acc + y_sh[t]
+    return dict(y=y, ids=ids, counts=counts)

@@ -1,12 +1,13 @@
 """Prefill-sized windows: Q4 experts run as tcgen05 grouped GEMMs (fp16 operands,
-fp32 accumulation in tensor memory). Parity against the oracle on sampled rows,
-against the mma.sync path on every row, and the path really taken."""
+fp32 accumulation in tensor memory). Parity against the oracle on every row (the
+bench's 4,096-token window included), against the mma.sync path, and the path
+really taken."""
 import numpy as np
 import pytest
 
 from quantized_expert_ffn_gb300 import _lib as L
 from synth import configs as C
-from tests.gpu_util import TOL, GpuLayers, oracle_layer, rel_err, to_dev
+from tests.gpu_util import TOL, GpuLayers, oracle_layer, oracle_layer_by_bucket, rel_err, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -43,17 +44,51 @@ def _forward(g, x):
     return y, lg, ids, path
 
 
-@pytest.mark.parametrize("T,n_rows", [(64, 12), (100, 12), (1000, 10)])
-def test_prefill_matches_oracle_on_sampled_rows(gemma, T, n_rows):
-    cfg = gemma.cfg
-    x = _x(cfg, T, step=900 + T)
-    y, lg, ids, path = _forward(gemma, to_dev(x))
+def _coverage(counts, nc=256):
+    """Column groups of <= nc live pairs per expert (the plan's split) and the B box
+    height each group's tile loads (round-up(n, 16) to the next of 16..256)."""
+    sizes = []
+    for c in counts[counts > 0]:
+        sizes += [nc] * (int(c) // nc) + ([int(c) % nc] if c % nc else [])
+    sizes = np.array(sizes)
+    r16 = (sizes + 15) // 16 * 16
+    boxes = np.select([r16 <= 16, r16 <= 32, r16 <= 64, r16 <= 128], [16, 32, 64, 128], 256)
+    return sizes, {int(b): int((boxes == b).sum()) for b in (16, 32, 64, 128, 256)}
+
+
+def _check_every_row(g, cfg, T, step):
+    x = _x(cfg, T, step=step)
+    y, lg, ids, path = _forward(g, to_dev(x))
     assert path == 2  # tensor-core grouped GEMMs
-    rows = np.sort(np.random.default_rng(T).choice(T, size=n_rows, replace=False))
-    r = oracle_layer(cfg, 0, C.as_f64(x), lg.cpu().numpy(), tokens=rows)
-    assert np.array_equal(ids.cpu().numpy()[rows], r["ids"])
-    err = rel_err(y.cpu().numpy()[rows], r["y"])
+    r = oracle_layer_by_bucket(cfg, 0, C.as_f64(x), lg.cpu().numpy())
+    assert np.array_equal(ids.cpu().numpy(), r["ids"])
+    err = rel_err(y.cpu().numpy(), r["y"])
+    sizes, boxes = _coverage(r["counts"])
+    print(f"\nT={T}: {len(sizes)} routed column groups, sizes {sizes.min()}..{sizes.max()}, "
+          f"{int((sizes <= 16).sum())} of <= 16 columns, partial last groups "
+          f"{int(((sizes % 256) != 0).sum())}; B boxes {boxes}; max rel err {err:.2e}")
     assert err <= TOL, err
+    return boxes
+
+
+@pytest.mark.parametrize("T", [64, 100, 1000])
+def test_prefill_matches_oracle_on_every_row(gemma, T):
+    _check_every_row(gemma, gemma.cfg, T, 900 + T)
+
+
+def test_prefill_full_window_matches_oracle_on_every_row(ctx):
+    # the 4,096-token window the bench times (same configuration, same inputs): every
+    # row against the oracle; with 128 experts and the calibrated Zipf skew it takes
+    # every B box height, groups of <= 16 columns, partial last groups of the large
+    # buckets, and both experts' last M-tiles (704 = 11 x 64 gate/up rows, 2,816 =
+    # 22 x 128 down rows; the shared expert's 2,112 = 33 x 64)
+    cfg = C.CONFIGS["prefill"]
+    g = GpuLayers(ctx, cfg)
+    try:
+        boxes = _check_every_row(g, cfg, 4096, 4096)
+        assert all(v > 0 for v in boxes.values()), boxes
+    finally:
+        g.close()
 
 
 def test_prefill_fp32_activations(gemma):

@@ -593,3 +593,26 @@ def test_layer_drop_removes_exactly_the_dropped_routes():
     kept = r["w"] != 0
     assert kept.sum() < kept.size
     np.testing.assert_allclose(r["w"][kept], base["w"][kept], rtol=1e-14, atol=0)
+
+
+def test_bucket_wise_layer_evaluation_equals_layer_forward():
+    # the every-row prefill check evaluates the oracle one expert bucket at a time;
+    # it must give the same bits as oracle.layer_forward on the same routing
+    from synth import configs as C
+    from tests.gpu_util import oracle_layer_by_bucket
+    cfg = C.CONFIGS["gemma_layer"]
+    T = 12
+    x = C.as_f64(C.activations(cfg, T, step=3))
+    Wr = C.as_f64(C.router_weights(cfg, 0))
+    lg = (x @ Wr.T + C.router_bias(cfg, 0)).astype(np.float32)
+    r = oracle_layer_by_bucket(cfg, 0, x, lg, threads=4)
+    ids, _, _ = oracle.topk(lg.astype(np.float64), cfg.K)
+    need = np.unique(ids)
+    blobs = C.experts(cfg, 0, need)
+    experts = [None] * cfg.E
+    for i, e in enumerate(need):
+        experts[int(e)] = blobs[i]
+    r2 = oracle.layer_forward(cfg.kind, cfg.zero_point, cfg.H, cfg.E, cfg.K, cfg.F, None, None, experts, x,
+                              shared=C.shared_expert(cfg, 0), F_shared=cfg.F_shared, logits_in=lg)
+    assert np.array_equal(r["ids"], r2["ids"])
+    assert np.array_equal(r["y"], r2["y"])
