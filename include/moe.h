@@ -146,9 +146,9 @@ MOE_API int moe_ctx_get_option(moe_ctx *ctx, int option, int *value);
 
 /* MOE_OPT_TEST_SKIP_ARRIVAL (default -1, settable, >= -1): a test hook for the
  * bounded waits. With value v >= 0, in every persistent decode launch CTA 0 leaves
- * out its arrival at the first grid barrier of layer v of the launch (a signal
- * that never comes): every CTA's wait at that barrier gives up after about a
- * second, MOE_STATUS_TIMEOUT is set, the kernel stops and returns, and the context
+ * out its router logits and its arrival flag of layer v of the launch (a signal
+ * that never comes): every CTA's wait for the layer's logits gives up after about
+ * a second, MOE_STATUS_TIMEOUT is set, the kernel stops and returns, and the context
  * stays usable (the call's outputs are then undefined). Nothing faults or traps. */
 #define MOE_OPT_TEST_SKIP_ARRIVAL 4
 

@@ -90,7 +90,7 @@ int check_dims(int H, int F) {
 struct WsLayout {
     size_t logits, ids, w, counts, offsets, perm, active, n_active, live, cols, groups_gu, groups_d, n_groups, h, yp,
         u, x16, bar, wide, total;
-    int sync_words;  // persistent path: barrier words + down tile counters
+    size_t sync_bytes;  // persistent path: its synchronisation area (SyncLayout)
     int max_routed_gu, max_routed_d, max_shared, h_ld;
 };
 
@@ -123,8 +123,8 @@ WsLayout ws_layout(const moe_layer_desc *d, int T, int nc_gu) {
     W.yp = take((P + T) * (size_t)d->H * 4);
     W.u = take((size_t)T * d->H * 2);
     W.x16 = take((P + T) * (size_t)d->H * 2);  // x in plan-column order (tensor-core path)
-    W.sync_words = 4 + d->H / 16;
-    W.bar = take((size_t)W.sync_words * 4);
+    W.sync_bytes = sync_layout(T, d->H, d->E, d->K, kMaxPersistLayers).bytes;
+    W.bar = take(W.sync_bytes);
     W.wide = take(use_wide(T, d->K) ? wide_scratch_bytes(T, d->K, d->E) : 0);  // multi-CTA sort and plan
     W.total = o;
     return W;
@@ -382,7 +382,7 @@ int try_persistent(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers, boo
     if (geom.ring_bytes == 0 || geom.bytes > (size_t)ctx->max_smem) return MOE_OK;
     int rc = persist_max_ctas((int)geom.bytes, &G);
     if (rc) return rc;
-    if (G != sms) return MOE_OK;
+    if (G != sms || G > kMaxGrid) return MOE_OK;
     if ((d0.E + G - 1) / G > 16) return MOE_OK;  // router rows per CTA
 
     PersistArgs a;
@@ -405,16 +405,19 @@ int try_persistent(moe_ctx *ctx, const moe_layer_desc *layers, int n_layers, boo
     a.x = x;
     a.y = stack ? nullptr : out;
     a.resid = stack ? out : nullptr;
-    a.logits = logits_out ? logits_out : (float *)(ws + W.logits);
+    a.logits = logits_out;
     a.ids_out = ids_out;
     a.h_ld = W.h_ld;
     const size_t hrows = (size_t)T * d0.K + T;
     a.h_hi = (__nv_bfloat16 *)(ws + W.h);
     a.h_lo = a.h_hi + hrows * W.h_ld;
+    const SyncLayout SL = sync_layout(T, d0.H, d0.E, d0.K, kMaxPersistLayers);
     a.bar = (unsigned *)(ws + W.bar);
-    a.d_cnt = (int *)(ws + W.bar) + 4;
-    a.yp = (float *)(ws + W.yp);
-    a.sync_words = W.sync_words;
+    a.gu_cnt = (int *)(ws + W.bar + SL.gu_cnt);
+    a.lg_t = (unsigned long long *)(ws + W.bar + SL.lg_t);
+    a.resid_t = (unsigned long long *)(ws + W.bar + SL.resid_t);
+    a.yp_t = (unsigned long long *)(ws + W.bar + SL.yp_t);
+    a.sync_bytes = SL.bytes;
     a.status = ctx->d_status;
     for (int l0 = 0; l0 < n_layers; l0 += kMaxPersistLayers) {
         const int n = n_layers - l0 < kMaxPersistLayers ? n_layers - l0 : kMaxPersistLayers;

@@ -6,23 +6,31 @@
 //      CTA for itself from the same resid;
 //   R  router logits: CTA c owns experts c, c+G, ...; four warps share a row; the
 //      rows, bias and slot-table row were prefetched into shared memory during the
-//      previous layer, and the next layer's are requested as soon as R is done;
-//   -- grid barrier --
-//   T  top-K, weights and the plan, every CTA the same result from the logits: the
-//      K-th largest of a few segment maxima is a threshold, the experts at or above
-//      it are ranked exactly; the distinct live experts and their columns; the
-//      split of the down work over the CTAs;
+//      previous layer, and the next layer's are requested during the down phase;
+//      the logits are published as tagged words, with a flag per CTA;
+//   T  top-K, weights and the plan, every CTA the same result from the logits (read
+//      as soon as every CTA's tagged words are there): the K-th largest of a few
+//      segment maxima is a threshold, the experts at or above it are ranked exactly;
+//      the distinct live experts and their columns; the split of the down work;
 //   GU gate/up items (16 rows of one expert, all of H) are dealt round-robin over
 //      CTAs and over the groups of S warps of a CTA (S = 4 for Q2, 8 for Q4); warp
-//      q of a group sums part q of H; the group adds the parts in order and applies
-//      the activation;
-//   -- grid barrier --
+//      q of a group sums part q of H; the group adds the parts in order, applies
+//      the activation, writes h and counts the item for its expert;
 //   D  down units (one expert x 16 output rows) in expert order, split over the
-//      CTAs so that gate/up plus down bytes are even, then over the CTA's warps;
-//      h of the CTA's experts is staged in shared memory; the last unit of a row
-//      tile to arrive (atomic ticket, no waiting) combines the experts in k order
-//      (+ the shared expert) and writes y, or adds into resid;
-//   -- grid barrier (stack only) --
+//      CTAs so that gate/up plus down bytes are even, then over the CTA's warps; a
+//      CTA waits only until the gate/up items of its own units' experts are
+//      counted, then stages their h in shared memory; a unit's outputs are tagged
+//      words; the warp that ran the last task's unit of a row tile combines the
+//      tile in k order (+ the shared expert) once every pair's words are there, and
+//      writes y, or the next layer's residual as tagged words.
+//
+// No grid-wide barrier: every exchange between CTAs is either data that carries
+// its own readiness (a 64-bit word = 32-bit value + the layer that wrote it, read
+// with one round trip as soon as it is there) or a per-expert counter
+// (release/acquire). The order of the phases makes reuse safe: a CTA publishes its
+// layer-l logits only after reading layer l's input, and layer l's residual output
+// is written only after every CTA's layer-l logits are seen, so no word is
+// overwritten before everyone has read it (logits alternate between two buffers).
 //
 // Weights move through one ring per warp in shared memory, filled by bulk copies
 // (TMA, cp.async.bulk, completion counted on an mbarrier) of a few chunks each, in
@@ -34,9 +42,9 @@
 //
 // Arithmetic per output element is that of the multi-kernel path (same device
 // functions, same splits of the reductions, same orders), so results match it bit
-// for bit. Every wait is bounded: a barrier or a copy that does not complete in
-// about a second sets MOE_STATUS_TIMEOUT and the CTAs stop at the next barrier;
-// before a warp leaves it waits (bounded) for every copy it issued.
+// for bit. Every wait is bounded: a wait or a copy that does not complete in about
+// a second sets MOE_STATUS_TIMEOUT and the stop word, every CTA leaves at its next
+// wait; before a warp leaves it waits (bounded) for every copy it issued.
 #include <type_traits>
 
 #include "decode_common.cuh"
@@ -85,43 +93,77 @@ __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Barrier over all CTAs of the (co-resident) grid. bar[0] counts arrivals
-// monotonically within the launch; bar[1] is the stop word. Returns false when
-// the kernel must stop (this or another CTA gave up waiting).
-// skip_arrival (a test hook, never set by the layer code) leaves this CTA's arrival
-// out, so that every wait on this barrier runs into its time limit.
-__device__ bool grid_sync(unsigned *bar, unsigned &target, uint32_t *status, int *s_flag,
-                          bool skip_arrival = false) {
-    target += gridDim.x;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        // release: every write of this CTA (ordered before by the bar.sync above)
-        // is visible before the arrival is
-        if (!skip_arrival) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar) : "memory");
-        const long long t0 = clock64();
-        int stop = 0;
-        // the stop word is set only by a CTA that gave up, and then the count never
-        // completes: it needs checking only while waiting
-        for (unsigned it = 0; (int)(ld_relaxed_u32(bar) - target) < 0; ++it) {
-            if ((it & 63) == 63) {
-                if (ld_relaxed_u32(bar + 1)) {
-                    stop = 1;
-                    break;
-                }
-                if (clock64() - t0 > kSpinCycles) {
-                    atomicExch(bar + 1, 1u);
-                    set_status(status, MOE_STATUS_TIMEOUT);
-                    stop = 1;
-                    break;
-                }
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long tagged(unsigned tag, uint32_t v) {
+    return ((unsigned long long)tag << 32) | v;
+}
+
+// One wait of one thread (a fresh Waiter per wait). It gives up after about a
+// second: it sets MOE_STATUS_TIMEOUT and the stop word, and returns false; it also
+// returns false as soon as another thread has set the stop word.
+struct Waiter {
+    unsigned *stop;
+    uint32_t *status;
+    long long t0 = 0;
+    unsigned it = 0;
+    // false: stop waiting. Between polls a thread sleeps, longer the longer it has
+    // waited (32 ns doubling to 512 ns): many SMs polling L2 without a pause slow
+    // down the very writes they wait for.
+    __device__ __forceinline__ bool keep_going() {
+        if (it == 0) t0 = clock64();
+        ++it;
+        __nanosleep(it < 5 ? 16u << it : 512u);
+        if ((it & 15) == 0) {
+            if (ld_relaxed_u32(stop)) return false;
+            if (clock64() - t0 > kSpinCycles) {
+                atomicExch(stop, 1u);
+                set_status(status, MOE_STATUS_TIMEOUT);
+                return false;
             }
         }
-        // acquire: the other CTAs' writes before their arrivals are visible to this CTA
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        *s_flag = stop;
+        return true;
     }
-    __syncthreads();
-    return *s_flag == 0;
+};
+
+// Load the tagged words addr(i) for the bits i of `mask` (i < N) with all loads in
+// flight, again for the ones not yet written with `tag`, until every one is; their
+// values in v. False if the wait gave up.
+template <int N, typename Addr>
+__device__ __forceinline__ bool wait_tagged(Addr addr, unsigned mask, unsigned tag, uint32_t (&v)[N], Waiter w) {
+    unsigned long long x[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        if (mask >> i & 1u) x[i] = ld_relaxed_u64(addr(i));
+    for (;;) {
+        bool all = true;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if ((mask >> i & 1u) && (unsigned)(x[i] >> 32) != tag) all = false;
+        if (all) break;
+        if (!w.keep_going()) return false;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if ((mask >> i & 1u) && (unsigned)(x[i] >> 32) != tag) x[i] = ld_relaxed_u64(addr(i));
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = (mask >> i & 1u) ? (uint32_t)x[i] : 0u;
+    return true;
+}
+
+// Wait until counter *p reaches `target` (relaxed polling, then an acquire fence:
+// what was written before the releasing increments is visible to this thread).
+__device__ __forceinline__ bool wait_count(const int *p, int target, Waiter w) {
+    while ((int)ld_relaxed_u32(reinterpret_cast<const unsigned *>(p)) < target)
+        if (!w.keep_going()) return false;
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    return true;
 }
 
 // ------------------------------------------------------------------ weight ring
@@ -279,7 +321,8 @@ __device__ void prefetch_router(const PersistArgs &a, int l, uint8_t *wr_s, int3
     const int wsz = a.wr_bf16 ? 2 : 4;
     const int row_bytes = a.H * wsz;
     const uint8_t *Wr = reinterpret_cast<const uint8_t *>(a.layers[l].Wr);
-    const int nr = (a.E - c + G - 1) / G;
+    const int nrb = (a.E + G - 1) / G, e0 = c * nrb;  // my experts: e0 .. e0 + nr - 1
+    const int nr = a.E - e0 < nrb ? (a.E - e0 > 0 ? a.E - e0 : 0) : nrb;
     const int32_t *tab = a.layers[l].table + (size_t)a.layers[l].layer * a.E;
     const bool tab_bulk = ((uintptr_t)tab & 15) == 0 && (a.E & 3) == 0;
     if (lane == 0) {
@@ -287,28 +330,29 @@ __device__ void prefetch_router(const PersistArgs &a, int l, uint8_t *wr_s, int3
         // come before the copies' writes
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_expect_tx(m, (unsigned)(nr * row_bytes + (tab_bulk ? a.E * 4 : 0)));
-        for (int r = 0; r < nr; ++r)
-            bulk_g2s(wr_s + (size_t)r * row_bytes, Wr + (size_t)(c + r * G) * row_bytes, (unsigned)row_bytes, m);
+        if (nr > 0) bulk_g2s(wr_s, Wr + (size_t)e0 * row_bytes, (unsigned)(nr * row_bytes), m);
         if (tab_bulk) bulk_g2s(tab_s, tab, (unsigned)(a.E * 4), m);
     }
     if (!tab_bulk)
         for (int i = lane; i < a.E; i += 32) cp_async4(tab_s + i, tab + i);
     if (a.layers[l].bias)
-        for (int r = lane; r < nr; r += 32) cp_async4(bias_s + r, a.layers[l].bias + c + r * G);
+        for (int r = lane; r < nr; r += 32) cp_async4(bias_s + r, a.layers[l].bias + e0 + r);
     cp_async_commit();
 }
 
 // Top-K keys of every token by sorting 32-logit chunks and merging them pairwise
 // (used when the threshold pass keeps too many candidates, e.g. many equal
-// logits). lists: T * ceil(E/32) * 32 keys of scratch.
-__device__ void topk_sort_merge(const float *logits, int T, int E, unsigned long long *lists,
+// logits); lg: the layer's tagged logits ([T][ceil(E/32) * 32]), all written.
+// lists: T * ceil(E/32) * 32 keys of scratch.
+__device__ void topk_sort_merge(const unsigned long long *lg, int T, int E, unsigned long long *lists,
                                 unsigned long long (*sel)[32]) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nch = (E + 31) / 32;
     for (int task = warp; task < T * nch; task += kPWarps) {
         const int t = task / nch, ch = task % nch;
         const int e = ch * 32 + lane;
-        const unsigned long long key = e < E ? topk_key(__ldcg(logits + (size_t)t * E + e), e) : 0ull;
+        const unsigned long long key =
+            e < E ? topk_key(__uint_as_float((uint32_t)__ldcg(lg + (size_t)t * nch * 32 + e)), e) : 0ull;
         lists[((size_t)t * nch + ch) * 32 + lane] = warp_sort32(key, lane);
     }
     __syncthreads();
@@ -327,6 +371,65 @@ __device__ void topk_sort_merge(const float *logits, int T, int E, unsigned long
         __syncthreads();
     }
     if (tid < T * 32) sel[tid >> 5][tid & 31] = lists[(size_t)(tid >> 5) * nch * 32 + (tid & 31)];
+}
+
+// The combine of row tile r of layer l by one warp (a separate function: its
+// registers do not weigh on the rest of the kernel). The tile's words, one token
+// at a time: lane (h, rr) = (lane / 16, lane % 16) reads output rr of pairs
+// k = k0 + 2u + h (u < kCw; k < K routed, k = K the shared expert), so a warp load
+// covers two pairs' lines; they land in cs (the warp's ring memory, empty once the
+// warp's units are done) and lanes 0..15 add them in k order.
+__device__ __noinline__ void combine_tile(const PersistArgs &a, const int *live, const float *w, float *cs, int r,
+                                          int l, bool has_shared, int lane) {
+    constexpr int kCw = 6;
+    const int T = a.T, K = a.K, H = a.H, P = T * K, KK = K + 1;
+    const int rr = lane & 15, hh = lane >> 4;
+    for (int t = 0; t < T; ++t) {
+        bool ok = true;
+        for (int k0 = 0; k0 < KK && ok; k0 += 2 * kCw) {
+            uint32_t v[kCw];
+            unsigned m = 0;
+#pragma unroll
+            for (int u = 0; u < kCw; ++u) {
+                const int k = k0 + 2 * u + hh;
+                if (k < K ? live[t * K + k] != 0 : (k == K && has_shared)) m |= 1u << u;
+            }
+            const unsigned long long *base = a.yp_t + (size_t)r * 16 + rr;
+            ok = wait_tagged<kCw>(
+                [&](int u) {
+                    const int k = k0 + 2 * u + hh;
+                    return base + (size_t)(k < K ? t * K + k : P + t) * H;
+                },
+                m, (unsigned)(l + 1), v, Waiter{a.bar + 1, a.status});
+#pragma unroll
+            for (int u = 0; u < kCw; ++u)
+                if (m >> u & 1u) cs[(k0 + 2 * u + hh) * 16 + rr] = __uint_as_float(v[u]);
+        }
+        if (!__all_sync(0xffffffffu, ok)) return;
+        __syncwarp();
+        if (lane < 16) {
+            const size_t oo = (size_t)t * H + (size_t)r * 16 + rr;
+            // the layer's input residual: the caller's at layer 0, else the tagged
+            // words of the previous layer (already there: read in N)
+            const float rv = !a.stack ? 0.f
+                             : l == 0 ? __ldcg(a.resid + oo)
+                                      : __uint_as_float((uint32_t)ld_relaxed_u64(a.resid_t + oo));
+            float acc = 0.f;
+            for (int k = 0; k < K; ++k)
+                if (live[t * K + k]) acc = fmaf(w[t * K + k], cs[k * 16 + rr], acc);
+            if (has_shared) acc += cs[K * 16 + rr];
+            // the stack's output: tagged words for the next layer of the launch (a
+            // token's 16 words of a tile fill one 128-byte line, written by this
+            // warp alone), the caller's resid after the last
+            if (!a.stack)
+                a.y[oo] = acc;
+            else if (l + 1 == a.n_layers)
+                a.resid[oo] = rv + acc;
+            else
+                st_relaxed_u64(a.resid_t + oo, tagged(l + 1, __float_as_uint(rv + acc)));
+        }
+        __syncwarp();
+    }
 }
 
 // OPTS: some layer of the launch has a router scale or non-default route options;
@@ -348,8 +451,6 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
     const int ldx = H + 8;
     const int g = lane >> 2, c = lane & 3;
     const int tab_ld = a.geom.tab_ld;
-    unsigned target = 0;
-    int *s_flag = &s.misc[2];
     constexpr int S_GU = GuSplit<KIND>::S;
     constexpr int NG = kPWarps / S_GU;  // gate/up warp groups per CTA
     const QLayout &L = a.L;
@@ -385,12 +486,31 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
         // ------------------------------------------------ N: layer input
         if (a.stack) {
             // RMSNorm of resid in the canonical order of rms_partial / rms_scale;
-            // resid is staged once in shared memory
+            // resid is staged once in shared memory. Layer 0 of a launch reads the
+            // caller's resid; a later layer waits for the words the previous layer's
+            // combine wrote (tagged l), every thread for its own words.
             float *rs = reinterpret_cast<float *>(u_region);  // [T][H]
-            const float4 *r4 = reinterpret_cast<const float4 *>(a.resid);
-            for (int idx = tid; idx < T * H / 4; idx += kPersistThreads)
-                reinterpret_cast<float4 *>(rs)[idx] = __ldcg(r4 + idx);
-            __syncthreads();
+            bool fail = false;
+            if (l == 0) {
+                const float4 *r4 = reinterpret_cast<const float4 *>(a.resid);
+                for (int idx = tid; idx < T * H / 4; idx += kPersistThreads)
+                    reinterpret_cast<float4 *>(rs)[idx] = __ldcg(r4 + idx);
+            } else {
+                for (int b0 = 0; b0 < T * H && !fail; b0 += 8 * kPersistThreads) {
+                    const unsigned long long *base = a.resid_t + b0 + tid;
+                    uint32_t v[8];
+                    unsigned m = 0;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (b0 + u * kPersistThreads + tid < T * H) m |= 1u << u;
+                    fail = !wait_tagged<8>([&](int u) { return base + u * kPersistThreads; }, m, (unsigned)l, v,
+                                           Waiter{a.bar + 1, a.status});
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (m >> u & 1u) rs[b0 + u * kPersistThreads + tid] = __uint_as_float(v[u]);
+                }
+            }
+            if (__syncthreads_or(fail)) break;
             for (int t = 0; t < T; ++t) {
                 const float p = rms_partial(rs + (size_t)t * H, H, tid);
                 if (lane == 0) s.wsum[t][warp] = p;
@@ -434,7 +554,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
         {
             const int wsz = a.wr_bf16 ? 2 : 4;
             const int q = warp & 3;
-            const int nr = (E - cta + G - 1) / G;  // experts cta, cta + G, ...
+            const int nrb = (E + G - 1) / G, e0 = cta * nrb;  // my experts: e0 .. e0 + nr - 1
+            const int nr = E - e0 < nrb ? (E - e0 > 0 ? E - e0 : 0) : nrb;
             const float *const rscale = Ly.router_scale;
             auto xf = [&](int t, int h, float v[8]) {
                 if (XF32 && !a.stack)
@@ -462,15 +583,22 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                     for (int t = 0; t < T; ++t) s.rpart[r][t][q] = acc[t];
             }
             __syncthreads();
+            // publish the logits of my experts (contiguous words of each token row), or,
+            // owning none, a flag (its own 32-byte sector), tagged l + 1; the test hook
+            // leaves CTA 0's out at fault_layer
+            const int Ep = (E + 31) & ~31;  // token rows of the tagged logits padded to 32
+            unsigned long long *lgt = a.lg_t + (size_t)(l & 1) * ((size_t)T * Ep + 4 * kMaxGrid);
+            const bool publish = !(a.fault_layer == l && cta == 0);
             if (tid < nr * T) {
                 const int r = tid / T, t = tid % T;
-                const int e = cta + r * G;
+                const int e = e0 + r;
                 const float v = combine_router4(&s.rpart[r][t][0]) + (Ly.bias ? s.bias[l & 1][r] : 0.f);
-                a.logits[(size_t)t * E + e] = v;
+                if (publish) st_relaxed_u64(lgt + (size_t)t * Ep + e, tagged(l + 1, __float_as_uint(v)));
+                if (a.logits) a.logits[(size_t)t * E + e] = v;
                 if (a.trace_logits) a.trace_logits[((size_t)l * T + t) * E + e] = v;
             }
+            if (nr == 0 && tid == 0 && publish) st_relaxed_u64(lgt + (size_t)T * Ep + 4 * cta, tagged(l + 1, 1u));
         }
-        if (!grid_sync(a.bar, target, a.status, s_flag, a.fault_layer == l && cta == 0)) break;
         // ------------------------------------------------ T: top-K and the plan (every CTA)
         {
             // ord keys of the logits; token rows are padded to Ep (a multiple of 32)
@@ -487,15 +615,35 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
             const int seg = 1 << lseg, nseg = Ep >> lseg;
             const bool all_cand = E <= kCandCap;  // no threshold: every expert is a candidate
             const unsigned lt = (1u << lane) - 1u;
-            // (1) keys and segment maxima (the loop bound is uniform in each warp)
+            // (1) keys and segment maxima (the loop bound is uniform in each warp); the
+            // logits are the tagged words every CTA published (tag l + 1), read as soon
+            // as they are all there, with the flags of the CTAs (a CTA's flag follows
+            // its layer input being read)
+            const unsigned long long *lgt = a.lg_t + (size_t)(l & 1) * ((size_t)TE + 4 * kMaxGrid);
+            const int c_noexp = (E + (E + G - 1) / G - 1) / ((E + G - 1) / G);  // first CTA owning no expert
             const float inv_ep = __frcp_rn((float)Ep);  // token of flat index i: (int)((i + 0.5) / Ep), exact here
             auto tok = [&](int i) { return (int)(((float)i + 0.5f) * inv_ep); };
+            bool fail = false;
             for (int b0 = 0; b0 < TE; b0 += 4 * kPersistThreads) {
                 float v[4];
+                {
+                    // words b0 + u * 512 + tid (u < 4) of the padded rows, and (first
+                    // pass) the flag of CTA tid
+                    uint32_t vv[5];
+                    unsigned m = 0;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int idx = b0 + u * kPersistThreads + tid, t = tok(idx), e = idx - t * Ep;
-                    v[u] = (idx < TE && e < E) ? __ldcg(a.logits + (size_t)t * E + e) : 0.f;
+                    for (int u = 0; u < 4; ++u) {
+                        const int idx = b0 + u * kPersistThreads + tid, t = tok(idx), e = idx - t * Ep;
+                        if (idx < TE && e < E) m |= 1u << u;
+                    }
+                    if (b0 == 0 && c_noexp + tid < G) m |= 1u << 4;
+                    const unsigned long long *base = lgt + b0 + tid, *flag = lgt + TE + 4 * (c_noexp + tid);
+                    if (!fail)
+                        fail = !wait_tagged<5>(
+                            [&](int u) { return u < 4 ? base + u * kPersistThreads : flag; }, m, (unsigned)(l + 1), vv,
+                            Waiter{a.bar + 1, a.status});
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) v[u] = __uint_as_float(vv[u]);
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -518,7 +666,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                     }
                 }
             }
-            __syncthreads();
+            if (__syncthreads_or(fail)) break;
             // (2) threshold of each token: the K-th largest segment maximum, counted
             // with multiplicity = the smallest maximum that fewer than K maxima
             // exceed. Each maximum is a distinct entry, so at least K entries reach
@@ -572,7 +720,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                 }
             } else {
                 // too many candidates (e.g. many equal logits)
-                topk_sort_merge(a.logits, T, E, reinterpret_cast<unsigned long long *>(u_region), s.sel);
+                topk_sort_merge(lgt, T, E, reinterpret_cast<unsigned long long *>(u_region), s.sel);
             }
             __syncthreads();
             // (5) weights of token t (warp t)
@@ -847,11 +995,17 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                             }
                         }
                     }
+                    // the item's h is written: count it for its expert (release: the
+                    // warp's stores, ordered before by __syncwarp, come first)
+                    __syncwarp();
+                    if (lane == 0) {
+                        int *cnt = a.gu_cnt + (size_t)l * kMaxUnits + (shared ? nU : j / tilesF);
+                        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");
+                    }
                 }
                 asm volatile("bar.sync %0, %1;" ::"r"(grp + 1), "r"(S_GU * 32) : "memory");
             }
         }
-        if (!grid_sync(a.bar, target, a.status, s_flag)) break;
         // ------------------------------------------------ D: down projection + combine
         {
             const int n_tasks = nU + (has_shared ? 1 : 0);
@@ -870,6 +1024,18 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                     c_hi = s.ustart[(ti_hi < nU ? ti_hi : nU - 1) + 1];
                 }
                 need_sh = ti_hi >= nU;
+            }
+            // wait until every gate/up item of the experts of my units is done (down
+            // units need the expert's whole h); thread i waits for the i-th expert
+            {
+                bool fail = false;
+                if (j1 > j0) {
+                    const int u = j0 / dt + tid;
+                    if (u <= (j1 - 1) / dt)
+                        fail = !wait_count(a.gu_cnt + (size_t)l * kMaxUnits + u, u < nU ? tilesF : tilesS,
+                                           Waiter{a.bar + 1, a.status});
+                }
+                if (__syncthreads_or(fail)) break;
             }
             const int nrow = c_hi - c_lo;
             const int lo_off = ((nrow * ldh + 63) & ~63) + 32;
@@ -946,7 +1112,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                             const int rr = g + 8 * (e4 >> 1), jj = nb * 4 + 2 * c + (e4 & 1);
                             if (jj < ncols) {
                                 const int row = shared ? P + jj : s.cols[col0 + jj];
-                                a.yp[(size_t)row * H + r * 16 + rr] = v[e4];
+                                st_relaxed_u64(a.yp_t + (size_t)row * H + r * 16 + rr,
+                                               tagged(l + 1, __float_as_uint(v[e4])));
                             }
                         }
                     }
@@ -992,46 +1159,26 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                     else
                         run(std::integral_constant<int, 1>{}, std::false_type{});
                 }
-                // the last unit of row tile r to arrive combines the experts in k order; the
-                // warp's y_pair stores are ordered before lane 0's release, and the combining
-                // warp reads the others' after lane 0's acquire
-                __syncwarp();
-                int ticket = 0;
-                if (lane == 0) {
-                    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
-                                 : "=r"(ticket)
-                                 : "l"(a.d_cnt + r)
-                                 : "memory");
-                }
-                ticket = __shfl_sync(0xffffffffu, ticket, 0);
-                if (ticket == n_tasks - 1) {
-                    __syncwarp();
-                    for (int o = lane; o < T * 16; o += 32) {
-                        const int t = o >> 4, rr = o & 15;
-                        const size_t col = (size_t)r * 16 + rr, oo = (size_t)t * H + col;
-                        // every load first (one round trip), then the sum in k order
-                        float yv[32];
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            yv[k] = (k < K && s.live[t * K + k]) ? __ldcg(a.yp + (size_t)(t * K + k) * H + col) : 0.f;
-                        const float ysh = has_shared ? __ldcg(a.yp + (size_t)(P + t) * H + col) : 0.f;
-                        const float rv = a.stack ? __ldcg(a.resid + oo) : 0.f;
-                        float acc = 0.f;
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            if (k < K && s.live[t * K + k]) acc = fmaf(s.w[t * K + k], yv[k], acc);
-                        if (has_shared) acc += ysh;
-                        if (a.stack)
-                            a.resid[oo] = rv + acc;
-                        else
-                            a.y[oo] = acc;
-                    }
-                    if (lane == 0) a.d_cnt[r] = 0;
-                }
             }
-        }
-        if (a.stack && l + 1 < a.n_layers) {
-            if (!grid_sync(a.bar, target, a.status, s_flag)) break;
+            // the combine: row tile r is summed by the warp that ran the last task's unit
+            // of that tile (the shared expert's, else the last routed expert's), after all
+            // of its own units; it reads every pair's y rows of the tile as tagged words
+            // as soon as they are all there, then adds them in k order (+ the shared
+            // expert). With no task at all, warp 0 of CTA c writes tiles c, c + G, ...
+            float *cs = reinterpret_cast<float *>(ring.base);  // the combine's scratch
+            if (n_tasks > 0) {
+                for (int di = 0;; ++di) {
+                    const int j = j0 + dw + kPWarps * di;
+                    if (j >= j1) break;
+                    if (j / dt == n_tasks - 1) combine_tile(a, s.live, s.w, cs, j % dt, l, has_shared, lane);
+                }
+            } else if (warp == 0) {
+                for (int r = cta; r < dt; r += G) combine_tile(a, s.live, s.w, cs, r, l, has_shared, lane);
+            }
+            // no warp starts polling for the next layer's input before the CTA's own
+            // combines are done (polling warps of the same SM delay the combiners'
+            // loads)
+            __syncthreads();
         }
     }
     ring_drain(ring);
@@ -1104,7 +1251,8 @@ int launch_decode_persistent(const PersistArgs &a, int G, cudaStream_t s) {
     else
         kern = a.x_f32 ? MOE_PICK(MOE_Q4_32, true) : MOE_PICK(MOE_Q4_32, false);
 #undef MOE_PICK
-    MOE_CUDA_TRY(cudaMemsetAsync(a.bar, 0, (size_t)a.sync_words * sizeof(unsigned), s));
+    if (G > kMaxGrid) return set_error(MOE_ERR_UNSUPPORTED, "persistent decode: %d CTAs > %d", G, kMaxGrid);
+    MOE_CUDA_TRY(cudaMemsetAsync(a.bar, 0, a.sync_bytes, s));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(kPersistThreads);

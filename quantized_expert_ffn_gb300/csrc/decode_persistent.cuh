@@ -12,6 +12,32 @@ constexpr size_t kRedBytes = (kPersistThreads / 32) * 32 * 8 * sizeof(float);
 constexpr int kMaxRingBytes = 16384;   // weight ring per warp (bytes)
 constexpr int kCandCap = 128;          // top-K candidates per token kept by the threshold pass
 constexpr int kMaxSeg = 64;            // segment maxima per token in the threshold pass
+constexpr int kMaxGrid = 512;          // CTAs of one launch (one per SM)
+constexpr int kMaxUnits = kMaxTok * 32 + 1;  // distinct experts of a window + the shared expert
+
+// Words of the launch's synchronisation area (zeroed before every launch), in order:
+//   u32 [4]                         stop word at [1]
+//   u32 [kMaxPersistLayers][kMaxUnits]  gate/up items done per expert of the plan
+//   u64 [2][T*Ep + 4*kMaxGrid]      tagged logits (token rows padded to Ep, E rounded
+//                                   up to 32) and the flags of the CTAs that own no
+//                                   expert (one per 32 bytes), by layer parity
+//   u64 [T*H]                       tagged residual (stack)
+//   u64 [T*K + T][H]                tagged down outputs per pair (+ shared, per token)
+// A tagged word holds a 32-bit value in its low half and the layer that wrote it
+// (+1) in its high half; a reader waits until the tag it needs is there.
+struct SyncLayout {
+    size_t gu_cnt, lg_t, resid_t, yp_t, bytes;
+};
+inline SyncLayout sync_layout(int T, int H, int E, int K, int n_layers) {
+    SyncLayout S;
+    auto up16 = [](size_t v) { return (v + 15) & ~size_t(15); };
+    S.gu_cnt = 16;
+    S.lg_t = up16(S.gu_cnt + (size_t)n_layers * kMaxUnits * 4);
+    S.resid_t = S.lg_t + (size_t)2 * ((size_t)T * ((E + 31) & ~31) + 4 * kMaxGrid) * 8;
+    S.yp_t = S.resid_t + (size_t)T * H * 8;
+    S.bytes = S.yp_t + (size_t)(T * K + T) * H * 8;
+    return S;
+}
 
 // Dynamic shared memory:
 //   [wr: router rows][tab: slot-table rows, 2 layers][xs, red | hst][rings | u]
@@ -42,7 +68,7 @@ struct PersistLayer {
 
 struct PersistArgs {
     int n_layers, T, H, E, K, act, stack, wr_bf16, x_f32;
-    int fault_layer;  // test hook: CTA 0 skips its arrival at layer fault_layer's first grid barrier (-1: off)
+    int fault_layer;  // test hook: CTA 0 publishes neither its logits nor its flag at layer fault_layer (-1: off)
     float eps;
     QLayout L, LS;
     Unpack un, un_s;
@@ -50,16 +76,18 @@ struct PersistArgs {
     const void *x;        // single layer: input [T][H]
     float *y;             // single layer: output [T][H]
     float *resid;         // stack: residual [T][H], updated in place
-    float *logits;        // [T][E] (scratch, or the caller's logits_out)
+    float *logits;        // [T][E] the caller's logits_out, or null
     float *trace_logits;  // stack: [n_layers][T][E] or null
     __nv_bfloat16 *trace_in;  // stack: [n_layers][T][H] or null
     int32_t *ids_out;     // single layer: [T][K] or null
     __nv_bfloat16 *h_hi, *h_lo;  // [T*K + T][h_ld]
     int h_ld;
-    float *yp;            // [T*K + T][H] per-pair down outputs
-    int *d_cnt;           // [H/16] arrivals per output row tile
-    unsigned *bar;        // [2]: arrivals, stop word; then the counters (all zeroed per launch)
-    int sync_words;       // 32-bit words zeroed before each launch from bar on
+    unsigned long long *yp_t;  // [T*K + T][H] tagged per-pair down outputs
+    unsigned *bar;        // the synchronisation area (SyncLayout), zeroed before each launch
+    int *gu_cnt;          // [n_layers][kMaxUnits] gate/up items done per plan expert
+    unsigned long long *lg_t;     // [2][T*Ep + 4*kMaxGrid] tagged logits, flags
+    unsigned long long *resid_t;  // [T*H] tagged residual between the layers of a stack
+    size_t sync_bytes;    // bytes of the synchronisation area
     uint32_t *status;
     PersistLayer layers[kMaxPersistLayers];
 };
