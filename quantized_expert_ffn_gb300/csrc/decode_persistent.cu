@@ -723,134 +723,202 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                 topk_sort_merge(lgt, T, E, reinterpret_cast<unsigned long long *>(u_region), s.sel);
             }
             __syncthreads();
-            // (5) weights of token t (warp t)
-            if (warp < T) {
-                const int t = warp;
-                const unsigned long long key = s.sel[t][lane];
-                const int si = topk_key_index(key);
-                const float sv = topk_key_value(key);
-                const bool bad = s.misc[4 + t] != 0;
-                const float m = topk_key_value(s.sel[t][0]);
-                float wk;
-                if (bad) {
-                    wk = __int_as_float(0x7fc00000);
-                    if (OPTS && lane == 0 && cta == 0 && Ly.route.omitted) Ly.route.omitted[t] = 0.f;
-                } else if constexpr (OPTS) {
-                    wk = route_weight(Ly.route, sv, m, si, K, lane, s.wex[t],
-                                      reinterpret_cast<int *>(u_region) + t * 64,
-                                      cta == 0 ? Ly.route.omitted : nullptr, t);
-                } else {
-                    wk = topk_weight_smem(sv, m, K, lane, s.wex[t]);
-                }
-                if (lane < K) {
-                    s.ids[t * K + lane] = si;
-                    s.w[t * K + lane] = wk;
-                    if (a.ids_out && cta == 0) a.ids_out[(size_t)t * K + lane] = si;
-                }
-                if (bad && lane == 0 && cta == 0) set_status(a.status, MOE_STATUS_NONFINITE);
-            }
-            // (6) stable order of pairs by expert: rank = #{q : (id_q, q) < (id_p, p)}
-            if (T == 1 && P <= 32) {
-                // one token: its pairs are warp 0's lanes
+            // down units (expert-major: unit j = expert j / dt, row tile j % dt) split
+            // over the CTAs by down bytes: CTA c takes the units whose byte midpoint
+            // falls in [c D / G, (c + 1) D / G) (single-precision arithmetic: CTA c and
+            // CTA c + 1 evaluate the same boundary with the same operations, so the
+            // ranges tile [0, n_units)); called by one thread
+            auto set_units = [&](int nu) {
+                const bool sh = Ly.shared != nullptr;
+                const int nr_units = nu * dt;
+                const int n_units = nr_units + (sh ? dt : 0);
+                const float dr = (float)L.d_tile_bytes, dsb = sh ? (float)a.LS.d_tile_bytes : 0.f;
+                const float Dr = (float)nr_units * dr, Dtot = Dr + (float)dt * dsb;
+                auto first_unit = [&](int c) -> int {
+                    if (c <= 0) return 0;
+                    const float b = __fdividef(Dtot * (float)c, (float)G);
+                    const float x = b - 0.5f * dr;  // routed: j*dr + dr/2 >= b
+                    const int j = x <= 0.f ? 0 : (int)ceilf(__fdividef(x, dr));
+                    if (j < nr_units || !sh) return j < nr_units ? j : nr_units;
+                    const float y = b - Dr - 0.5f * dsb;  // shared: Dr + k*dsb + dsb/2 >= b
+                    const int jj = nr_units + (y <= 0.f ? 0 : (int)ceilf(__fdividef(y, dsb)));
+                    return jj < n_units ? jj : n_units;
+                };
+                s.misc[12] = first_unit(cta);
+                s.misc[13] = cta == G - 1 ? n_units : first_unit(cta + 1);
+            };
+            if (T == 1 && !OPTS) {
+                // one token (K <= 32 pairs of distinct experts): weights, the order by
+                // expert and the plan in warp 0's registers, the same arithmetic as the
+                // steps below (the softmax sum in k order)
                 if (warp == 0) {
-                    __syncwarp();
-                    const int ep = lane < P ? s.ids[lane] : 0x7FFFFFFF;
-                    int r = 0;
-                    for (int q = 0; q < P; ++q) {
-                        const int eq = s.ids[q];
-                        r += (eq < ep) | ((eq == ep) & (q < lane));
-                    }
-                    if (lane < P) s.sorted[r] = lane;
-                    __syncwarp();
-                }
-            } else {
-                __syncthreads();
-                if (tid < P) {
-                    const int ep = s.ids[tid];
-                    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-#pragma unroll 2
-                    for (int q4 = 0; q4 < P; q4 += 4) {
-                        const int4 v4 = *reinterpret_cast<const int4 *>(s.ids + q4);
-                        r0 += (q4 < P) & ((v4.x < ep) | ((v4.x == ep) & (q4 < tid)));
-                        r1 += (q4 + 1 < P) & ((v4.y < ep) | ((v4.y == ep) & (q4 + 1 < tid)));
-                        r2 += (q4 + 2 < P) & ((v4.z < ep) | ((v4.z == ep) & (q4 + 2 < tid)));
-                        r3 += (q4 + 3 < P) & ((v4.w < ep) | ((v4.w == ep) & (q4 + 3 < tid)));
-                    }
-                    s.sorted[(r0 + r1) + (r2 + r3)] = tid;
-                }
-                __syncthreads();
-            }
-            if (warp == 0) {
-                int running = 0;
-                bool absent = false, oob = false;
-                for (int base = 0; base < P; base += 32) {
-                    const int r = base + lane;
-                    int p = -1, e = -1, slot = -1, live = 0;
-                    if (r < P) {
-                        p = s.sorted[r];
-                        e = s.ids[p];
-                        slot = tab[e];
+                    const unsigned long long key = s.sel[0][lane];
+                    const int si = lane < K ? topk_key_index(key) : 0x7FFFFFFF;
+                    const float sv = topk_key_value(key);
+                    const float m = __shfl_sync(0xffffffffu, sv, 0);
+                    const bool bad = s.misc[4] != 0;
+                    const float ex = (lane < K && !bad) ? expf(sv - m) : 0.f;
+                    // loops unrolled to 32 so that every shuffle is issued up front (lanes
+                    // k >= K hold ex = 0: adding them leaves the sum's bits unchanged)
+                    float exk[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) exk[k] = __shfl_sync(0xffffffffu, ex, k);
+                    float sum = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) sum += exk[k];
+                    const float wk = bad ? __int_as_float(0x7fc00000) : ex / sum;
+                    int rank = 0;  // place in expert order (the K experts are distinct)
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) rank += __shfl_sync(0xffffffffu, si, q) < si;
+                    int slot = -1;
+                    bool absent = false, oob = false, live = false;
+                    if (lane < K) {
+                        slot = tab[si];
                         if (slot < 0) absent = true;
                         else if (slot >= Ly.capacity) oob = true;
-                        else live = s.w[p] != 0.f;
-                        s.live[p] = live;
+                        else live = wk != 0.f;
+                        s.ids[lane] = si;
+                        s.w[lane] = wk;
+                        s.live[lane] = live;
+                        if (a.ids_out && cta == 0) a.ids_out[lane] = si;
                     }
-                    const unsigned m = __ballot_sync(0xffffffffu, live);
+                    const unsigned lm = __ballot_sync(0xffffffffu, live);
+                    int pos = 0;  // place among the live pairs in expert order
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int rq = __shfl_sync(0xffffffffu, rank, q);
+                        pos += (int)((lm >> q) & 1u) & (rq < rank);
+                    }
                     if (live) {
-                        const int pos = running + __popc(m & ((1u << lane) - 1));
-                        s.cols[pos] = p;
-                        s.cexp[pos] = e;
-                        s.cslot[pos] = slot;
+                        s.cols[pos] = lane;
+                        s.cexp[pos] = s.uexp[pos] = si;
+                        s.cslot[pos] = s.uslot[pos] = slot;
+                        s.ustart[pos] = pos;
                     }
-                    running += __popc(m);
-                }
-                absent = __any_sync(0xffffffffu, absent);
-                oob = __any_sync(0xffffffffu, oob);
-                if (cta == 0 && lane == 0) {
-                    if (absent) set_status(a.status, MOE_STATUS_EXPERT_ABSENT);
-                    if (oob) set_status(a.status, MOE_STATUS_BOUNDS);
-                }
-                __syncwarp();
-                const int nlive = running;
-                int nu = 0;
-                for (int base = 0; base < nlive; base += 32) {
-                    const int i = base + lane;
-                    const bool first = i < nlive && (i == 0 || s.cexp[i - 1] != s.cexp[i]);
-                    const unsigned m = __ballot_sync(0xffffffffu, first);
-                    if (first) {
-                        const int u = nu + __popc(m & ((1u << lane) - 1));
-                        s.ustart[u] = i;
-                        s.uexp[u] = s.cexp[i];
-                        s.uslot[u] = s.cslot[i];
+                    absent = __any_sync(0xffffffffu, absent);
+                    oob = __any_sync(0xffffffffu, oob);
+                    if (cta == 0 && lane == 0) {
+                        if (bad) set_status(a.status, MOE_STATUS_NONFINITE);
+                        if (absent) set_status(a.status, MOE_STATUS_EXPERT_ABSENT);
+                        if (oob) set_status(a.status, MOE_STATUS_BOUNDS);
                     }
-                    nu += __popc(m);
+                    if (lane == 0) {
+                        const int nlive = __popc(lm);
+                        s.ustart[nlive] = nlive;
+                        s.misc[0] = nlive;
+                        s.misc[1] = nlive;
+                        set_units(nlive);
+                    }
                 }
-                if (lane == 0) {
-                    s.ustart[nu] = nlive;
-                    s.misc[0] = nu;
-                    s.misc[1] = nlive;
-                    // down units (expert-major: unit j = expert j / dt, row tile j % dt)
-                    // split over the CTAs by down bytes: CTA c takes the units whose
-                    // byte midpoint falls in [c D / G, (c + 1) D / G)
-                    // (single-precision arithmetic: CTA c and CTA c + 1 evaluate the same
-                    // boundary with the same operations, so the ranges tile [0, n_units))
-                    const bool sh = Ly.shared != nullptr;
-                    const int nr_units = nu * dt;
-                    const int n_units = nr_units + (sh ? dt : 0);
-                    const float dr = (float)L.d_tile_bytes, dsb = sh ? (float)a.LS.d_tile_bytes : 0.f;
-                    const float Dr = (float)nr_units * dr, Dtot = Dr + (float)dt * dsb;
-                    auto first_unit = [&](int c) -> int {
-                        if (c <= 0) return 0;
-                        const float b = __fdividef(Dtot * (float)c, (float)G);
-                        const float x = b - 0.5f * dr;  // routed: j*dr + dr/2 >= b
-                        const int j = x <= 0.f ? 0 : (int)ceilf(__fdividef(x, dr));
-                        if (j < nr_units || !sh) return j < nr_units ? j : nr_units;
-                        const float y = b - Dr - 0.5f * dsb;  // shared: Dr + k*dsb + dsb/2 >= b
-                        const int jj = nr_units + (y <= 0.f ? 0 : (int)ceilf(__fdividef(y, dsb)));
-                        return jj < n_units ? jj : n_units;
-                    };
-                    s.misc[12] = first_unit(cta);
-                    s.misc[13] = cta == G - 1 ? n_units : first_unit(cta + 1);
+            } else {
+                // (5) weights of token t (warp t)
+                if (warp < T) {
+                    const int t = warp;
+                    const unsigned long long key = s.sel[t][lane];
+                    const int si = topk_key_index(key);
+                    const float sv = topk_key_value(key);
+                    const bool bad = s.misc[4 + t] != 0;
+                    const float m = topk_key_value(s.sel[t][0]);
+                    float wk;
+                    if (bad) {
+                        wk = __int_as_float(0x7fc00000);
+                        if (OPTS && lane == 0 && cta == 0 && Ly.route.omitted) Ly.route.omitted[t] = 0.f;
+                    } else if constexpr (OPTS) {
+                        wk = route_weight(Ly.route, sv, m, si, K, lane, s.wex[t],
+                                          reinterpret_cast<int *>(u_region) + t * 64,
+                                          cta == 0 ? Ly.route.omitted : nullptr, t);
+                    } else {
+                        wk = topk_weight_smem(sv, m, K, lane, s.wex[t]);
+                    }
+                    if (lane < K) {
+                        s.ids[t * K + lane] = si;
+                        s.w[t * K + lane] = wk;
+                        if (a.ids_out && cta == 0) a.ids_out[(size_t)t * K + lane] = si;
+                    }
+                    if (bad && lane == 0 && cta == 0) set_status(a.status, MOE_STATUS_NONFINITE);
+                }
+                // (6) stable order of pairs by expert: rank = #{q : (id_q, q) < (id_p, p)}
+                if (T == 1 && P <= 32) {
+                    // one token: its pairs are warp 0's lanes
+                    if (warp == 0) {
+                        __syncwarp();
+                        const int ep = lane < P ? s.ids[lane] : 0x7FFFFFFF;
+                        int r = 0;
+                        for (int q = 0; q < P; ++q) {
+                            const int eq = s.ids[q];
+                            r += (eq < ep) | ((eq == ep) & (q < lane));
+                        }
+                        if (lane < P) s.sorted[r] = lane;
+                        __syncwarp();
+                    }
+                } else {
+                    __syncthreads();
+                    if (tid < P) {
+                        const int ep = s.ids[tid];
+                        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+    #pragma unroll 2
+                        for (int q4 = 0; q4 < P; q4 += 4) {
+                            const int4 v4 = *reinterpret_cast<const int4 *>(s.ids + q4);
+                            r0 += (q4 < P) & ((v4.x < ep) | ((v4.x == ep) & (q4 < tid)));
+                            r1 += (q4 + 1 < P) & ((v4.y < ep) | ((v4.y == ep) & (q4 + 1 < tid)));
+                            r2 += (q4 + 2 < P) & ((v4.z < ep) | ((v4.z == ep) & (q4 + 2 < tid)));
+                            r3 += (q4 + 3 < P) & ((v4.w < ep) | ((v4.w == ep) & (q4 + 3 < tid)));
+                        }
+                        s.sorted[(r0 + r1) + (r2 + r3)] = tid;
+                    }
+                    __syncthreads();
+                }
+                if (warp == 0) {
+                    int running = 0;
+                    bool absent = false, oob = false;
+                    for (int base = 0; base < P; base += 32) {
+                        const int r = base + lane;
+                        int p = -1, e = -1, slot = -1, live = 0;
+                        if (r < P) {
+                            p = s.sorted[r];
+                            e = s.ids[p];
+                            slot = tab[e];
+                            if (slot < 0) absent = true;
+                            else if (slot >= Ly.capacity) oob = true;
+                            else live = s.w[p] != 0.f;
+                            s.live[p] = live;
+                        }
+                        const unsigned m = __ballot_sync(0xffffffffu, live);
+                        if (live) {
+                            const int pos = running + __popc(m & ((1u << lane) - 1));
+                            s.cols[pos] = p;
+                            s.cexp[pos] = e;
+                            s.cslot[pos] = slot;
+                        }
+                        running += __popc(m);
+                    }
+                    absent = __any_sync(0xffffffffu, absent);
+                    oob = __any_sync(0xffffffffu, oob);
+                    if (cta == 0 && lane == 0) {
+                        if (absent) set_status(a.status, MOE_STATUS_EXPERT_ABSENT);
+                        if (oob) set_status(a.status, MOE_STATUS_BOUNDS);
+                    }
+                    __syncwarp();
+                    const int nlive = running;
+                    int nu = 0;
+                    for (int base = 0; base < nlive; base += 32) {
+                        const int i = base + lane;
+                        const bool first = i < nlive && (i == 0 || s.cexp[i - 1] != s.cexp[i]);
+                        const unsigned m = __ballot_sync(0xffffffffu, first);
+                        if (first) {
+                            const int u = nu + __popc(m & ((1u << lane) - 1));
+                            s.ustart[u] = i;
+                            s.uexp[u] = s.cexp[i];
+                            s.uslot[u] = s.cslot[i];
+                        }
+                        nu += __popc(m);
+                    }
+                    if (lane == 0) {
+                        s.ustart[nu] = nlive;
+                        s.misc[0] = nu;
+                        s.misc[1] = nlive;
+                        set_units(nu);
+                    }
                 }
             }
             __syncthreads();
