@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill (T=4096 Gemma-shaped layer) line")
     ap.add_argument("--no-residency", action="store_true", help="skip the residency-policy replay and load line")
+    ap.add_argument("--no-verify", action="store_true",
+                    help="skip the 48-layer chain at T=4 and the single Q2_0 layer at T=1 and T=4")
     ap.add_argument("--no-gemma-decode", action="store_true",
                     help="skip the Gemma-shaped layer's decode and verify windows (T = 1, 2, 8)")
     return ap.parse_args()
@@ -393,6 +395,94 @@ def run_gemma_decode(L, torch, ctx, Ts=(1, 2, 8), n_layers: int = 16, steps: int
     return rows
 
 
+def distinct_per_layer(lg, K):
+    """Distinct experts chosen per layer from traced logits [layers][T][E] (larger
+    logit first, ties to the lower index)."""
+    out = []
+    for ll in lg:
+        chosen = set()
+        for row in ll:
+            order = np.lexsort((np.arange(row.size), -row))
+            chosen.update(int(e) for e in order[:K])
+        out.append(len(chosen))
+    return out
+
+
+def run_stack_window(L, torch, ctx, st, T: int, steps: int = 100, warmup: int = 5):
+    """The 48-layer chain at a T-token verify window: graph replays of one
+    moe_stack_forward per step; distinct experts per layer from a traced pass."""
+    cfg = st.cfg
+    n = len(st.descs)
+    ws = torch.empty(L.moe_layer_workspace(st.descs[0], T) + T * cfg.H * 4 + 4096, dtype=torch.uint8, device="cuda")
+    resid = torch.from_numpy(C.as_f64(C.activations(cfg, T, step=40 + T)).astype(np.float32)).cuda()
+    stream = torch.cuda.Stream()
+    tlg = torch.empty(n, T, cfg.E, dtype=torch.float32, device="cuda")
+    tin = torch.empty(n, T, cfg.H, dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(stream):
+        L.moe_stack_forward(ctx, st.descs, resid.clone(), EPS, ws, tin, tlg)
+    stream.synchronize()
+    status = L.moe_status(ctx, stream)
+    path = L.moe_ctx_get_option(ctx, L.OPT_LAST_PATH)
+    distinct = distinct_per_layer(tlg.cpu().numpy(), cfg.K)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        L.moe_stack_forward(ctx, st.descs, resid, EPS, ws)
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del graph
+    return dict(T=T, ms_per_step=ms, distinct=distinct, status=status, path=path)
+
+
+def run_q2_single_layer(L, torch, ctx, st, Ts=(1, 4), steps: int = 30, warmup: int = 3):
+    """The single Q2_0 layer (H=2560, 512 experts, top-10, F=640) in decode and verify
+    windows: one moe_layer_forward per layer on each of the stack's 48 distinct layers
+    (34 GB of experts, so every call's bytes come from HBM), the 48 calls captured in
+    a graph and replayed, the same T-token input to every layer."""
+    cfg = st.cfg
+    n = len(st.descs)
+    stream = torch.cuda.Stream()
+    rows = []
+    ws = torch.empty(L.moe_layer_workspace(st.descs[0], max(Ts)), dtype=torch.uint8, device="cuda")
+    for T in Ts:
+        x = torch.from_numpy(C.activations(cfg, T, step=8000 + T).view(np.int16)).view(torch.bfloat16).cuda()
+        y = torch.empty(T, cfg.H, device="cuda")
+        lg = torch.empty(n, T, cfg.E, dtype=torch.float32, device="cuda")
+        with torch.cuda.stream(stream):
+            for l in range(n):
+                L.moe_layer_forward(ctx, st.descs[l], x, y, ws, logits=lg[l], stream=stream)
+        stream.synchronize()
+        status = L.moe_status(ctx, stream)
+        path = L.moe_ctx_get_option(ctx, L.OPT_LAST_PATH)
+        distinct = distinct_per_layer(lg.cpu().numpy(), cfg.K)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for l in range(n):
+                L.moe_layer_forward(ctx, st.descs[l], x, y, ws, stream=stream)
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_layer = e0.elapsed_time(e1) / (steps * n)
+        del graph
+        rows.append(dict(T=T, ms_per_layer=ms_layer, distinct=float(np.mean(distinct)), status=status, path=path))
+    return rows
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from quantized_expert_ffn_gb300 import _lib as L
@@ -419,14 +509,7 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         L.moe_stack_forward(ctx, st.descs, resid.clone(), EPS, ws, tin, tlg)
     stream.synchronize()
-    lg = tlg.cpu().numpy()
-    distinct = []
-    for l in range(args.layers):
-        chosen = set()
-        for t in range(T):
-            order = np.lexsort((np.arange(cfg.E), -lg[l, t]))  # logit descending, index ascending
-            chosen.update(int(e) for e in order[:cfg.K])
-        distinct.append(len(chosen))
+    distinct = distinct_per_layer(tlg.cpu().numpy(), cfg.K)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         L.moe_stack_forward(ctx, st.descs, resid, EPS, ws)
@@ -482,13 +565,15 @@ def run_ours(args, rank, world, local_rank):
     stream.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
+    verify = None if args.no_verify else run_stack_window(L, torch, ctx, st, 4)
+    single = None if args.no_verify else run_q2_single_layer(L, torch, ctx, st)
     pre = None if args.no_prefill else run_prefill(L, torch, ctx)
     gemma = None if args.no_gemma_decode else run_gemma_decode(L, torch, ctx)
     resid_line = None if (args.no_residency or rank != 0) else run_residency(L, torch, ctx)
 
     ms, e2e_ms_max = max_over_ranks([ms, e2e_ms], "cuda")
     return dict(ms=ms, e2e_ms=e2e_ms_max, layer_ms=layer_ms, clocks=clocks, status=status, cfg=cfg, path=path,
-                distinct=distinct, prefill=pre, gemma=gemma, residency=resid_line)
+                distinct=distinct, prefill=pre, gemma=gemma, residency=resid_line, verify=verify, single=single)
 
 
 # ------------------------------------------------------------------ oracle (CPU)
@@ -524,6 +609,77 @@ def oracle_sample_rate(seconds: float, T: int = 1, max_steps: int | None = None)
     return (done * T / busy if busy > 0 else 0.0), done, busy
 
 
+def oracle_sample_rate_threads(seconds: float, T: int = 1, threads: int | None = None, rounds: int | None = None,
+                               warmup_rounds: int = 0):
+    """The same oracle work on every host core: one thread per core, each running
+    layer-token samples (router, top-k, layer) for about `seconds` of wall time; the
+    inputs are generated before the timed window (the oracle's C calls release the
+    Python lock, so the threads run in parallel). With `rounds`, every thread runs
+    exactly that many samples instead (after `warmup_rounds` untimed ones). Returns
+    (layer-tokens/s, threads, samples done, wall seconds)."""
+    import concurrent.futures as cf
+    import oracle
+    cfg = C.CONFIGS["q2_stack"]
+    oracle.build()
+    n = threads or os.cpu_count() or 1
+    samples = []
+    for i in range(n):
+        layer = i % cfg.layers
+        Wr = C.as_f64(C.router_weights(cfg, layer))
+        b = C.router_bias(cfg, layer).astype(np.float64)
+        x = oracle.rmsnorm(C.as_f64(C.activations(cfg, T, step=2000 + i)), EPS)
+        lg = oracle.router_logits(x, Wr, b)
+        ids, _, _ = oracle.topk(lg, cfg.K)
+        need = np.unique(ids)
+        blobs = C.experts(cfg, layer, need)
+        experts = [None] * cfg.E
+        for j, e in enumerate(need):
+            experts[int(e)] = blobs[j]
+        samples.append((Wr, b, x, experts))
+
+    def work(i, deadline, rounds=None):
+        Wr, b, x, experts = samples[i]
+        done = 0
+        while (time.perf_counter() < deadline) if rounds is None else (done < rounds):
+            lg = oracle.router_logits(x, Wr, b)
+            oracle.topk(lg, cfg.K)
+            oracle.layer_forward(cfg.kind, cfg.zero_point, cfg.H, cfg.E, cfg.K, cfg.F, None, None, experts, x,
+                                 logits_in=lg)
+            done += 1
+        return done
+
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        if warmup_rounds:
+            list(ex.map(lambda i: work(i, 0.0, warmup_rounds), range(n)))
+        t0 = time.perf_counter()
+        if rounds is not None:
+            done = sum(ex.map(lambda i: work(i, 0.0, rounds), range(n)))
+        else:
+            done = sum(ex.map(lambda i: work(i, t0 + seconds), range(n)))
+        wall = time.perf_counter() - t0
+    return done * T / wall, n, done, wall
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for key in ("Model name", "BIOS Model name"):
+            for line in out.splitlines():
+                if line.startswith(key + ":"):
+                    name = line.split(":", 1)[1].strip()
+                    if name and name != "-":
+                        return name
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -537,16 +693,17 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
-        if args.warmup > 0:  # W untimed steps of the same work
-            oracle_sample_rate(1e9, args.T, max_steps=args.warmup)
-        rate, done, busy = oracle_sample_rate(1e9, args.T, max_steps=args.steps)
+        # a step: every host core runs one layer-step of the workload (W untimed steps
+        # first); the oracle's C calls run in parallel threads
+        rate, nthr, done, wall = oracle_sample_rate_threads(0.0, args.T, rounds=args.steps,
+                                                            warmup_rounds=args.warmup)
         line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": n_gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": busy / max(done, 1) * 1e3,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / max(args.steps, 1) * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": cfgj,
-                "cpu_baseline": {"kind": "oracle", "value": rate, "unit": UNIT, "cores": 1,
-                                 "sample": f"{done} layer-steps of one {args.T}-token window each "
-                                           f"(router, top-k, experts, combine; fp64, one thread)"},
+                "cpu_baseline": {"kind": "oracle", "value": rate, "unit": UNIT, "cores": nthr, "cpu": cpu_model(),
+                                 "sample": f"{done} layer-steps of one {args.T}-token window each on {nthr} threads "
+                                           f"(router, top-k, experts, combine; fp64)"},
                 "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return 0
@@ -621,13 +778,47 @@ def main():
                         "16 distinct layers (~7 GB) replayed, one moe_layer_forward per layer",
             "unit": "layer-tokens/s", "hbm_peak_gbs": hbm,
             "rows": [dict(row, frac_of_hbm=row["gbs"] / hbm) for row in r["gemma"]]}
+    if r.get("verify"):
+        v = r["verify"]
+        vb = sum(v["distinct"]) * expert_bytes + args.layers * router_bytes
+        gbs = vb / (v["ms_per_step"] / 1e3) / 1e9
+        line["verify_window"] = {
+            "workload": f"the same {args.layers}-layer Q2_0 chain at a {v['T']}-token verify window "
+                        "(one moe_stack_forward per step, graph replays)",
+            "T": v["T"], "ms_per_step": v["ms_per_step"],
+            "layer_tokens_per_s": job_value(n_gpus, args.layers * v["T"], v["ms_per_step"]),
+            "stack_tokens_per_s": job_value(n_gpus, v["T"], v["ms_per_step"]),
+            "distinct_experts_per_layer": float(np.mean(v["distinct"])), "bytes_per_step": vb,
+            "gbs": gbs, "frac_of_hbm": gbs / hbm_peak, "hbm_peak_gbs": hbm_peak,
+            "path": {1: "persistent", 2: "tcgen05 grouped GEMMs", 0: "mma.sync"}.get(v["path"], str(v["path"])),
+            "device_status": v["status"]}
+    if r.get("single"):
+        rows = []
+        for row in r["single"]:
+            b = row["distinct"] * expert_bytes + router_bytes
+            gbs = b / (row["ms_per_layer"] / 1e3) / 1e9
+            rows.append(dict(T=row["T"], ms_per_layer=row["ms_per_layer"],
+                             layer_tokens_per_s=row["T"] / (row["ms_per_layer"] / 1e3),
+                             distinct_experts=row["distinct"], bytes_per_layer=b, gbs=gbs, frac_of_hbm=gbs / hbm_peak,
+                             path={1: "persistent", 2: "tcgen05 grouped GEMMs", 0: "mma.sync"}.get(row["path"],
+                                                                                                 str(row["path"])),
+                             status=row["status"]))
+        line["q2_layer_decode"] = {
+            "workload": "single Q2_0 layer H=2560 E=512 top-10 F=640 (Zipf(1.1) router bias), one moe_layer_forward "
+                        f"per layer on each of the {args.layers} distinct layers of the chain (34 GB), graph replays",
+            "unit": "layer-tokens/s", "hbm_peak_gbs": hbm_peak,
+            "bytes": "per layer: distinct experts x 1,382,400 B + router 2,621,440 B", "rows": rows}
     if r.get("residency"):
         line["residency"] = r["residency"]
     if rank == 0 and not args.no_cpu_baseline:
-        rate, done, busy = oracle_sample_rate(10.0, T)
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": f"{done} layer-steps ({T}-token windows) of the same layers, "
-                                          f"{busy:.1f} s of fp64 single-thread work"}
+        rate1, done1, busy1 = oracle_sample_rate(8.0, T)
+        rate, nthr, done, wall = oracle_sample_rate_threads(8.0, T)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": nthr, "kind": "oracle",
+                                "cpu": cpu_model(),
+                                "sample": f"{done} layer-steps ({T}-token windows) of the chain's layers on {nthr} "
+                                          f"threads, {wall:.1f} s wall (fp64; inputs generated outside the timing)",
+                                "single_thread": {"value": rate1, "unit": UNIT, "cores": 1,
+                                                  "sample": f"{done1} layer-steps, {busy1:.1f} s of one thread"}}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
