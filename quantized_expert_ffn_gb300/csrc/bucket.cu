@@ -43,6 +43,43 @@ __device__ int block_exclusive_scan(int v, int *total, int *scratch /* >= 33 int
     return warp_base + inc - v;
 }
 
+// The groups of one expert's my_lc live pairs (plan columns my_cs ..), at most nc
+// columns each; every thread of the CTA calls it (tid < E: expert tid). With
+// nc = 256 (the tensor-core GEMMs, whose CTAs take tiles round-robin in list
+// order) the list is ordered for the schedule: every full group first, in expert
+// order, then the partial groups from the largest down, so that the longest tiles
+// start first. A group's tiles compute their outputs alone, so the order changes
+// no result. Other widths keep expert order. *total = number of groups.
+__device__ void emit_groups(int E, int my_lc, int my_cs, int slot, int nc, Group *groups, int *total, int *scr) {
+    __shared__ int hist[256];
+    const int tid = threadIdx.x;
+    if (nc != 256) {
+        const int ng = tid < E ? (my_lc + nc - 1) / nc : 0;
+        const int gb = block_exclusive_scan(ng, total, scr);
+        if (tid < E)
+            for (int j = 0; j < ng; ++j) groups[gb + j] = Group{slot, my_cs + j * nc, min(nc, my_lc - j * nc), 0};
+        return;
+    }
+    const int nfull = tid < E ? my_lc / 256 : 0, part = tid < E ? my_lc % 256 : 0;
+    int tot_full, tot_part;
+    const int fb = block_exclusive_scan(nfull, &tot_full, scr);
+    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const int rank = part > 0 ? atomicAdd(&hist[part], 1) : 0;  // place among groups of its size
+    __syncthreads();
+    // start of each size's run: the full groups, then sizes 255, 254, ..., 1
+    const int v = tid < 255 ? hist[255 - tid] : 0;
+    const int start = block_exclusive_scan(v, &tot_part, scr);
+    if (tid < 255) hist[255 - tid] = start;
+    __syncthreads();
+    if (tid < E) {
+        for (int j = 0; j < nfull; ++j) groups[fb + j] = Group{slot, my_cs + j * 256, 256, 0};
+        if (part > 0) groups[tot_full + hist[part] + rank] = Group{slot, my_cs + nfull * 256, part, 0};
+    }
+    *total = tot_full + tot_part;
+    __syncthreads();
+}
+
 // One CTA of 1024 threads. Counting pass (order-free), exclusive scan, then the
 // stable placement: pairs are placed in chunks of 1024 in pair order; inside a
 // chunk a pair's rank among equal experts = (count in earlier warps) + (count in
@@ -190,18 +227,10 @@ __global__ void __launch_bounds__(kBucketThreads) k_plan(PlanArgs a) {
     if (tid < E) cstart[tid] = my_cs;
     __syncthreads();
     // groups
-    const int ng_gu = tid < E ? (my_lc + a.nc_gu - 1) / a.nc_gu : 0;
-    const int ng_d = tid < E ? (my_lc + a.nc_d - 1) / a.nc_d : 0;
     int tot_gu, tot_d;
-    const int gb_gu = block_exclusive_scan(ng_gu, &tot_gu, scr);
-    const int gb_d = block_exclusive_scan(ng_d, &tot_d, scr);
-    if (tid < E && my_lc > 0) {
-        const int slot = a.table[(size_t)a.layer * E + tid];
-        for (int j = 0; j < ng_gu; ++j)
-            a.groups_gu[gb_gu + j] = Group{slot, my_cs + j * a.nc_gu, min(a.nc_gu, my_lc - j * a.nc_gu), 0};
-        for (int j = 0; j < ng_d; ++j)
-            a.groups_d[gb_d + j] = Group{slot, my_cs + j * a.nc_d, min(a.nc_d, my_lc - j * a.nc_d), 0};
-    }
+    const int slot = (tid < E && my_lc > 0) ? a.table[(size_t)a.layer * E + tid] : -1;
+    emit_groups(E, tid < E ? my_lc : 0, my_cs, slot, a.nc_gu, a.groups_gu, &tot_gu, scr);
+    emit_groups(E, tid < E ? my_lc : 0, my_cs, slot, a.nc_d, a.groups_d, &tot_d, scr);
     if (tid == 0) {
         a.n_groups[0] = tot_gu;
         a.n_groups[1] = tot_d;
@@ -352,18 +381,10 @@ __global__ void __launch_bounds__(kBucketThreads) k_plan_groups(PlanArgs a, int 
     const int my_lc = tid < E ? lc[tid] : 0;
     int dummy;
     const int my_cs = block_exclusive_scan(my_lc, &dummy, scr);
-    const int ng_gu = tid < E ? (my_lc + a.nc_gu - 1) / a.nc_gu : 0;
-    const int ng_d = tid < E ? (my_lc + a.nc_d - 1) / a.nc_d : 0;
     int tot_gu, tot_d;
-    const int gb_gu = block_exclusive_scan(ng_gu, &tot_gu, scr);
-    const int gb_d = block_exclusive_scan(ng_d, &tot_d, scr);
-    if (tid < E && my_lc > 0) {
-        const int slot = a.table[(size_t)a.layer * E + tid];
-        for (int j = 0; j < ng_gu; ++j)
-            a.groups_gu[gb_gu + j] = Group{slot, my_cs + j * a.nc_gu, min(a.nc_gu, my_lc - j * a.nc_gu), 0};
-        for (int j = 0; j < ng_d; ++j)
-            a.groups_d[gb_d + j] = Group{slot, my_cs + j * a.nc_d, min(a.nc_d, my_lc - j * a.nc_d), 0};
-    }
+    const int slot = (tid < E && my_lc > 0) ? a.table[(size_t)a.layer * E + tid] : -1;
+    emit_groups(E, my_lc, my_cs, slot, a.nc_gu, a.groups_gu, &tot_gu, scr);
+    emit_groups(E, my_lc, my_cs, slot, a.nc_d, a.groups_d, &tot_d, scr);
     if (tid == 0) {
         a.n_groups[0] = tot_gu;
         a.n_groups[1] = tot_d;

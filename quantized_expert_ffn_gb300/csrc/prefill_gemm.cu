@@ -226,7 +226,7 @@ struct TileInfo {
     int nk;  // K stages
 };
 
-// Tile t of one launch: t = (group, M-tile).
+// Tile t of one launch: t = (group, M-tile), the shared expert's groups first.
 __device__ __forceinline__ bool tile_info(const UmmaArgs &a, int n_routed, int t, TileInfo &ti) {
     if (a.mode == 2) {
         // router: tile t = (128 experts mt, kRN tokens nt)
@@ -237,19 +237,22 @@ __device__ __forceinline__ bool tile_info(const UmmaArgs &a, int n_routed, int t
         ti.nk = a.H / kBK;
         return ti.grp.ncols > 0;
     }
+    // the shared expert's tiles (all of them full width) first, then the routed
+    // groups in the plan's list order (full groups, then partial ones largest first):
+    // CTAs take tiles round-robin, so the longest tiles start first
     const int mp = a.n_mt, mps = a.n_mt_s;
-    const int nr = n_routed * mp;
+    const int ns = a.n_shared * mps;
     int j;
-    if (t < nr) {
-        ti.grp = a.groups[t / mp];
-        j = t % mp;
-        ti.shared = false;
-    } else {
-        const int t2 = t - nr;
-        if (t2 >= a.n_shared * mps) return false;
-        ti.grp = a.groups[a.max_routed + t2 / mps];
-        j = t2 % mps;
+    if (t < ns) {
+        ti.grp = a.groups[a.max_routed + t / mps];
+        j = t % mps;
         ti.shared = true;
+    } else {
+        const int t2 = t - ns;
+        if (t2 >= n_routed * mp) return false;
+        ti.grp = a.groups[t2 / mp];
+        j = t2 % mp;
+        ti.shared = false;
     }
     ti.mt = j;
     const QLayout &L = ti.shared ? a.src.LS : a.src.L;
