@@ -1007,6 +1007,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                     trow = XF32 ? ((g < 4) ? t : 4 + t) : t;
                 }
                 const BTile bt[1] = {{xs + (size_t)trow * ldx + 2 * c, valid}};
+                const Unpack un = shared ? a.un_s : a.un;  // in registers for the item's chunks
                 float acc[2][1][4] = {};
                 const uint8_t *pbase = nullptr;
                 int pnc = 0, pbytes = 0;
@@ -1027,7 +1028,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                         ring_pop(ring, pbytes);
                         produce();
                     }
-                    mma_chunk<KIND, 2, 1>(rg, half, bt, ch * 128, shared ? a.un_s : a.un, acc);
+                    mma_chunk<KIND, 2, 1>(rg, half, bt, ch * 128, un, acc);
                 }
                 // the group adds the S parts in part order (as the multi-kernel k_gateup)
 #pragma unroll
@@ -1150,7 +1151,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                 } else {
                     ncols = T;
                 }
-                const Unpack &un = shared ? a.un_s : a.un;
+                const Unpack un = shared ? a.un_s : a.un;  // in registers for the unit's chunks
                 // B tiles: columns nb*4 + (g & 3); lanes g < 4 read hi limbs, g >= 4 lo limbs
                 // staged: B rows in shared memory (the pointer provably shared, so the
                 // loads are shared-memory loads); otherwise h limbs in global memory
