@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
     // chunks per piece: two pieces of each kind fit in the ring at once; larger pieces
     // mean fewer bulk copies (the copy engine takes them one at a time)
     const int pcg_fit = a.geom.ring_bytes / (2 * L.gu_chunk_bytes);
-    const int pcg = pcg_fit < 1 ? 1 : (pcg_fit > 8 ? 8 : pcg_fit);
+    const int pcg2 = pcg_fit < 1 ? 1 : (pcg_fit > 8 ? 8 : pcg_fit);
     const int pcd_fit = a.geom.ring_bytes / (2 * L.d_chunk_bytes);
     const int pcd = pcd_fit < 1 ? 1 : (pcd_fit > 8 ? 8 : pcd_fit);
 
@@ -932,6 +932,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
         const int grp = warp / S_GU, q = warp % S_GU;
         const int n_ch = L.gu_chunks;  // the shared expert has the same H chunks
         const int cb0 = gu_chunk_begin(q, n_ch, S_GU), cb1 = gu_chunk_begin(q + 1, n_ch, S_GU);
+        // a group with one item this layer takes its part in one piece when it fits in
+        // three quarters of the ring (fewer copies to issue: the copy unit takes them one
+        // at a time); otherwise two pieces of each kind fit in the ring at once
+        const bool one_item = cta + G * (grp + NG) >= n_items;
+        const bool one_piece = one_item && cb1 > cb0 && (cb1 - cb0) * L.gu_chunk_bytes * 4 <= 3 * a.geom.ring_bytes;
+        const int pcg = one_piece ? cb1 - cb0 : pcg2;
         const int dw = kPWarps - 1 - warp;  // down units go to the last warps first
         auto gu_tile = [&](int j) -> const uint8_t * {
             if (j >= nU * tilesF) return Ly.shared + (long long)(j - nU * tilesF) * a.LS.gu_tile_bytes;
