@@ -672,25 +672,38 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
             // exceed. Each maximum is a distinct entry, so at least K entries reach
             // it and every top-K entry does. A warp ranks one maximum against all
             // (shared-memory broadcasts and a ballot: warp shuffles are slow here).
-            if (!all_cand) {
-                for (int t = 0; t < T; ++t) {
-                    const uint32_t *sm = segmax + t * kMaxSeg;
-                    for (int i = warp; i < nseg; i += kPWarps) {
-                        const uint32_t mi = sm[i];
-                        int rank = 0;
-                        for (int j = lane; j - lane < nseg; j += 32)
-                            rank += __popc(__ballot_sync(0xffffffffu, j < nseg && sm[j] > mi));
-                        if (lane == 0 && rank < K) atomicMin(&s.theta[t], mi);
+            // One token with at most 32 segments: every warp finds the threshold itself
+            // (lane i ranks maximum i against the others), so no barrier is needed
+            // before the candidates.
+            const bool warp_theta = T == 1 && nseg <= 32 && !all_cand;
+            uint32_t theta_w = 0u;
+            if (warp_theta) {
+                const uint32_t mine = lane < nseg ? segmax[lane] : 0u;
+                int rank = 0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) rank += (j < nseg) & (__shfl_sync(0xffffffffu, mine, j) > mine);
+                theta_w = __reduce_min_sync(0xffffffffu, (lane < nseg && rank < K) ? mine : 0xFFFFFFFFu);
+            } else {
+                if (!all_cand) {
+                    for (int t = 0; t < T; ++t) {
+                        const uint32_t *sm = segmax + t * kMaxSeg;
+                        for (int i = warp; i < nseg; i += kPWarps) {
+                            const uint32_t mi = sm[i];
+                            int rank = 0;
+                            for (int j = lane; j - lane < nseg; j += 32)
+                                rank += __popc(__ballot_sync(0xffffffffu, j < nseg && sm[j] > mi));
+                            if (lane == 0 && rank < K) atomicMin(&s.theta[t], mi);
+                        }
                     }
                 }
+                __syncthreads();
             }
-            __syncthreads();
             // (3) candidates: the entries at or above the threshold
             for (int b0 = 0; b0 < TE; b0 += kPersistThreads) {
                 if (b0 + warp * 32 >= TE) break;
                 const int idx = b0 + tid, t = tok(idx), e = idx - t * Ep;
                 const uint32_t o = ords[idx];
-                const bool c = e < E && o >= (all_cand ? 0u : s.theta[t]);
+                const bool c = e < E && o >= (all_cand ? 0u : warp_theta ? theta_w : s.theta[t]);
                 const unsigned bal = __ballot_sync(0xffffffffu, c);
                 int base = 0;
                 if (lane == 0 && bal) base = atomicAdd(&s.ncand[t], __popc(bal));
