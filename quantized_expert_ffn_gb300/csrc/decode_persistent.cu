@@ -113,13 +113,12 @@ struct Waiter {
     uint32_t *status;
     long long t0 = 0;
     unsigned it = 0;
-    // false: stop waiting. Between polls a thread sleeps, longer the longer it has
-    // waited (32 ns doubling to 512 ns): many SMs polling L2 without a pause slow
-    // down the very writes they wait for.
+    // false: stop waiting. Polls follow each other without a pause (sleeping between
+    // them, even for tens of nanoseconds, delayed the chain more than the polling
+    // traffic it saved).
     __device__ __forceinline__ bool keep_going() {
         if (it == 0) t0 = clock64();
         ++it;
-        __nanosleep(it < 5 ? 16u << it : 512u);
         if ((it & 15) == 0) {
             if (ld_relaxed_u32(stop)) return false;
             if (clock64() - t0 > kSpinCycles) {
