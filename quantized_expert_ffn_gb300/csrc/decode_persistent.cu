@@ -608,9 +608,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
             uint32_t *const segmax = ords + TE;                              // [kMaxTok][kMaxSeg]
             unsigned long long *const cand =
                 reinterpret_cast<unsigned long long *>(segmax + kMaxTok * kMaxSeg);  // [kMaxTok][kCandCap]
-            // segments of `seg` entries, at least 2K of them per token where kMaxSeg allows
+            // segments of `seg` entries, at least K + 2 of them per token where kMaxSeg allows
             int lseg = 5;
-            while (lseg > 0 && (Ep >> lseg) < 2 * K && (Ep >> (lseg - 1)) <= kMaxSeg) --lseg;
+            while (lseg > 0 && (Ep >> lseg) < K + 2 && (Ep >> (lseg - 1)) <= kMaxSeg) --lseg;
             const int seg = 1 << lseg, nseg = Ep >> lseg;
             const bool all_cand = E <= kCandCap;  // no threshold: every expert is a candidate
             const unsigned lt = (1u << lane) - 1u;
