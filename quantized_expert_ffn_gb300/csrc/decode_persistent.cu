@@ -13,7 +13,7 @@
 //      segment maxima is a threshold, the experts at or above it are ranked exactly;
 //      the distinct live experts and their columns; the split of the down work;
 //   GU gate/up items (16 rows of one expert, all of H) are dealt round-robin over
-//      CTAs and over the groups of S warps of a CTA (S = 4 for Q2, 8 for Q4); warp
+//      CTAs and over the groups of S warps of a CTA (S = 5 for Q2, 8 for Q4); warp
 //      q of a group sums part q of H; the group adds the parts in order, applies
 //      the activation, writes h and counts the item for its expert;
 //   D  down units (one expert x 16 output rows) in expert order, split over the
@@ -452,6 +452,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
     const int tab_ld = a.geom.tab_ld;
     constexpr int S_GU = GuSplit<KIND>::S;
     constexpr int NG = kPWarps / S_GU;  // gate/up warp groups per CTA
+    static_assert((size_t)NG * S_GU * 32 * 8 * sizeof(float) <= kRedBytes, "gate/up reduction scratch");
     const QLayout &L = a.L;
     const int dt = L.d_tiles;  // output row tiles (the shared expert has the same)
 
@@ -941,7 +942,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
         const int n_items = nU * tilesF + tilesS;
         const int j0 = s.misc[12], j1 = s.misc[13];
         // ------------------------------------------------ weight copies of this warp
+        // gate/up groups of S warps; warps past NG * S (16 % S of them) take no gate/up
+        // work (they would be a group short of S warps at its named barrier)
         const int grp = warp / S_GU, q = warp % S_GU;
+        const bool gu_warp = grp < NG;
         const int n_ch = L.gu_chunks;  // the shared expert has the same H chunks
         const int cb0 = gu_chunk_begin(q, n_ch, S_GU), cb1 = gu_chunk_begin(q + 1, n_ch, S_GU);
         // a group with one item this layer takes its part in one piece when it fits in
@@ -969,7 +973,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
                         pch = cb0;
                     }
                     const int j = cta + G * (grp + NG * pm);
-                    if (cb0 >= cb1 || j >= n_items) {
+                    if (!gu_warp || cb0 >= cb1 || j >= n_items) {
                         pphase = 1;
                         continue;
                     }
@@ -1002,7 +1006,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) k_decode(const __grid_cons
         // ------------------------------------------------ GU: gate/up + activation
         {
             float *gred = red + (size_t)grp * S_GU * 32 * 8;
-            for (int m = 0;; ++m) {
+            for (int m = 0; gu_warp; ++m) {
                 const int j = cta + G * (grp + NG * m);
                 if (j >= n_items) break;
                 const bool shared = j >= nU * tilesF;
