@@ -13,7 +13,7 @@
 //      segment maxima is a threshold, the experts at or above it are ranked exactly;
 //      the distinct live experts and their columns; the split of the down work;
 //   GU gate/up items (16 rows of one expert, all of H) are dealt round-robin over
-//      CTAs and over the groups of S warps of a CTA (S = 5 for Q2, 8 for Q4); warp
+//      CTAs and over the groups of S warps of a CTA (S = 5 for Q2, 4 for Q4); warp
 //      q of a group sums part q of H; the group adds the parts in order, applies
 //      the activation, writes h and counts the item for its expert;
 //   D  down units (one expert x 16 output rows) in expert order, split over the
