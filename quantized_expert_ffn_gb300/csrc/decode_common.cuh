@@ -142,16 +142,20 @@ __device__ __forceinline__ void mma_chunk(const ChunkRegs<KIND> (&r)[NMAT], bool
 
 // The canonical split of a gate/up row tile's chunks into parts: part w sums
 // chunks [w*n/S, (w+1)*n/S) and the S partial sums are added in part order
-// (((p0 + p1) + p2) + ...). S = 5 for Q2 (1,152-byte chunks; four chunks per part
-// at H = 2560, and three groups of five warps per 16-warp CTA) and 4 for Q4
-// (2,304-byte chunks; five or six per part at H = 2816, and four groups of four
-// warps per CTA: 608 groups on 152 SMs take a one-token window's 484 row tiles of
-// the Gemma-shaped layer in one round, where groups of eight took two).
+// (((p0 + p1) + p2) + ...). S = 4 for both formats: four groups of four warps per
+// 16-warp CTA, 608 groups on 152 SMs, so every row tile of a one-token window has a
+// group of its own (400 for the H=2560, E=512, top-10 layer; 484 for the
+// Gemma-shaped layer with its shared expert) and the busy warps spread evenly over
+// an SM's four sub-partitions. A part is five chunks at H = 2560 (Q2, 1,152 bytes
+// each) and five or six at H = 2816 (Q4, 2,304 bytes each).
 template <int KIND>
 struct GuSplit {
-    static constexpr int S = KIND == MOE_Q2_64 ? 5 : 4;
+    static constexpr int S = 4;
 };
-__host__ __device__ __forceinline__ int gu_split(int kind) { return kind == MOE_Q2_64 ? 5 : 4; }
+__host__ __device__ __forceinline__ int gu_split(int kind) {
+    (void)kind;
+    return 4;
+}
 __device__ __forceinline__ int gu_chunk_begin(int w, int n, int S) { return w * n / S; }
 
 // bf16 hi/lo limbs of an fp32 value

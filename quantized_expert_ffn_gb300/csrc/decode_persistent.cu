@@ -13,9 +13,9 @@
 //      segment maxima is a threshold, the experts at or above it are ranked exactly;
 //      the distinct live experts and their columns; the split of the down work;
 //   GU gate/up items (16 rows of one expert, all of H) are dealt round-robin over
-//      CTAs and over the groups of S warps of a CTA (S = 5 for Q2, 4 for Q4); warp
-//      q of a group sums part q of H; the group adds the parts in order, applies
-//      the activation, writes h and counts the item for its expert;
+//      CTAs and over the groups of S = 4 warps of a CTA; warp q of a group sums
+//      part q of H; the group adds the parts in order, applies the activation,
+//      writes h and counts the item for its expert;
 //   D  down units (one expert x 16 output rows) in expert order, split over the
 //      CTAs so that gate/up plus down bytes are even, then over the CTA's warps; a
 //      CTA waits only until the gate/up items of its own units' experts are
