@@ -270,14 +270,20 @@ __global__ void __launch_bounds__(kBucketThreads) k_bucket_count(const int32_t *
     for (int e = tid; e < E; e += blockDim.x) cc[(size_t)c * E + e] = sm[e];
 }
 
-// Totals, offsets and active experts; cc[c][e] becomes the number of expert-e
-// pairs in chunks before c.
-__global__ void __launch_bounds__(kBucketThreads) k_bucket_scan(int C, int E, int32_t *cc, int32_t *counts,
-                                                                int32_t *offsets, int32_t *active,
-                                                                int32_t *n_active) {
+// Stable placement of chunk c (the in-chunk rank as in k_bucket). The scan is
+// folded in: expert e's base in chunk c is its offset (exclusive scan of the
+// totals) plus its pairs in the chunks before c, which every CTA sums from the
+// per-chunk histograms; CTA 0 also writes the totals, offsets and active experts.
+__global__ void __launch_bounds__(kBucketThreads) k_bucket_place(const int32_t *__restrict__ ids, int P, int E, int C,
+                                                                 const int32_t *__restrict__ cc, int32_t *counts,
+                                                                 int32_t *offsets, int32_t *active, int32_t *n_active,
+                                                                 int32_t *perm) {
+    extern __shared__ int sm[];
     __shared__ int scr[64];
-    const int tid = threadIdx.x;
-    int run = 0;
+    int *base = sm;       // [E]
+    int *wt = base + E;   // [32][E]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, c = blockIdx.x;
+    int before = 0, run = 0;  // expert tid: pairs in the chunks before c, in all chunks
     if (tid < E) {
         // batches of 8 chunks: the loads of a batch are in flight together
         for (int c0 = 0; c0 < C; c0 += 8) {
@@ -286,34 +292,26 @@ __global__ void __launch_bounds__(kBucketThreads) k_bucket_scan(int C, int E, in
             for (int j = 0; j < 8; ++j) v[j] = c0 + j < C ? cc[(size_t)(c0 + j) * E + tid] : 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                if (c0 + j < C) cc[(size_t)(c0 + j) * E + tid] = run;
+                if (c0 + j == c) before = run;
                 run += v[j];
             }
         }
     }
     int total;
     const int pre = block_exclusive_scan(tid < E ? run : 0, &total, scr);
-    if (tid < E) {
-        counts[tid] = run;
-        offsets[tid] = pre;
+    if (tid < E) base[tid] = pre + before;
+    if (c == 0) {
+        if (tid < E) {
+            counts[tid] = run;
+            offsets[tid] = pre;
+        }
+        if (tid == 0) offsets[E] = total;
+        const int act = (tid < E && run > 0) ? 1 : 0;
+        int nact;
+        const int apos = block_exclusive_scan(act, &nact, scr);
+        if (act) active[apos] = tid;
+        if (tid == 0) *n_active = nact;
     }
-    if (tid == 0) offsets[E] = total;
-    const int act = (tid < E && run > 0) ? 1 : 0;
-    int nact;
-    const int apos = block_exclusive_scan(act, &nact, scr);
-    if (act) active[apos] = tid;
-    if (tid == 0) *n_active = nact;
-}
-
-// Stable placement of chunk c (the in-chunk rank as in k_bucket).
-__global__ void __launch_bounds__(kBucketThreads) k_bucket_place(const int32_t *__restrict__ ids, int P, int E,
-                                                                 const int32_t *cc, const int32_t *offsets,
-                                                                 int32_t *perm) {
-    extern __shared__ int sm[];
-    int *base = sm;       // [E]
-    int *wt = base + E;   // [32][E]
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, c = blockIdx.x;
-    for (int e = tid; e < E; e += blockDim.x) base[e] = offsets[e] + cc[(size_t)c * E + e];
     for (int i = tid; i < 32 * E; i += blockDim.x) wt[i] = 0;
     __syncthreads();
     const int p = c * kBucketThreads + tid;
@@ -324,11 +322,11 @@ __global__ void __launch_bounds__(kBucketThreads) k_bucket_place(const int32_t *
     if (e >= 0 && rank == 0) wt[warp * E + e] = __popc(same);
     __syncthreads();
     for (int ee = tid; ee < E; ee += blockDim.x) {
-        int run = base[ee];
+        int r = base[ee];
         for (int w = 0; w < 32; ++w) {
             const int n = wt[w * E + ee];
-            wt[w * E + ee] = run;
-            run += n;
+            wt[w * E + ee] = r;
+            r += n;
         }
     }
     __syncthreads();
@@ -336,11 +334,15 @@ __global__ void __launch_bounds__(kBucketThreads) k_bucket_place(const int32_t *
 }
 
 // Plan, pass 1 (one CTA per 1,024 bucket positions): liveness of the pair at
-// each position, live pairs per expert (lc) and per CTA (blk); pairs whose id is
-// out of range (not in the buckets) are marked dead by their own index.
-__global__ void __launch_bounds__(kBucketThreads) k_plan_live(PlanArgs a, int32_t *lc, int32_t *blk) {
+// each position, the CTA's live pairs per expert (lcb[c][e]) and in all (blk[c]);
+// pairs whose id is out of range (not in the buckets) are marked dead by their
+// own index.
+__global__ void __launch_bounds__(kBucketThreads) k_plan_live(PlanArgs a, int32_t *lcb, int32_t *blk) {
+    extern __shared__ int hl[];  // [E]
     const int tid = threadIdx.x, i = blockIdx.x * kBucketThreads + tid;
     const int P = a.T * a.K, E = a.E;
+    for (int e = tid; e < E; e += blockDim.x) hl[e] = 0;
+    __syncthreads();
     const int nb = a.offsets[E];
     bool absent = false, oob = false;
     int live = 0, e = -1;
@@ -361,25 +363,47 @@ __global__ void __launch_bounds__(kBucketThreads) k_plan_live(PlanArgs a, int32_
         }
     }
     const unsigned same = __match_any_sync(0xffffffffu, live ? e : -1);
-    if (live && (same & ((1u << (tid & 31)) - 1)) == 0) atomicAdd(&lc[e], __popc(same));
+    if (live && (same & ((1u << (tid & 31)) - 1)) == 0) atomicAdd(&hl[e], __popc(same));
     const int n = __syncthreads_count(live);
+    for (int ee = tid; ee < E; ee += blockDim.x) lcb[(size_t)blockIdx.x * E + ee] = hl[ee];
     if (tid == 0) blk[blockIdx.x] = n;
     if (__syncthreads_or(absent) && tid == 0) set_status(a.status, MOE_STATUS_EXPERT_ABSENT);
     if (__syncthreads_or(oob) && tid == 0) set_status(a.status, MOE_STATUS_BOUNDS);
 }
 
-// Plan, pass 2 (one CTA): column bases of the position blocks and of the
-// experts, the groups, the group counts and the shared expert's columns/groups.
-__global__ void __launch_bounds__(kBucketThreads) k_plan_groups(PlanArgs a, int nblk, const int32_t *lc,
-                                                                int32_t *blk) {
+// Plan, pass 2 (one CTA per 1,024 bucket positions): the live pairs in bucket
+// order are the routed plan columns, after the live pairs of the CTAs before.
+// CTA 0 also sums the live pairs per expert, builds the groups and the group
+// counts, and writes the shared expert's columns and groups.
+__global__ void __launch_bounds__(kBucketThreads) k_plan_cols(PlanArgs a, int nblk, const int32_t *lcb,
+                                                              const int32_t *blk) {
     __shared__ int scr[64];
-    const int tid = threadIdx.x, E = a.E;
+    __shared__ int cta_base;
+    const int tid = threadIdx.x, i = blockIdx.x * kBucketThreads + tid, E = a.E;
     int nlive;
-    const int bl = tid < nblk ? blk[tid] : 0;
-    const int bb = block_exclusive_scan(bl, &nlive, scr);
-    if (tid < nblk) blk[tid] = bb;
-    const int my_lc = tid < E ? lc[tid] : 0;
+    const int bb = block_exclusive_scan(tid < nblk ? blk[tid] : 0, &nlive, scr);
+    if (tid == (int)blockIdx.x) cta_base = bb;  // blockIdx.x < nblk <= blockDim.x
+    __syncthreads();
+    const int nb = a.offsets[E];
+    int p = -1, live = 0;
+    if (i < nb) {
+        p = a.perm[i];
+        live = a.live[p];
+    }
     int dummy;
+    const int pre = block_exclusive_scan(live, &dummy, scr);
+    if (live) a.cols[cta_base + pre] = p;
+    if (blockIdx.x != 0) return;
+    int my_lc = 0;
+    if (tid < E) {
+        for (int c0 = 0; c0 < nblk; c0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = c0 + j < nblk ? lcb[(size_t)(c0 + j) * E + tid] : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) my_lc += v[j];
+        }
+    }
     const int my_cs = block_exclusive_scan(my_lc, &dummy, scr);
     int tot_gu, tot_d;
     const int slot = (tid < E && my_lc > 0) ? a.table[(size_t)a.layer * E + tid] : -1;
@@ -400,22 +424,6 @@ __global__ void __launch_bounds__(kBucketThreads) k_plan_groups(PlanArgs a, int 
     }
 }
 
-// Plan, pass 3 (one CTA per 1,024 bucket positions): the live pairs in bucket
-// order are the routed plan columns.
-__global__ void __launch_bounds__(kBucketThreads) k_plan_cols(PlanArgs a, const int32_t *blk) {
-    __shared__ int scr[64];
-    const int tid = threadIdx.x, i = blockIdx.x * kBucketThreads + tid;
-    const int nb = a.offsets[a.E];
-    int p = -1, live = 0;
-    if (i < nb) {
-        p = a.perm[i];
-        live = a.live[p];
-    }
-    int dummy;
-    const int pre = block_exclusive_scan(live, &dummy, scr);
-    if (live) a.cols[blk[blockIdx.x] + pre] = p;
-}
-
 }  // namespace
 
 int launch_bucket(const int32_t *ids, int T, int K, int E, int32_t *counts, int32_t *offsets, int32_t *perm,
@@ -433,10 +441,11 @@ int init_bucket_attributes(int max_smem) {
     return rc;
 }
 
+// The bucket's per-chunk histograms, then (reusing the same ints) the plan's
+// per-CTA live counts per expert and per CTA.
 size_t wide_scratch_bytes(int T, int K, int E) {
     const size_t C = ((size_t)T * K + kBucketThreads - 1) / kBucketThreads;
-    const size_t a = C * (size_t)E, b = (size_t)E + 2 * C;
-    return (a > b ? a : b) * sizeof(int32_t);
+    return (C * (size_t)E + C) * sizeof(int32_t);
 }
 
 bool use_wide(int T, int K) {
@@ -449,22 +458,18 @@ int launch_bucket_wide(const int32_t *ids, int T, int K, int E, int32_t *counts,
     const int P = T * K, C = (P + kBucketThreads - 1) / kBucketThreads;
     k_bucket_count<<<C, kBucketThreads, (size_t)E * sizeof(int), s>>>(ids, P, E, scratch, status);
     MOE_CUDA_TRY(cudaGetLastError());
-    k_bucket_scan<<<1, kBucketThreads, 0, s>>>(C, E, scratch, counts, offsets, active, n_active);
-    MOE_CUDA_TRY(cudaGetLastError());
-    k_bucket_place<<<C, kBucketThreads, (size_t)33 * E * sizeof(int), s>>>(ids, P, E, scratch, offsets, perm);
+    k_bucket_place<<<C, kBucketThreads, (size_t)33 * E * sizeof(int), s>>>(ids, P, E, C, scratch, counts, offsets,
+                                                                           active, n_active, perm);
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }
 
 int launch_plan_wide(const PlanArgs &a, int32_t *scratch, cudaStream_t s) {
     const int P = a.T * a.K, C = (P + kBucketThreads - 1) / kBucketThreads;
-    int32_t *lc = scratch, *blk = scratch + a.E;
-    MOE_CUDA_TRY(cudaMemsetAsync(lc, 0, (size_t)a.E * sizeof(int32_t), s));
-    k_plan_live<<<C, kBucketThreads, 0, s>>>(a, lc, blk);
+    int32_t *lcb = scratch, *blk = scratch + (size_t)C * a.E;
+    k_plan_live<<<C, kBucketThreads, (size_t)a.E * sizeof(int32_t), s>>>(a, lcb, blk);
     MOE_CUDA_TRY(cudaGetLastError());
-    k_plan_groups<<<1, kBucketThreads, 0, s>>>(a, C, lc, blk);
-    MOE_CUDA_TRY(cudaGetLastError());
-    k_plan_cols<<<C, kBucketThreads, 0, s>>>(a, blk);
+    k_plan_cols<<<C, kBucketThreads, 0, s>>>(a, C, lcb, blk);
     MOE_CUDA_TRY(cudaGetLastError());
     return MOE_OK;
 }
